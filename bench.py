@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step (KV append + plan + decode + combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3_8b] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
+one batch: kv_append of the step's new K/V row per sequence (at position
+L_b - 1), then paged_decode_plan, paged_decode_run and paged_decode_combine,
+all through the C ABI on one CUDA stream.
+
+value      = algorithmic bytes of the step / device time of the step, GB/s:
+             unique K+V bytes read + q read + out written + append bytes
+             (k_new/v_new read and written into the pool).
+e2e        = the same metric through paged_decode_attention / kv_append with
+             the step's inputs (q, k_new, v_new, page table, lengths,
+             positions) copied from pinned host memory each step and the
+             output copied back, all inside the timed region.
+roofline   = the decode kernel alone: its algorithmic bytes (K+V+q+out) over
+             its event-timed duration, against the measured HBM copy peak.
+cpu_baseline = the float64 oracle on the host cores, on a bounded sample.
+
+--impl reference times the oracle itself as the reference arm (same metric,
+workload and unit, each step a bounded sample).
+
+Multi-GPU: the path does not exchange data between GPUs; N>1 runs N
+independent replicas (one per rank) and reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attn: achieved HBM GB/s (% of peak) and decode seqs/s"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["paged_kv_decode_16_gb300/csrc/decode.cuh",
+                  "paged_kv_decode_16_gb300/csrc/common.cuh"]
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama3_8b_shape.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-workers", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha")):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != decode_source_hash():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t_start = self.t_end = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.wall = []
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 10:
+                continue
+            rec = [x.strip() for x in rec]
+            try:
+                ts = time.mktime(time.strptime(rec[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except Exception:
+                ts = None
+            rows.append((ts, rec))
+        # samples inside the timed region (1 s slack for the timestamp granularity)
+        inside = [r for ts, r in rows
+                  if ts is not None and self.t_start is not None
+                  and self.t_start - 1.0 <= ts <= self.t_end + 1.0]
+        use = inside or [r for _, r in rows]
+        sm = []
+        smax = None
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            try:
+                sm.append(float(r[2]))
+                smax = float(r[3])
+            except ValueError:
+                pass
+            for name, val in zip(names, r[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(use),
+                "samples_in_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+def step_bytes(w) -> dict:
+    kv = w.kv_bytes_unique()
+    qo = w.qo_bytes()
+    app = w.append_bytes()
+    return {"kv_unique": kv, "kv_logical": w.kv_bytes_logical(), "qo": qo, "append": app,
+            "step": kv + qo + app, "decode": kv + qo}
+
+
+def copy_peak_gbs(torch, dev) -> float:
+    """Same-run device copy bandwidth (read + write bytes), 1 GiB bf16, best of 10."""
+    n = 1 << 29
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = float("inf")
+    for _ in range(12):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        b.copy_(a)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    del a, b
+    return 2 * n * 2 / (best * 1e-3) / 1e9
+
+
+def cpu_oracle_sample(w, target_s: float = 12.0):
+    """Time the oracle on host copies of the workload: whole batches while they
+    fit in the budget, otherwise sequences one by one (all query heads)."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_decode_16_gb300 import workloads as wl
+
+    q = wl.to_bits(w.q)
+    kp, vp = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
+    cores = oracle.max_threads()
+    per_tok = w.n_kv_heads * w.head_dim * 4
+    seqs = 0
+    nbytes = 0
+    t0 = time.perf_counter()
+    order = np.random.default_rng(0).permutation(w.batch)
+    i = 0
+    while time.perf_counter() - t0 < target_s and seqs < 100 * w.batch:
+        b = int(order[i % w.batch])
+        i += 1
+        rows = np.array([(b, h) for h in range(w.n_q_heads)], dtype=np.int32)
+        oracle.paged_decode_rows(q, kp, vp, w.page_table, w.context_lens, w.scale, w.dtype_name,
+                                 rows)
+        seqs += 1
+        nbytes += int(w.context_lens[b]) * per_tok + 2 * w.n_q_heads * w.head_dim * 2
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "seqs_per_s": seqs / dt,
+            "sample": f"{seqs} sequences x all {w.n_q_heads} query heads of the {w.name} "
+                      f"workload, float64 oracle with OpenMP over query heads, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    """Reference arm: the float64 oracle on the host cores, same metric/unit."""
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401  (workload tensors live on the CPU here)
+
+    from paged_kv_decode_16_gb300 import workloads as wl
+    w = wl.make(args.workload, seed=args.seed, device="cpu")
+    if w.append:
+        import oracle
+        kp, vp = oracle.kv_append(wl.to_bits(w.k_pool), wl.to_bits(w.v_pool),
+                                  wl.to_bits(w.k_new), wl.to_bits(w.v_new), w.page_table,
+                                  w.positions)
+        w.k_pool = torch.from_numpy(kp.view("int16")).view(w.dtype)
+        w.v_pool = torch.from_numpy(vp.view("int16")).view(w.dtype)
+    budget = max(0.05, min(12.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, target_s=budget)
+    vals, seqs = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(w, target_s=budget)
+        vals.append(r["value"])
+        seqs.append(r["seqs_per_s"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals) if vals else 0.0
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wall / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+                   "storage_dtype": w.dtype_name, "seed": args.seed},
+        "seqs_per_s": statistics.mean(seqs) if seqs else 0.0,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"] if vals else None,
+                         "kind": "oracle", "sample": r["sample"] if vals else ""},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import paged_kv_decode_16_gb300 as pkv
+    from paged_kv_decode_16_gb300 import workloads as wl
+
+    world, rank, local = dist_info()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+
+    w = wl.make(args.workload, seed=args.seed, device=dev)
+    B = w.batch
+    table = torch.from_numpy(w.page_table).to(dev)
+    lens = torch.from_numpy(w.context_lens).to(dev)
+    pos = torch.from_numpy(w.positions).to(dev)
+    pool = pkv.kv_pool_create(w.num_pages, w.page_size, w.n_kv_heads, w.head_dim, w.dtype,
+                              w.k_pool, w.v_pool)
+    out = torch.empty_like(w.q)
+    nw = args.num_workers
+    ws = pkv.alloc_workspace(B, w.n_q_heads, w.n_kv_heads, w.head_dim, nw, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    by = step_bytes(w)
+
+    def step(ev0=None, ev1=None):
+        pkv.kv_append(pool, w.k_new, w.v_new, table, pos)
+        pkv.paged_decode_plan(lens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size,
+                              table.shape[1], ws, nw)
+        if ev0 is not None:
+            ev0.record(stream)
+        pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, out, ws, nw)
+        if ev1 is not None:
+            ev1.record(stream)
+        pkv.paged_decode_combine(out, w.n_kv_heads, ws, nw)
+
+    peak, peak_kind = measured_peak()
+    same_run_copy = copy_peak_gbs(torch, dev)
+    sampler = ClockSampler(local)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pkv.pkv_read_device_status(ws):
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    t_start.record(stream)
+    for i in range(K):
+        step(dec0[i], dec1[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in zip(dec0, dec1)]
+    ms_step = total_ms / K
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    dec_avg = statistics.mean(dec_ms)
+    clocks = sampler.finish()
+
+    # ---- end to end through host buffers (pinned), one sync per step ----
+    q_h = w.q.cpu().pin_memory()
+    kn_h, vn_h = w.k_new.cpu().pin_memory(), w.v_new.cpu().pin_memory()
+    tb_h = table.cpu().pin_memory()
+    ln_h, ps_h = lens.cpu().pin_memory(), pos.cpu().pin_memory()
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    q_d, kn_d, vn_d = torch.empty_like(w.q), torch.empty_like(w.k_new), torch.empty_like(w.v_new)
+    tb_d, ln_d, ps_d = torch.empty_like(table), torch.empty_like(lens), torch.empty_like(pos)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, tb_h, ln_h, ps_h))
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        for dst, src in ((q_d, q_h), (kn_d, kn_h), (vn_d, vn_h), (tb_d, tb_h), (ln_d, ln_h),
+                         (ps_d, ps_h)):
+            dst.copy_(src, non_blocking=True)
+        pkv.kv_append(pool, kn_d, vn_d, tb_d, ps_d)
+        pkv.paged_decode_attention(q_d, w.k_pool, w.v_pool, tb_d, ln_d, w.scale, out, ws, nw)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(10):
+        e2e_step()
+    KE = max(1, min(args.e2e_steps, K))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(KE):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / KE
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    status = pkv.pkv_read_device_status(ws)
+
+    value = world * by["step"] / (ms_step * 1e-3) / 1e9
+    achieved = by["decode"] / (dec_avg * 1e-3) / 1e9
+    traffic = traffic_from_profile()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype_name, "data": "synthetic",
+        "config": {
+            "workload": args.workload, "batch": B, "n_q_heads": w.n_q_heads,
+            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+            "context_lens": f"uniform [512, 4096], mean {float(w.context_lens.mean()):.0f}"
+            if args.workload == "llama3_8b" else f"mean {float(w.context_lens.mean()):.0f}",
+            "seed": args.seed, "num_workers": nw or "auto",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": (f"inputs larger than L2: {by['kv_unique'] / 2**20:.0f} MiB of K/V per step "
+                   f"vs 129 MB L2; no flush") if by["kv_unique"] > L2_BYTES
+            else "inputs smaller than L2 (warm numbers)",
+            "step": "kv_append + paged_decode_plan + paged_decode_run + paged_decode_combine",
+        },
+        "seqs_per_s": world * B / (ms_step * 1e-3),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "bytes_per_step": by,
+        "decode_kernel_ms": dec_avg,
+        "same_run_copy_gbs": same_run_copy,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "pkv::decode_kernel", "algorithmic_bytes": by["decode"]},
+        "e2e": {"value": world * by["step"] / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": KE},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w)
+    elif rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line))
+    pool.destroy()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,254 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV decode library.
+ *
+ * One decode step of grouped-query attention (GQA) for a batch of sequences,
+ * each with exactly one new query token, over a KV cache stored in fixed-size
+ * pages that sequences reach through their own page-table rows (rows may share
+ * pages, e.g. a common prompt prefix), plus the append of the step's new K/V
+ * rows into the page pool.
+ *
+ * Where the operations are defined (page title, section):
+ *   - CacheIR, "Compiler Example": the decode graph lowers attention into
+ *     fused_rmsnorm_qkv_rope followed by paged_attention_decode over the cached
+ *     keys and values.
+ *   - CacheIR, "Current Capabilities" (Runtime row) and "Boundaries":
+ *     persistent shared page-backed KV pools, batched decode over shared page
+ *     tables, multi-batch page-table decode attention with GQA mapping, a
+ *     batched paged-attention ABI and a reduced paged-attention decode.
+ *   - TorchInferno, "Runtime Scaffolds": runtime.paged (page-table KV allocation
+ *     and materialization) and runtime.paged_attention (the paged attention
+ *     reference); "Custom Kernels": paged_decode_attention and
+ *     batched_paged_decode_attention; "OpenAI-Compatible Serving" knob list:
+ *     KV-append, grouped and streaming (block-S) decode attention kernels.
+ *   - Experimental LibTorch prefix cache, "Identity, ownership and output
+ *     behavior": stream-ordered work, caller-owned lifetimes, host-side
+ *     validation before launch and rejection of aliased output storage.
+ *
+ * Math (the plain reading; the pages print no formula): for sequence b with
+ * context length L_b and query head hq,
+ *     s_t = scale * <q[b][hq], k_t>,       t = 0 .. L_b - 1
+ *     out[b][hq] = sum_t softmax(s)_t * v_t     (out = 0 when L_b = 0)
+ * where k_t, v_t are row (t % P) of page page_table[b][t / P] for KV head
+ * hq / (n_q_heads / n_kv_heads).  Arithmetic is fp32 with fp16/bf16 inputs;
+ * the output is rounded to the input dtype (round to nearest even).
+ *
+ * Conventions for every call
+ * --------------------------
+ *   Pointers marked (device) are CUDA device pointers owned by the caller; the
+ *   library never frees them and keeps no reference after the call returns
+ *   (except pools created with borrowed memory, see kv_pool_create).  Pointers
+ *   marked (host) are ordinary host memory.  All device work is enqueued on
+ *   `stream` (a cudaStream_t; NULL = the legacy default stream) and nothing
+ *   synchronises the host except pkv_read_device_status.
+ *   Layouts (row-major, contiguous):
+ *     q, out          [batch][n_q_heads][head_dim]
+ *     k_pool, v_pool  [num_pages][n_kv_heads][page_size][head_dim]
+ *     page_table      int32 [batch][table_stride]   (entries past the pages a
+ *                                                    sequence uses are ignored)
+ *     context_lens    int32 [batch]   tokens attended, including the new one
+ *     k_new, v_new    [batch][n_kv_heads][head_dim]
+ *     positions       int32 [batch]   slot written by the append; < 0 = skip
+ *                                     (a padded batch slot never writes)
+ *   Supported: dtype fp16 or bf16 (q, pools, out all the same); head_dim 64 or
+ *   128; page_size a multiple of 16, at most 256; n_q_heads a multiple of
+ *   n_kv_heads; every device pointer 16-byte aligned.
+ *   Errors: argument errors are found on the host before anything is enqueued
+ *   and returned as a pkv_status; nothing is launched then.  Errors that depend
+ *   on device data (a page id outside [0, num_pages), a context length beyond
+ *   table_stride * page_size) are found by the kernels, which skip the bad
+ *   access and set bits in a device status word (PKV_DEV_*).  No kernel traps,
+ *   asserts or waits without a bound.  No C++ exception crosses this ABI.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size or shape */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, page_size, dtype */
+    PKV_ERR_ALIAS = 3,         /* out overlaps an input */
+    PKV_ERR_OUT_OF_PAGES = 4,  /* allocator has too few free pages */
+    PKV_ERR_WORKSPACE = 5,     /* workspace missing, too small or misaligned */
+    PKV_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+    PKV_ERR_DEVICE_CHECK = 7,  /* pkv_read_device_status found a set bit */
+    PKV_ERR_REFCOUNT = 8       /* retain/release of a page that is not allocated */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits of the device status word. */
+#define PKV_DEV_BAD_PAGE 0x1u   /* a page id outside [0, num_pages) was skipped */
+#define PKV_DEV_BAD_LEN  0x2u   /* a length/position beyond the table row was clamped/skipped */
+#define PKV_DEV_TIMEOUT  0x4u   /* a bounded wait on a copy gave up (copy never landed) */
+
+typedef struct CUstream_st* pkv_stream; /* same type as cudaStream_t */
+typedef struct pkv_pool pkv_pool;       /* opaque */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* pkv_status_string(pkv_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Page pool and host page allocator
+ * (CacheIR, "Current Capabilities": persistent shared CUDA page-backed KV
+ *  pools; "Boundaries": shared KV page allocator accounting across forked
+ *  request sessions; TorchInferno, "Runtime Scaffolds": runtime.paged).
+ * ------------------------------------------------------------------------ */
+
+/* Create a pool of num_pages pages, each [n_kv_heads][page_size][head_dim].
+ * k_pool / v_pool (device): both NULL -> the pool allocates (cudaMalloc) and
+ * owns the memory; both non-NULL -> the pool borrows them (they must stay
+ * alive until kv_pool_destroy).  *out receives the handle.  The host
+ * allocator starts with every page free.  Errors: INVALID_ARG, UNSUPPORTED,
+ * CUDA (allocation failed). */
+pkv_status kv_pool_create(int num_pages, int page_size, int n_kv_heads, int head_dim,
+                          pkv_dtype dtype, void* k_pool, void* v_pool, pkv_pool** out);
+
+/* Free the handle (and the memory, if owned).  NULL is accepted.  The caller
+ * must make sure no enqueued work still uses owned memory. */
+pkv_status kv_pool_destroy(pkv_pool* pool);
+
+/* Device base addresses of the K and V pools (NULL for a NULL handle). */
+void* kv_pool_k(const pkv_pool* pool);
+void* kv_pool_v(const pkv_pool* pool);
+
+/* Take n free pages (all or nothing); ids_out (host) receives n page ids, each
+ * with reference count 1.  Errors: INVALID_ARG, OUT_OF_PAGES (nothing taken).
+ * Thread-safe. */
+pkv_status kv_pool_alloc_pages(pkv_pool* pool, int n, int32_t* ids_out);
+
+/* Add one reference to each listed page (sharing a prefix page with another
+ * sequence).  ids (host).  All ids are checked first; on REFCOUNT or
+ * INVALID_ARG nothing changes.  Thread-safe. */
+pkv_status kv_pool_retain_pages(pkv_pool* pool, const int32_t* ids, int n);
+
+/* Drop one reference from each listed page; a page whose count reaches zero
+ * returns to the free list.  All ids are checked first (an id listed more
+ * times than its count, or a free page, is REFCOUNT and nothing changes).
+ * Thread-safe. */
+pkv_status kv_pool_release_pages(pkv_pool* pool, const int32_t* ids, int n);
+
+/* Number of free pages; -1 for a NULL handle. */
+int kv_pool_free_count(const pkv_pool* pool);
+
+/* Reference count of one page (0 = free); -1 for a bad handle or id. */
+int kv_pool_refcount(const pkv_pool* pool, int32_t page_id);
+
+/* Pool geometry (any output pointer may be NULL). */
+pkv_status kv_pool_info(const pkv_pool* pool, int* num_pages, int* page_size,
+                        int* n_kv_heads, int* head_dim, pkv_dtype* dtype);
+
+/* ------------------------------------------------------------------------
+ * Per-step KV append
+ * (TorchInferno, "OpenAI-Compatible Serving" knob list: KV-append kernel;
+ *  CacheIR, "Compiler Example": the new K/V are written before the paged
+ *  decode; TorchInferno, "Quickstart": a padded slot must never alias a live
+ *  KV row).
+ * ------------------------------------------------------------------------ */
+
+/* For every b with positions[b] >= 0 and every KV head h, copy k_new[b][h][:]
+ * and v_new[b][h][:] bit for bit into row positions[b] % page_size of page
+ * page_table[b][positions[b] / page_size].  k_new, v_new, page_table,
+ * positions (device).  dev_status (device, nullable): a uint32 that receives
+ * PKV_DEV_BAD_PAGE / PKV_DEV_BAD_LEN bits (ORed in) for skipped rows.
+ * Distinct sequences must not append into the same (page, slot).  One kernel
+ * launch; batch = 0 launches nothing. */
+pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
+                     const int32_t* page_table, int table_stride, const int32_t* positions,
+                     int batch, uint32_t* dev_status, pkv_stream stream);
+
+/* Materialize each sequence's cached rows as a dense block:
+ * k_out[b][h][t][:] = k_pool[page_table[b][t / P]][h][t % P][:] (and v) for
+ * t < min(context_lens[b], max_len); other rows of k_out/v_out are not
+ * written.  k_out, v_out [batch][n_kv_heads][max_len][head_dim] (device).
+ * Bit copy (TorchInferno, "Runtime Scaffolds": runtime.paged
+ * materialization).  dev_status as for kv_append. */
+pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_stride,
+                     const int32_t* context_lens, int batch, int max_len, void* k_out,
+                     void* v_out, uint32_t* dev_status, pkv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Decode attention
+ * (CacheIR, "Boundaries": multi-batch page-table decode attention with GQA
+ *  mapping, reduced paged-attention decode; TorchInferno, "Custom Kernels":
+ *  paged_decode_attention / batched_paged_decode_attention, and the
+ *  grouped and streaming block-S decode variants in the serving knob list.)
+ *
+ * Work split: every (sequence, KV head) is cut into chunks of 16 tokens; the
+ * chunks of the whole batch are laid end to end and divided into equal
+ * contiguous ranges, one per worker (a warp); a worker reads each chunk's K
+ * and V once for the whole query group.  A (sequence, KV head) that lies in a
+ * single worker's range is finished by that worker; one spread over several
+ * workers leaves fp32 partial states (m, l, o) that paged_decode_combine
+ * merges.  The split depends only on the context lengths and the worker
+ * count, never on physical page ids, so permuting pages gives bitwise equal
+ * results.
+ *
+ * num_workers: 0 = automatic (a multiple of the GPU's SM count, capped so
+ * each worker gets several chunks); n > 0 = at most n workers (n = 1: one
+ * worker walks the whole batch, no partial states).
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace paged_decode_attention needs for these shapes on
+ * the current device with this num_workers.  *bytes receives the size.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA (device query failed). */
+pkv_status paged_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int num_workers, size_t* bytes);
+
+/* Plan step: validates context_lens on the device (clamping to the table row,
+ * flagging PKV_DEV_BAD_LEN), clears the status word, and writes the chunk
+ * prefix sums and the worker count into the workspace.  One kernel (one CTA). */
+pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_heads,
+                             int n_kv_heads, int head_dim, int page_size, int table_stride,
+                             int num_workers, void* workspace, size_t ws_bytes,
+                             pkv_stream stream);
+
+/* Main step on a workspace prepared by paged_decode_plan with the same shapes:
+ * the decode kernel (persistent grid of workers; TMA bulk copies of K/V chunks
+ * into shared memory, fp32 online softmax).  Writes out for every (sequence,
+ * KV head) finished by one worker and partial states for the rest. */
+pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, int table_stride, int batch,
+                            int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                            int num_pages, pkv_dtype dtype, float scale, void* out,
+                            void* workspace, size_t ws_bytes, int num_workers,
+                            pkv_stream stream);
+
+/* Combine step: for every (sequence, KV head) split over several workers,
+ * out = sum_i w_i o_i / sum_i w_i l_i with w_i = 2^(m_i - max m) (partials
+ * keep m in base-2 units); writes zeros for sequences with no tokens. */
+pkv_status paged_decode_combine(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                pkv_dtype dtype, void* out, void* workspace, size_t ws_bytes,
+                                int num_workers, pkv_stream stream);
+
+/* The whole decode: plan + run + combine (three kernels on `stream`).
+ * q, k_pool, v_pool, page_table, context_lens, out, workspace (device).
+ * out must not overlap q, the pools, the table, the lengths or the workspace
+ * (ALIAS).  ws_bytes >= paged_decode_workspace_size(...) (else WORKSPACE).
+ * scale multiplies q.k before the softmax (usually 1/sqrt(head_dim)). */
+pkv_status paged_decode_attention(const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* page_table, int table_stride,
+                                  const int32_t* context_lens, int batch, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                  pkv_dtype dtype, float scale, void* out, void* workspace,
+                                  size_t ws_bytes, int num_workers, pkv_stream stream);
+
+/* Copy the workspace's device status word to *status_out (host).  This call
+ * synchronises with the device.  Returns DEVICE_CHECK when any bit is set,
+ * OK otherwise (CUDA on a failed copy). */
+pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

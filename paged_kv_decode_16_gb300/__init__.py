@@ -1,1 +1,341 @@
-"""GB300-native paged GQA decode attention (CUDA library + thin Python binding)."""
+"""GB300-native paged GQA decode attention: thin Python binding of libpagedkv.so.
+
+Every function here has the name of the C-ABI entry point it calls
+(``include/pagedkv.h``) and only marshals arguments: torch tensors are
+checked for device, dtype and contiguity and passed as raw device pointers;
+the current torch CUDA stream is passed as the stream.  All computation runs
+in the library's CUDA kernels.  There is no fallback: if the library was not
+built, or a call fails, an exception is raised.
+
+PyTorch is used only to own device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "PagedKVError", "load_library", "library_path", "pkv_status_string", "pkv_version",
+    "Pool", "kv_pool_create", "kv_append", "kv_gather", "paged_decode_workspace_size",
+    "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
+    "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
+]
+
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+                3: "PKV_ERR_ALIAS", 4: "PKV_ERR_OUT_OF_PAGES", 5: "PKV_ERR_WORKSPACE",
+                6: "PKV_ERR_CUDA", 7: "PKV_ERR_DEVICE_CHECK", 8: "PKV_ERR_REFCOUNT"}
+DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
+_DT = {torch.float16: 0, torch.bfloat16: 1}
+
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS_NAMES.get(code, str(code))
+        super().__init__(f"{where}: {self.name} ({pkv_status_string(code)})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libpagedkv.so (building it first when missing and nvcc is present)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"CUDA library not built: {path}")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    V, I, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    sig = {
+        "pkv_status_string": ([I], ctypes.c_char_p),
+        "pkv_version": ([], I),
+        "kv_pool_create": ([I, I, I, I, I, V, V, ctypes.POINTER(V)], I),
+        "kv_pool_destroy": ([V], I),
+        "kv_pool_k": ([V], V),
+        "kv_pool_v": ([V], V),
+        "kv_pool_alloc_pages": ([V, I, V], I),
+        "kv_pool_retain_pages": ([V, V, I], I),
+        "kv_pool_release_pages": ([V, V, I], I),
+        "kv_pool_free_count": ([V], I),
+        "kv_pool_refcount": ([V, ctypes.c_int32], I),
+        "kv_pool_info": ([V, V, V, V, V, V], I),
+        "kv_append": ([V, V, V, V, I, V, I, V, V], I),
+        "kv_gather": ([V, V, I, V, I, I, V, V, V, V], I),
+        "paged_decode_workspace_size": ([I, I, I, I, I, ctypes.POINTER(Z)], I),
+        "paged_decode_plan": ([V, I, I, I, I, I, I, I, V, Z, V], I),
+        "paged_decode_run": ([V, V, V, V, I, I, I, I, I, I, I, I, F, V, V, Z, I, V], I),
+        "paged_decode_combine": ([I, I, I, I, I, V, V, Z, I, V], I),
+        "paged_decode_attention": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, V], I),
+        "pkv_read_device_status": ([V, ctypes.POINTER(ctypes.c_uint32)], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def pkv_status_string(code: int) -> str:
+    return load_library().pkv_status_string(int(code)).decode()
+
+
+def pkv_version() -> int:
+    return load_library().pkv_version()
+
+
+def _check(code: int, where: str):
+    if code != PKV_OK:
+        raise PagedKVError(code, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"dtype {t.dtype} not supported (float16 or bfloat16)")
+    return _DT[t.dtype]
+
+
+# ---------------------------------------------------------------------------
+class Pool:
+    """Handle of a page pool (kv_pool_create).  Borrowed torch tensors are kept
+    alive by the handle."""
+
+    def __init__(self, handle: int, k: torch.Tensor | None, v: torch.Tensor | None,
+                 num_pages: int, page_size: int, n_kv_heads: int, head_dim: int, dtype):
+        self._h = ctypes.c_void_p(handle)
+        self._keep = (k, v)
+        self.num_pages, self.page_size = num_pages, page_size
+        self.n_kv_heads, self.head_dim, self.dtype = n_kv_heads, head_dim, dtype
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise ValueError("pool destroyed")
+        return self._h
+
+    def k_ptr(self) -> int:
+        return load_library().kv_pool_k(self.handle) or 0
+
+    def v_ptr(self) -> int:
+        return load_library().kv_pool_v(self.handle) or 0
+
+    def alloc_pages(self, n: int) -> list[int]:
+        ids = (ctypes.c_int32 * max(n, 1))()
+        _check(load_library().kv_pool_alloc_pages(self.handle, n, ids), "kv_pool_alloc_pages")
+        return list(ids[:n])
+
+    def retain_pages(self, ids) -> None:
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(load_library().kv_pool_retain_pages(self.handle, arr, len(ids)),
+               "kv_pool_retain_pages")
+
+    def release_pages(self, ids) -> None:
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(load_library().kv_pool_release_pages(self.handle, arr, len(ids)),
+               "kv_pool_release_pages")
+
+    def free_count(self) -> int:
+        return load_library().kv_pool_free_count(self.handle)
+
+    def refcount(self, page_id: int) -> int:
+        return load_library().kv_pool_refcount(self.handle, int(page_id))
+
+    def destroy(self) -> None:
+        if self._h:
+            code = load_library().kv_pool_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+            self._keep = (None, None)
+            _check(code, "kv_pool_destroy")
+
+    def __del__(self):
+        try:
+            if self._h:
+                load_library().kv_pool_destroy(self._h)
+        except Exception:
+            pass
+
+
+def kv_pool_create(num_pages: int, page_size: int, n_kv_heads: int, head_dim: int,
+                   dtype=torch.bfloat16, k_pool: torch.Tensor | None = None,
+                   v_pool: torch.Tensor | None = None) -> Pool:
+    """Create a pool; with k_pool/v_pool given ([NP, Hkv, P, D] device tensors)
+    the pool borrows them, otherwise it allocates device memory itself."""
+    if (k_pool is None) != (v_pool is None):
+        raise ValueError("give both k_pool and v_pool or neither")
+    code_dt = _DT.get(dtype)
+    if code_dt is None:
+        raise ValueError(f"dtype {dtype} not supported")
+    if k_pool is not None:
+        shape = (num_pages, n_kv_heads, page_size, head_dim)
+        for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+            _dev(t, name, dtype, 4)
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{name} shape {tuple(t.shape)} != {shape}")
+    h = ctypes.c_void_p()
+    _check(load_library().kv_pool_create(num_pages, page_size, n_kv_heads, head_dim, code_dt,
+                                         _ptr(k_pool), _ptr(v_pool), ctypes.byref(h)),
+           "kv_pool_create")
+    return Pool(h.value, k_pool, v_pool, num_pages, page_size, n_kv_heads, head_dim, dtype)
+
+
+def kv_append(pool: Pool, k_new: torch.Tensor, v_new: torch.Tensor, page_table: torch.Tensor,
+              positions: torch.Tensor, dev_status: torch.Tensor | None = None,
+              stream=None) -> None:
+    """Write k_new/v_new [B, Hkv, D] into slot positions[b] of each sequence."""
+    _dev(k_new, "k_new", pool.dtype, 3)
+    _dev(v_new, "v_new", pool.dtype, 3)
+    _dev(page_table, "page_table", torch.int32, 2)
+    _dev(positions, "positions", torch.int32, 1)
+    B = positions.shape[0]
+    if k_new.shape != v_new.shape or k_new.shape != (B, pool.n_kv_heads, pool.head_dim):
+        raise ValueError("k_new/v_new must be [B, Hkv, D] matching the pool")
+    if page_table.shape[0] != B:
+        raise ValueError("page_table rows != batch")
+    if dev_status is not None:
+        _dev(dev_status, "dev_status", torch.int32)
+    _check(load_library().kv_append(pool.handle, _ptr(k_new), _ptr(v_new), _ptr(page_table),
+                                    page_table.shape[1], _ptr(positions), B, _ptr(dev_status),
+                                    _stream(stream)), "kv_append")
+
+
+def kv_gather(pool: Pool, page_table: torch.Tensor, context_lens: torch.Tensor, max_len: int,
+              k_out: torch.Tensor, v_out: torch.Tensor, dev_status: torch.Tensor | None = None,
+              stream=None) -> None:
+    """Dense [B, Hkv, max_len, D] copy of each sequence's cached rows."""
+    _dev(page_table, "page_table", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    B = context_lens.shape[0]
+    for name, t in (("k_out", k_out), ("v_out", v_out)):
+        _dev(t, name, pool.dtype, 4)
+        if tuple(t.shape) != (B, pool.n_kv_heads, max_len, pool.head_dim):
+            raise ValueError(f"{name} must be [B, Hkv, max_len, D]")
+    if dev_status is not None:
+        _dev(dev_status, "dev_status", torch.int32)
+    _check(load_library().kv_gather(pool.handle, _ptr(page_table), page_table.shape[1],
+                                    _ptr(context_lens), B, max_len, _ptr(k_out), _ptr(v_out),
+                                    _ptr(dev_status), _stream(stream)), "kv_gather")
+
+
+def paged_decode_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                                num_workers: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().paged_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                                      num_workers, ctypes.byref(n)),
+           "paged_decode_workspace_size")
+    return n.value
+
+
+def alloc_workspace(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                    num_workers: int = 0, device=None) -> torch.Tensor:
+    """A torch uint8 buffer of the size paged_decode_attention needs (256-B aligned)."""
+    n = paged_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, num_workers)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def _decode_shapes(q, k_pool, v_pool, page_table, out):
+    _dev(q, "q", None, 3)
+    dt = _dtype_code(q)
+    _dev(k_pool, "k_pool", q.dtype, 4)
+    _dev(v_pool, "v_pool", q.dtype, 4)
+    _dev(out, "out", q.dtype, 3)
+    _dev(page_table, "page_table", torch.int32, 2)
+    B, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or out.shape != q.shape:
+        raise ValueError("q/out [B, Hq, D] and pools [NP, Hkv, P, D] disagree")
+    if page_table.shape[0] != B:
+        raise ValueError("page_table rows != batch")
+    return B, Hq, Hkv, D, P, NP, dt
+
+
+def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: torch.Tensor, workspace: torch.Tensor, num_workers: int = 0,
+                           stream=None) -> torch.Tensor:
+    """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over context_lens[b]
+    tokens read through page_table[b] (plan + decode + combine kernels)."""
+    B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8)
+    _check(load_library().paged_decode_attention(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1],
+        _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace),
+        workspace.numel(), int(num_workers), _stream(stream)), "paged_decode_attention")
+    return out
+
+
+def paged_decode_plan(context_lens: torch.Tensor, n_q_heads: int, n_kv_heads: int,
+                      head_dim: int, page_size: int, table_stride: int, workspace: torch.Tensor,
+                      num_workers: int = 0, stream=None) -> None:
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8)
+    _check(load_library().paged_decode_plan(
+        _ptr(context_lens), context_lens.shape[0], n_q_heads, n_kv_heads, head_dim, page_size,
+        table_stride, int(num_workers), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "paged_decode_plan")
+
+
+def paged_decode_run(q, k_pool, v_pool, page_table, scale: float, out, workspace,
+                     num_workers: int = 0, stream=None) -> None:
+    B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
+    _dev(workspace, "workspace", torch.uint8)
+    _check(load_library().paged_decode_run(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1], B, Hq, Hkv,
+        D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+        int(num_workers), _stream(stream)), "paged_decode_run")
+
+
+def paged_decode_combine(out: torch.Tensor, n_kv_heads: int, workspace: torch.Tensor,
+                         num_workers: int = 0, stream=None) -> None:
+    _dev(out, "out", None, 3)
+    _dev(workspace, "workspace", torch.uint8)
+    B, Hq, D = out.shape
+    _check(load_library().paged_decode_combine(
+        B, Hq, n_kv_heads, D, _dtype_code(out), _ptr(out), _ptr(workspace), workspace.numel(),
+        int(num_workers), _stream(stream)), "paged_decode_combine")
+
+
+def pkv_read_device_status(workspace: torch.Tensor) -> int:
+    """The status word of the last decode on this workspace (synchronises)."""
+    _dev(workspace, "workspace", torch.uint8)
+    v = ctypes.c_uint32()
+    code = load_library().pkv_read_device_status(_ptr(workspace), ctypes.byref(v))
+    if code not in (0, 7):
+        _check(code, "pkv_read_device_status")
+    return v.value

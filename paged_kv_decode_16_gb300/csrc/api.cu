@@ -1,0 +1,413 @@
+// api.cu -- the C ABI (include/pagedkv.h): host-side validation, workspace
+// layout, and the stream-ordered launches of the plan, decode and combine
+// kernels, the KV append and the gather.
+//
+// Conventions follow Experimental LibTorch prefix cache, "Identity, ownership
+// and output behavior": work is ordered on the caller's stream, the caller
+// owns every buffer, the host validates shapes and rejects aliased output
+// before anything is launched, and failures are reported, never thrown.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "common.cuh"
+#include "kernels_aux.cuh"
+#include "pool_impl.hpp"
+
+namespace {
+
+using pkv::DecodeKernelInfo;
+using pkv::WsHeader;
+
+constexpr int kMinChunksPerWorker = 4;  // automatic worker count: at least this many chunks each
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// G = sub_groups * gs with gs <= 8 (the widest group one warp serves); the
+// smallest number of sub-groups that divides G.
+inline bool split_group(int group, int* sub_groups, int* gs) {
+    for (int ns = (group + 7) / 8; ns <= group; ++ns) {
+        if (group % ns == 0) {
+            *sub_groups = ns;
+            *gs = group / ns;
+            return true;
+        }
+    }
+    return false;
+}
+
+pkv_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size) {
+    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || page_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (page_size % 16 != 0 || page_size > 256) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+DecodeKernelInfo decode_info(pkv_dtype dtype, int head_dim, int gs) {
+    return dtype == PKV_BF16 ? pkv::decode_info_bf16(head_dim, gs)
+                             : pkv::decode_info_f16(head_dim, gs);
+}
+
+// Per (device, kernel): dynamic shared memory opt-in done, and the automatic
+// worker count = SMs x resident CTAs per SM x warps per CTA.
+std::mutex g_mu;
+std::map<std::pair<int, const void*>, int> g_auto_workers;
+
+pkv_status prepare_kernel(const DecodeKernelInfo& info, int* auto_workers) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(info.fn));
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_auto_workers.find(key);
+        if (it != g_auto_workers.end()) {
+            *auto_workers = it->second;
+            return PKV_OK;
+        }
+    }
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(info.fn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             info.smem_bytes) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, reinterpret_cast<const void*>(info.fn), info.warps * 32,
+            info.smem_bytes) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    const int workers = sms * (per_sm > 0 ? per_sm : 1) * info.warps;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_auto_workers[key] = workers;
+    *auto_workers = workers;
+    return PKV_OK;
+}
+
+struct WsLayout {
+    size_t lens_eff, prefix, partials, total;
+};
+
+WsLayout ws_layout(int batch, long long units, int gs, int head_dim, int workers) {
+    WsLayout w;
+    size_t off = sizeof(WsHeader);
+    w.lens_eff = off;
+    off += align256((size_t)batch * 4);
+    w.prefix = off;
+    off += align256((size_t)(batch + 1) * 4);
+    w.partials = off;
+    off += align256((size_t)(units + workers) * gs * (head_dim + 2) * 4);
+    w.total = off;
+    return w;
+}
+
+// Everything the three decode steps derive from the shapes.
+struct DecodeSetup {
+    int group, sub_groups, gs, units_per_b;
+    long long units;
+    int workers;       // launched workers (upper bound of the plan's count)
+    int workers_auto;  // automatic count for this kernel on this device
+    DecodeKernelInfo info;
+    WsLayout ws;
+};
+
+pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                        pkv_dtype dtype, int num_workers, DecodeSetup* s) {
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
+    if (st != PKV_OK) return st;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (num_workers < 0) return PKV_ERR_INVALID_ARG;
+    s->group = n_q_heads / n_kv_heads;
+    if (!split_group(s->group, &s->sub_groups, &s->gs)) return PKV_ERR_UNSUPPORTED;
+    s->units_per_b = n_kv_heads * s->sub_groups;
+    s->units = (long long)batch * s->units_per_b;
+    s->info = decode_info(dtype, head_dim, s->gs);
+    if (!s->info.fn) return PKV_ERR_UNSUPPORTED;
+    st = prepare_kernel(s->info, &s->workers_auto);
+    if (st != PKV_OK) return st;
+    s->workers = num_workers > 0 ? num_workers : s->workers_auto;
+    s->ws = ws_layout(batch, s->units, s->gs, head_dim, s->workers);
+    return PKV_OK;
+}
+
+pkv_status check_workspace(const void* workspace, size_t ws_bytes, const DecodeSetup& s) {
+    if (!workspace) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_WORKSPACE;
+    if (ws_bytes < s.ws.total) return PKV_ERR_WORKSPACE;
+    return PKV_OK;
+}
+
+inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+pkv_status do_plan(const int32_t* context_lens, int batch, int page_size, int table_stride,
+                   int num_workers, void* workspace, const DecodeSetup& s, cudaStream_t stream) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return cuda_status(pkv::launch_plan(
+        context_lens, batch, s.units_per_b, (long long)table_stride * page_size,
+        num_workers > 0 ? s.workers : 0, s.workers_auto, kMinChunksPerWorker,
+        reinterpret_cast<int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<int32_t*>(ws + s.ws.prefix),
+        reinterpret_cast<WsHeader*>(ws), stream));
+}
+
+pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
+                  int table_stride, int batch, int n_q_heads, int n_kv_heads, int page_size,
+                  int num_pages, float scale, void* out, void* workspace, const DecodeSetup& s,
+                  cudaStream_t stream) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    pkv::DecodeParams p;
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.table = table;
+    p.lens_eff = reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff);
+    p.prefix = reinterpret_cast<const int32_t*>(ws + s.ws.prefix);
+    p.hdr = reinterpret_cast<const WsHeader*>(ws);
+    p.status = &reinterpret_cast<WsHeader*>(ws)->status;
+    p.partials = reinterpret_cast<float*>(ws + s.ws.partials);
+    p.out = out;
+    p.table_stride = table_stride;
+    p.batch = batch;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.page_size = page_size;
+    p.num_pages = num_pages;
+    p.group = s.group;
+    p.sub_groups = s.sub_groups;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int blocks = (s.workers + s.info.warps - 1) / s.info.warps;
+    s.info.fn<<<blocks, s.info.warps * 32, s.info.smem_bytes, stream>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, void* out,
+                      void* workspace, const DecodeSetup& s, cudaStream_t stream) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (batch == 0) return PKV_OK;
+    return cuda_status(pkv::launch_combine(
+        dtype, head_dim, reinterpret_cast<const float*>(ws + s.ws.partials),
+        reinterpret_cast<const int32_t*>(ws + s.ws.prefix),
+        reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<const WsHeader*>(ws),
+        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.group, n_q_heads, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PKV_ERR_ALIAS: return "output overlaps an input";
+        case PKV_ERR_OUT_OF_PAGES: return "not enough free pages";
+        case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case PKV_ERR_CUDA: return "CUDA runtime error";
+        case PKV_ERR_DEVICE_CHECK: return "device status reports skipped input";
+        case PKV_ERR_REFCOUNT: return "page reference count error";
+    }
+    return "unknown status";
+}
+
+int pkv_version(void) { return 100; }
+
+pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
+                     const int32_t* page_table, int table_stride, const int32_t* positions,
+                     int batch, uint32_t* dev_status, pkv_stream stream) {
+    if (!pool || batch < 0 || table_stride <= 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!k_new || !v_new || !page_table || !positions) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(pool->k) || !aligned16(pool->v))
+        return PKV_ERR_INVALID_ARG;
+    const size_t pool_bytes =
+        (size_t)pool->num_pages * pool->n_kv_heads * pool->page_size * pool->head_dim * 2;
+    const size_t row_bytes = (size_t)batch * pool->n_kv_heads * pool->head_dim * 2;
+    if (overlaps(k_new, row_bytes, pool->k, pool_bytes) ||
+        overlaps(k_new, row_bytes, pool->v, pool_bytes) ||
+        overlaps(v_new, row_bytes, pool->k, pool_bytes) ||
+        overlaps(v_new, row_bytes, pool->v, pool_bytes))
+        return PKV_ERR_ALIAS;
+    return cuda_status(pkv::launch_append(k_new, v_new, page_table, table_stride, positions, batch,
+                                          pool->n_kv_heads, pool->head_dim, pool->page_size,
+                                          pool->num_pages, pool->k, pool->v, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_stride,
+                     const int32_t* context_lens, int batch, int max_len, void* k_out,
+                     void* v_out, uint32_t* dev_status, pkv_stream stream) {
+    if (!pool || batch < 0 || max_len < 0 || table_stride <= 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0 || max_len == 0) return PKV_OK;
+    if (batch > 65535 || pool->n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!page_table || !context_lens || !k_out || !v_out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_out) || !aligned16(v_out)) return PKV_ERR_INVALID_ARG;
+    const size_t pool_bytes =
+        (size_t)pool->num_pages * pool->n_kv_heads * pool->page_size * pool->head_dim * 2;
+    const size_t out_bytes = (size_t)batch * pool->n_kv_heads * max_len * pool->head_dim * 2;
+    if (overlaps(k_out, out_bytes, pool->k, pool_bytes) ||
+        overlaps(k_out, out_bytes, pool->v, pool_bytes) ||
+        overlaps(v_out, out_bytes, pool->k, pool_bytes) ||
+        overlaps(v_out, out_bytes, pool->v, pool_bytes) || overlaps(k_out, out_bytes, v_out, out_bytes))
+        return PKV_ERR_ALIAS;
+    return cuda_status(pkv::launch_gather(pool->k, pool->v, page_table, table_stride, context_lens,
+                                          batch, pool->n_kv_heads, pool->head_dim, pool->page_size,
+                                          pool->num_pages, max_len, k_out, v_out, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status paged_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int num_workers, size_t* bytes) {
+    if (!bytes) return PKV_ERR_INVALID_ARG;
+    *bytes = 0;
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, 16);
+    if (st != PKV_OK) return st;
+    if (num_workers < 0) return PKV_ERR_INVALID_ARG;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, PKV_BF16, num_workers,
+                           &s)) != PKV_OK)
+        return st;
+    *bytes = s.ws.total;
+    return PKV_OK;
+}
+
+// Host-only argument checks of a decode call (no CUDA call is made), in the
+// order: shapes, scalars, pointers, alignment, aliasing of out.
+static pkv_status validate_decode_args(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* page_table, int table_stride,
+                                       const int32_t* context_lens, bool need_lens, int batch,
+                                       int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                                       int num_pages, pkv_dtype dtype, float scale,
+                                       const void* out, const void* workspace, size_t ws_bytes,
+                                       int num_workers) {
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
+    if (st != PKV_OK) return st;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (num_pages <= 0 || table_stride <= 0 || num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_pool || !v_pool || !page_table || !out || (need_lens && !context_lens))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    const size_t qo_bytes = (size_t)batch * n_q_heads * head_dim * 2;
+    const size_t pool_bytes = (size_t)num_pages * n_kv_heads * page_size * head_dim * 2;
+    const size_t table_bytes = (size_t)batch * table_stride * 4;
+    if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_pool, pool_bytes) ||
+        overlaps(out, qo_bytes, v_pool, pool_bytes) ||
+        overlaps(out, qo_bytes, page_table, table_bytes) ||
+        (need_lens && overlaps(out, qo_bytes, context_lens, (size_t)batch * 4)) ||
+        overlaps(out, qo_bytes, workspace, ws_bytes))
+        return PKV_ERR_ALIAS;
+    return PKV_OK;
+}
+
+pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_heads,
+                             int n_kv_heads, int head_dim, int page_size, int table_stride,
+                             int num_workers, void* workspace, size_t ws_bytes,
+                             pkv_stream stream) {
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
+    if (st != PKV_OK) return st;
+    if (table_stride <= 0 || num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!context_lens) return PKV_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, PKV_BF16,
+                           num_workers, &s)) != PKV_OK)
+        return st;
+    if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
+    return do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, int table_stride, int batch,
+                            int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                            int num_pages, pkv_dtype dtype, float scale, void* out,
+                            void* workspace, size_t ws_bytes, int num_workers,
+                            pkv_stream stream) {
+    pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride, nullptr,
+                                         false, batch, n_q_heads, n_kv_heads, head_dim,
+                                         page_size, num_pages, dtype, scale, out, workspace,
+                                         ws_bytes, num_workers);
+    if (st != PKV_OK || batch == 0) return st;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           &s)) != PKV_OK)
+        return st;
+    if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
+    return do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
+                  page_size, num_pages, scale, out, workspace, s,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_decode_combine(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                pkv_dtype dtype, void* out, void* workspace, size_t ws_bytes,
+                                int num_workers, pkv_stream stream) {
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, 16);
+    if (st != PKV_OK) return st;
+    if ((dtype != PKV_F16 && dtype != PKV_BF16) || num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!out || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
+    if (overlaps(out, (size_t)batch * n_q_heads * head_dim * 2, workspace, ws_bytes))
+        return PKV_ERR_ALIAS;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, dtype, num_workers, &s)) !=
+        PKV_OK)
+        return st;
+    if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
+    return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_decode_attention(const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* page_table, int table_stride,
+                                  const int32_t* context_lens, int batch, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                  pkv_dtype dtype, float scale, void* out, void* workspace,
+                                  size_t ws_bytes, int num_workers, pkv_stream stream) {
+    pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
+                                         context_lens, true, batch, n_q_heads, n_kv_heads,
+                                         head_dim, page_size, num_pages, dtype, scale, out,
+                                         workspace, ws_bytes, num_workers);
+    if (st != PKV_OK || batch == 0) return st;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           &s)) != PKV_OK)
+        return st;
+    if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
+                      cs)) != PKV_OK)
+        return st;
+    if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
+                     page_size, num_pages, scale, out, workspace, s, cs)) != PKV_OK)
+        return st;
+    return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
+}
+
+pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
+    if (!workspace || !status_out) return PKV_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    *status_out = v;
+    return v ? PKV_ERR_DEVICE_CHECK : PKV_OK;
+}
+
+}  // extern "C"

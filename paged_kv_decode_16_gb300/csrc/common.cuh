@@ -1,0 +1,182 @@
+// common.cuh -- shared device helpers of the paged decode library (sm_103a).
+//
+// Inline PTX for the Blackwell async-copy path: mbarrier wait/arrive with a
+// transaction count, and the bulk (TMA) global->shared copy that completes on
+// an mbarrier.  Every wait is bounded: after kSpinLimit failed polls the caller
+// gets `false` and reports PKV_DEV_TIMEOUT instead of spinning forever.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+constexpr int kChunk = 16;               // tokens per pipeline stage
+constexpr unsigned kFull = 0xffffffffu;  // full-warp shuffle mask
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// Workspace header (first 256 bytes of the decode workspace).
+struct WsHeader {
+    uint32_t status;         // PKV_DEV_* bits of the current call
+    int32_t total_chunks;    // chunks over all (sequence, KV head, sub-group) units
+    int32_t num_workers;     // workers that received a non-empty range
+    int32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Order earlier generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy) writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+    return false;
+}
+
+// Bulk async copy global -> shared (no tensor map), completes `bytes` of
+// transaction on `bar`.  dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Same, with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// 16-bit storage types and their conversions.
+template <typename T>
+struct Cvt;
+
+template <>
+struct Cvt<__nv_bfloat16> {
+    // 8 packed bf16 (one 16-byte vector) -> 8 floats
+    static __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+
+template <>
+struct Cvt<__half> {
+    static __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+            float2 x = __half22float2(h);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+
+__host__ __device__ constexpr int next_pow2(int x) {
+    return x <= 1 ? 1 : (x <= 2 ? 2 : (x <= 4 ? 4 : (x <= 8 ? 8 : 16)));
+}
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Parameters of the decode kernel (one struct, passed by value).
+struct DecodeParams {
+    const void* q;            // [B][Hq][D]
+    const void* k_pool;       // [NP][Hkv][P][D]
+    const void* v_pool;
+    const int32_t* table;     // [B][stride]
+    const int32_t* lens_eff;  // [B] lengths after the plan's clamp (workspace)
+    const int32_t* prefix;    // [B+1] chunk prefix sums (workspace)
+    const WsHeader* hdr;      // total chunks, worker count
+    uint32_t* status;
+    float* partials;          // [slots][GS*(D+2)]
+    void* out;                // [B][Hq][D]
+    int table_stride;
+    int batch, n_q_heads, n_kv_heads, page_size, num_pages;
+    int group;                // G = Hq / Hkv
+    int sub_groups;           // units per KV head (G = sub_groups * GS)
+    float scale_log2;         // scale * log2(e)
+};
+
+// Launch configuration of one decode-kernel instantiation.
+struct DecodeKernelInfo {
+    void (*fn)(DecodeParams);
+    int warps;       // warps (workers) per CTA
+    int stages;      // chunk buffers per warp
+    int smem_bytes;  // dynamic shared memory per CTA
+    int gs;          // query heads served per unit
+};
+
+}  // namespace pkv

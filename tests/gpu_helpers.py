@@ -1,0 +1,93 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and the oracle on host copies of the same inputs, and compare.
+
+Tolerance (decode outputs, fp16/bf16 inputs, fp32 accumulation, output
+rounded to the input dtype):
+  * every element: |gpu - ref| <= ATOL + RTOL * |ref|      (ATOL 2e-3, RTOL 1e-2)
+  * strict form, also required on the five named workloads:
+      max |gpu - ref| <= ATOL  and  max |gpu - ref| / max(|ref|, ATOL/RTOL) <= RTOL
+Append, gather and page-table indexing are compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_decode_16_gb300 as pkv
+from paged_kv_decode_16_gb300 import workloads as wl
+
+ATOL = 2e-3
+RTOL = 1e-2
+
+
+def to_dev(w: wl.Workload, dev="cuda"):
+    table = torch.from_numpy(np.ascontiguousarray(w.page_table)).to(dev)
+    lens = torch.from_numpy(np.ascontiguousarray(w.context_lens)).to(dev)
+    pos = torch.from_numpy(np.ascontiguousarray(w.positions)).to(dev)
+    return table, lens, pos
+
+
+def run_gpu(w: wl.Workload, num_workers: int = 0, append: bool | None = None):
+    """kv_append (when the workload has one) then paged_decode_attention.
+    Returns (out tensor, workspace, host status)."""
+    dev = w.q.device
+    table, lens, pos = to_dev(w, dev)
+    if append if append is not None else w.append:
+        pool = pkv.kv_pool_create(w.num_pages, w.page_size, w.n_kv_heads, w.head_dim, w.dtype,
+                                  w.k_pool, w.v_pool)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        pkv.kv_append(pool, w.k_new, w.v_new, table, pos, dev_status=st)
+        assert int(st.item()) == 0
+    out = torch.empty_like(w.q)
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, num_workers,
+                             device=dev)
+    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws,
+                               num_workers=num_workers)
+    torch.cuda.synchronize()
+    return out, ws, pkv.pkv_read_device_status(ws)
+
+
+def oracle_inputs(w: wl.Workload, pools_before=None, append: bool | None = None):
+    """Host bit patterns for the oracle; applies the append on the host copy
+    of the pre-append pools when the workload has one."""
+    kp, vp = pools_before if pools_before is not None else (wl.to_bits(w.k_pool),
+                                                            wl.to_bits(w.v_pool))
+    if append if append is not None else w.append:
+        kp, vp = oracle.kv_append(kp, vp, wl.to_bits(w.k_new), wl.to_bits(w.v_new),
+                                  w.page_table, w.positions)
+    return wl.to_bits(w.q), kp, vp
+
+
+def oracle_full(w: wl.Workload, pools_before=None, append=None) -> np.ndarray:
+    q, kp, vp = oracle_inputs(w, pools_before, append)
+    return oracle.paged_decode(q, kp, vp, w.page_table, w.context_lens, w.scale, w.dtype_name)
+
+
+def oracle_rows(w: wl.Workload, rows, pools_before=None, append=None) -> np.ndarray:
+    q, kp, vp = oracle_inputs(w, pools_before, append)
+    return oracle.paged_decode_rows(q, kp, vp, w.page_table, w.context_lens, w.scale,
+                                    w.dtype_name, rows)
+
+
+def errors(got: np.ndarray, ref: np.ndarray):
+    err = np.abs(got - ref)
+    rel = err / np.maximum(np.abs(ref), ATOL / RTOL)
+    return float(err.max(initial=0.0)), float(rel.max(initial=0.0))
+
+
+def assert_close(got, ref: np.ndarray, strict: bool = False, what: str = ""):
+    if isinstance(got, torch.Tensor):
+        got = got.float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - (ATOL + RTOL * np.abs(ref))), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; worst at {i}: "
+                             f"gpu {got[i]!r} ref {ref[i]!r}")
+    if strict:
+        mx, rel = errors(got, ref)
+        assert mx <= ATOL, f"{what}: max abs err {mx:.3g} > {ATOL}"
+        assert rel <= RTOL, f"{what}: max rel err {rel:.3g} > {RTOL}"

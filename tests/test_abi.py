@@ -1,0 +1,210 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before touching CUDA; the host page
+allocator keeps correct reference counts."""
+import ctypes
+import os
+import re
+import threading
+
+import pytest
+
+import paged_kv_decode_16_gb300 as pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+OK, INVALID, UNSUPPORTED, ALIAS, OUT_OF_PAGES, WORKSPACE, CUDA, DEVCHECK, REFCOUNT = range(9)
+F16, BF16 = 0, 1
+A = 1 << 20  # fake, 256-byte aligned "device" addresses; validation never dereferences them
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return pkv.load_library()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 20, names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in pagedkv.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert pkv.pkv_status_string(code)
+    assert pkv.pkv_status_string(99) == "unknown status"
+    assert pkv.pkv_version() >= 100
+
+
+def _decode(lib, **kw):
+    a = dict(q=A, k=A * 8, v=A * 16, table=A * 24, stride=4, lens=A * 25, batch=2, hq=8, hkv=2,
+             d=128, p=16, np_=8, dt=BF16, scale=0.088, out=A * 26, ws=A * 27, ws_bytes=1 << 20,
+             workers=0)
+    a.update(kw)
+    V = ctypes.c_void_p
+    return lib.paged_decode_attention(V(a["q"]), V(a["k"]), V(a["v"]), V(a["table"]), a["stride"],
+                                      V(a["lens"]), a["batch"], a["hq"], a["hkv"], a["d"], a["p"],
+                                      a["np_"], a["dt"], ctypes.c_float(a["scale"]), V(a["out"]),
+                                      V(a["ws"]), a["ws_bytes"], a["workers"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), UNSUPPORTED),
+    (dict(d=256), UNSUPPORTED),
+    (dict(p=8), UNSUPPORTED),
+    (dict(p=24), UNSUPPORTED),
+    (dict(hq=6, hkv=4), INVALID),
+    (dict(hkv=0), INVALID),
+    (dict(batch=-1), INVALID),
+    (dict(np_=0), INVALID),
+    (dict(stride=0), INVALID),
+    (dict(dt=5), INVALID),
+    (dict(workers=-2), INVALID),
+    (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(q=0), INVALID),
+    (dict(lens=0), INVALID),
+    (dict(out=0), INVALID),
+    (dict(ws=0), WORKSPACE),
+    (dict(ws=A + 64), WORKSPACE),
+    (dict(q=A + 8), INVALID),
+    (dict(out=A * 26 + 4), INVALID),
+    (dict(out=A), ALIAS),                 # out == q
+    (dict(out=A * 8 + 4096), ALIAS),      # inside the K pool
+    (dict(out=A * 24), ALIAS),            # on the page table
+    (dict(out=A * 27 + 1024), ALIAS),     # inside the workspace
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert _decode(lib, batch=0, q=0, out=0, ws=0) == OK
+
+
+def test_append_and_gather_host_checks(lib):
+    V = ctypes.c_void_p
+    h = V()
+    assert lib.kv_pool_create(8, 16, 2, 128, BF16, V(A), V(A * 2), ctypes.byref(h)) == OK
+    try:
+        assert lib.kv_append(h, V(A * 3), V(A * 4), V(A * 5), 4, V(A * 6), 0, None, None) == OK
+        assert lib.kv_append(h, None, V(A * 4), V(A * 5), 4, V(A * 6), 2, None, None) == INVALID
+        assert lib.kv_append(h, V(A * 3 + 2), V(A * 4), V(A * 5), 4, V(A * 6), 2, None,
+                             None) == INVALID
+        # new rows inside the pool being written
+        assert lib.kv_append(h, V(A + 256), V(A * 4), V(A * 5), 4, V(A * 6), 2, None,
+                             None) == ALIAS
+        assert lib.kv_append(None, V(A * 3), V(A * 4), V(A * 5), 4, V(A * 6), 2, None,
+                             None) == INVALID
+        assert lib.kv_gather(h, V(A * 5), 4, V(A * 6), 2, 64, V(A * 8), V(A * 8), None,
+                             None) == ALIAS
+        assert lib.kv_gather(h, V(A * 5), 0, V(A * 6), 2, 64, V(A * 8), V(A * 9), None,
+                             None) == INVALID
+    finally:
+        assert lib.kv_pool_destroy(h) == OK
+
+
+def test_pool_create_checks(lib):
+    V = ctypes.c_void_p
+    h = V()
+    assert lib.kv_pool_create(8, 16, 2, 96, BF16, V(A), V(A), ctypes.byref(h)) == UNSUPPORTED
+    assert lib.kv_pool_create(8, 12, 2, 128, BF16, V(A), V(A), ctypes.byref(h)) == UNSUPPORTED
+    assert lib.kv_pool_create(0, 16, 2, 128, BF16, V(A), V(A), ctypes.byref(h)) == INVALID
+    assert lib.kv_pool_create(8, 16, 2, 128, BF16, V(A), None, ctypes.byref(h)) == INVALID
+    assert lib.kv_pool_create(8, 16, 2, 128, BF16, V(A + 4), V(A), ctypes.byref(h)) == INVALID
+    assert lib.kv_pool_create(8, 16, 2, 128, 3, V(A), V(A), ctypes.byref(h)) == INVALID
+    assert lib.kv_pool_destroy(None) == OK
+
+
+def _borrowed_pool(lib, n):
+    V = ctypes.c_void_p
+    h = V()
+    assert lib.kv_pool_create(n, 16, 2, 64, F16, V(A), V(A * 2), ctypes.byref(h)) == OK
+    return h
+
+
+def _ids(*v):
+    return (ctypes.c_int32 * max(len(v), 1))(*v)
+
+
+def test_allocator_refcounts(lib):
+    h = _borrowed_pool(lib, 6)
+    try:
+        assert lib.kv_pool_free_count(h) == 6
+        out = (ctypes.c_int32 * 4)()
+        assert lib.kv_pool_alloc_pages(h, 4, out) == OK
+        got = list(out)
+        assert sorted(got) == [0, 1, 2, 3] and lib.kv_pool_free_count(h) == 2
+        assert lib.kv_pool_alloc_pages(h, 3, out) == OUT_OF_PAGES
+        assert lib.kv_pool_free_count(h) == 2  # all or nothing
+        # share the first two pages (a prefix) with a second sequence
+        assert lib.kv_pool_retain_pages(h, _ids(got[0], got[1]), 2) == OK
+        assert lib.kv_pool_refcount(h, got[0]) == 2
+        assert lib.kv_pool_release_pages(h, _ids(*got), 4) == OK
+        assert lib.kv_pool_free_count(h) == 4
+        assert lib.kv_pool_refcount(h, got[0]) == 1 and lib.kv_pool_refcount(h, got[2]) == 0
+        # releasing a free page, or one page more often than held, changes nothing
+        assert lib.kv_pool_release_pages(h, _ids(got[2]), 1) == REFCOUNT
+        assert lib.kv_pool_release_pages(h, _ids(got[0], got[0]), 2) == REFCOUNT
+        assert lib.kv_pool_refcount(h, got[0]) == 1
+        assert lib.kv_pool_retain_pages(h, _ids(got[3]), 1) == REFCOUNT
+        assert lib.kv_pool_retain_pages(h, _ids(99), 1) == INVALID
+        assert lib.kv_pool_release_pages(h, _ids(-1), 1) == INVALID
+        assert lib.kv_pool_release_pages(h, _ids(got[0], got[1]), 2) == OK
+        assert lib.kv_pool_free_count(h) == 6
+        assert lib.kv_pool_refcount(h, 99) == -1
+    finally:
+        lib.kv_pool_destroy(h)
+
+
+def test_allocator_threads(lib):
+    """Concurrent alloc/retain/release from several threads keeps the books."""
+    h = _borrowed_pool(lib, 512)
+    errors = []
+
+    def worker(seed):
+        import random
+        rnd = random.Random(seed)
+        held = []
+        for _ in range(300):
+            if held and rnd.random() < 0.5:
+                ids = held.pop(rnd.randrange(len(held)))
+                if lib.kv_pool_release_pages(h, _ids(*ids), len(ids)) != OK:
+                    errors.append("release")
+            else:
+                n = rnd.randint(1, 4)
+                out = (ctypes.c_int32 * n)()
+                rc = lib.kv_pool_alloc_pages(h, n, out)
+                if rc == OK:
+                    ids = list(out)
+                    if rnd.random() < 0.3:  # share them once more
+                        if lib.kv_pool_retain_pages(h, _ids(*ids), n) != OK:
+                            errors.append("retain")
+                        held.append(ids)
+                    held.append(ids)
+                elif rc != OUT_OF_PAGES:
+                    errors.append(f"alloc {rc}")
+        for ids in held:
+            if lib.kv_pool_release_pages(h, _ids(*ids), len(ids)) != OK:
+                errors.append("final release")
+
+    ts = [threading.Thread(target=worker, args=(s,)) for s in range(8)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    try:
+        assert not errors, errors[:5]
+        assert lib.kv_pool_free_count(h) == 512
+        assert all(lib.kv_pool_refcount(h, i) == 0 for i in range(512))
+    finally:
+        lib.kv_pool_destroy(h)

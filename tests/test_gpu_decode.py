@@ -1,0 +1,269 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle."""
+import itertools
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_16_gb300 as pkv
+from paged_kv_decode_16_gb300 import workloads as wl
+from gpu_helpers import (assert_close, errors, oracle_full, oracle_rows, run_gpu, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_rows(w, rng, n_random=48):
+    """All heads of the first, last and two middle sequences plus random rows."""
+    seqs = sorted({0, w.batch - 1, w.batch // 2, w.batch // 3})
+    rows = [(b, h) for b in seqs for h in range(w.n_q_heads)]
+    rows += [(int(rng.integers(w.batch)), int(rng.integers(w.n_q_heads))) for _ in range(n_random)]
+    return np.array(rows, dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", wl.NAMES)
+def test_named_workload_matches_oracle(name):
+    w = wl.make(name, seed=0, device="cuda")
+    before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+    out, ws, status = run_gpu(w)
+    assert status == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    if name == "tiny":
+        ref = oracle_full(w, before)
+        assert_close(got, ref, strict=True, what=name)
+    else:
+        rows = _sample_rows(w, np.random.default_rng(1))
+        ref = oracle_rows(w, rows, before)
+        assert_close(got[rows[:, 0], rows[:, 1]], ref, strict=True, what=name)
+    if w.append:
+        # the append itself is bit-exact against the oracle's
+        kp, vp = oracle.kv_append(*before, wl.to_bits(w.k_new), wl.to_bits(w.v_new),
+                                  w.page_table, w.positions)
+        assert np.array_equal(kp, wl.to_bits(w.k_pool))
+        assert np.array_equal(vp, wl.to_bits(w.v_pool))
+
+
+GROUPS = [(4, 4), (4, 2), (12, 4), (8, 2), (14, 2), (16, 2), (32, 2), (9, 1), (20, 2), (6, 1)]
+LENS = {
+    "one": [1],
+    "around_chunk": [15, 16, 17, 1, 31, 33],
+    "around_page": [31, 32, 33, 64, 65, 2],
+    "ragged": None,  # random in [1, 300], batch 13
+}
+
+
+def _sweep_cases():
+    cases = []
+    rng = np.random.default_rng(123)
+    for dt, D, P in itertools.product((torch.bfloat16, torch.float16), (64, 128), (16, 32)):
+        for (hq, hkv) in GROUPS:
+            lens_name = list(LENS)[int(rng.integers(len(LENS)))]
+            workers = [0, 1, 2, 3, 7, 1000][int(rng.integers(6))]
+            cases.append((dt, D, P, hq, hkv, lens_name, workers))
+    return cases
+
+
+@pytest.mark.parametrize("dt,D,P,hq,hkv,lens_name,workers", _sweep_cases())
+def test_random_sweep(dt, D, P, hq, hkv, lens_name, workers):
+    seed = zlib.crc32(repr((str(dt), D, P, hq, hkv, lens_name, workers)).encode())
+    lens = LENS[lens_name]
+    if lens is None:
+        lens = np.random.default_rng(seed).integers(1, 301, size=13)
+    w = wl.make_random(seed, batch=len(lens), n_q_heads=hq, n_kv_heads=hkv, head_dim=D,
+                       page_size=P, dtype=dt, lens=lens, device="cuda", poison=True)
+    out, ws, status = run_gpu(w, num_workers=workers, append=False)
+    assert status == 0
+    ref = oracle_full(w, append=False)
+    assert_close(out, ref, what=f"{dt} D{D} P{P} G{hq}/{hkv} {lens_name} w{workers}")
+
+
+@pytest.mark.parametrize("workers", [1, 2, 3, 5, 64, 0])
+def test_forced_worker_counts_agree(workers):
+    """Every split of the same batch matches the oracle (partials + combine)."""
+    w = wl.make_random(7, batch=9, n_q_heads=32, n_kv_heads=8, head_dim=128, page_size=16,
+                       dtype=torch.bfloat16, lens=[1, 16, 17, 100, 257, 600, 33, 48, 1000],
+                       device="cuda", poison=True)
+    out, ws, status = run_gpu(w, num_workers=workers, append=False)
+    assert status == 0
+    assert_close(out, oracle_full(w, append=False), strict=True, what=f"workers={workers}")
+
+
+def test_long_sequence_split_many_ways():
+    w = wl.make_random(8, batch=2, n_q_heads=28, n_kv_heads=4, head_dim=128, page_size=32,
+                       dtype=torch.float16, lens=[20000, 3], device="cuda", poison=True)
+    ref = oracle_full(w, append=False)
+    for workers in (0, 97, 500):
+        out, _, status = run_gpu(w, num_workers=workers, append=False)
+        assert status == 0
+        assert_close(out, ref, strict=True, what=f"workers={workers}")
+
+
+def test_page_permutation_is_bitwise_invariant():
+    """Same dense cache under two page permutations -> identical bits."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, D, P = 6, 16, 4, 128, 16
+    lens = np.array([40, 1, 300, 17, 64, 129])
+    dense_k = wl.to_bits(torch.randn(B, Hkv, 300, D).to(torch.bfloat16))
+    dense_v = wl.to_bits(torch.randn(B, Hkv, 300, D).to(torch.bfloat16))
+    q = torch.randn(B, Hq, D).to(torch.bfloat16).cuda()
+    outs = []
+    for seed in (1, 2):
+        kp, vp, table = wl.scatter_dense(dense_k, dense_v, lens, P, np.random.default_rng(seed),
+                                         extra_pages=5, fill=0x7FC0)
+        kt = torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).cuda()
+        vt = torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16).cuda()
+        out = torch.empty_like(q)
+        ws = pkv.alloc_workspace(B, Hq, Hkv, D, 37)
+        pkv.paged_decode_attention(q, kt, vt, torch.from_numpy(table).cuda(),
+                                   torch.from_numpy(lens.astype(np.int32)).cuda(), 0.088, out, ws,
+                                   num_workers=37)
+        outs.append(out.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    del rng
+
+
+def test_shared_prefix_equals_private_copies_bitwise():
+    w = wl.make("prefix_sharing", seed=3, device="cuda", batch=6)
+    table, lens, _ = to_dev(w)
+    n_prefix = w.prefix_len // w.page_size
+    # give every sequence private copies of the prefix pages
+    extra = w.batch * n_prefix
+    kp = torch.cat([w.k_pool, w.k_pool.new_empty((extra,) + tuple(w.k_pool.shape[1:]))])
+    vp = torch.cat([w.v_pool, w.v_pool.new_empty((extra,) + tuple(w.v_pool.shape[1:]))])
+    priv = w.page_table.copy()
+    for b in range(w.batch):
+        for j in range(n_prefix):
+            new_id = w.num_pages + b * n_prefix + j
+            kp[new_id] = w.k_pool[w.page_table[b, j]]
+            vp[new_id] = w.v_pool[w.page_table[b, j]]
+            priv[b, j] = new_id
+    out_shared = torch.empty_like(w.q)
+    out_priv = torch.empty_like(w.q)
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, out_shared, ws)
+    pkv.paged_decode_attention(w.q, kp, vp, torch.from_numpy(priv).cuda(), lens, w.scale,
+                               out_priv, ws)
+    assert torch.equal(out_shared.view(torch.int16), out_priv.view(torch.int16))
+
+
+def test_rerun_is_bitwise_deterministic():
+    w = wl.make("mixed_append", seed=2, device="cuda", batch=40)
+    a, _, _ = run_gpu(w, append=False)
+    b, _, _ = run_gpu(w, append=False)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_append_then_gather_is_bit_exact():
+    for dt, D, P in ((torch.float16, 128, 32), (torch.bfloat16, 64, 16)):
+        w = wl.make_random(11, batch=7, n_q_heads=8, n_kv_heads=2, head_dim=D, page_size=P,
+                           dtype=dt, lens=[1, 16, 17, 33, 64, 100, 2], device="cuda")
+        w.positions[3] = -1  # padded slot: must not write
+        table, lens, pos = to_dev(w)
+        before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+        pool = pkv.kv_pool_create(w.num_pages, P, 2, D, dt, w.k_pool, w.v_pool)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pkv.kv_append(pool, w.k_new, w.v_new, table, pos, dev_status=st)
+        kp, vp = oracle.kv_append(*before, wl.to_bits(w.k_new), wl.to_bits(w.v_new), w.page_table,
+                                  w.positions)
+        assert np.array_equal(wl.to_bits(w.k_pool), kp)
+        assert np.array_equal(wl.to_bits(w.v_pool), vp)
+        Lmax = int(w.context_lens.max())
+        ko = torch.zeros(7, 2, Lmax, D, dtype=dt, device="cuda")
+        vo = torch.zeros_like(ko)
+        pkv.kv_gather(pool, table, lens, Lmax, ko, vo, dev_status=st)
+        assert int(st.item()) == 0
+        gk = oracle.gather(kp, w.page_table, w.context_lens, Lmax)
+        gv = oracle.gather(vp, w.page_table, w.context_lens, Lmax)
+        assert np.array_equal(wl.to_bits(ko), gk)
+        assert np.array_equal(wl.to_bits(vo), gv)
+        pool.destroy()
+
+
+def test_empty_sequences_give_zeros():
+    w = wl.make_random(13, batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16,
+                       dtype=torch.bfloat16, lens=[0, 5, 0, 40], device="cuda", poison=True)
+    for workers in (0, 1, 3):
+        out, _, status = run_gpu(w, num_workers=workers, append=False)
+        assert status == 0
+        assert_close(out, oracle_full(w, append=False), strict=True)
+        assert (out[0] == 0).all() and (out[2] == 0).all()
+
+
+def test_bad_page_id_is_flagged_and_skipped():
+    w = wl.make_random(17, batch=3, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16,
+                       dtype=torch.bfloat16, lens=[40, 20, 33], device="cuda")
+    good = oracle_full(w, append=False)
+    w.page_table[1, 0] = w.num_pages + 5  # outside the pool
+    w.page_table[2, 1] = -3
+    out, ws, status = run_gpu(w, append=False)
+    assert status & pkv.DEV_BAD_PAGE
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert_close(got[0], good[0], what="untouched sequence")
+    assert np.isfinite(got).all()
+
+
+def test_length_beyond_table_is_flagged_and_clamped():
+    w = wl.make_random(19, batch=2, n_q_heads=4, n_kv_heads=4, head_dim=64, page_size=16,
+                       dtype=torch.float16, lens=[20, 32], device="cuda")
+    ref = oracle_full(w, append=False)
+    w.context_lens[0] = 10_000  # table row holds 2 pages -> clamped to 32 tokens
+    out, ws, status = run_gpu(w, append=False)
+    assert status & pkv.DEV_BAD_LEN
+    assert_close(out[1:], ref[1:])
+    assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+def test_guard_bands_untouched():
+    """Canaries around out and past the end of the workspace stay intact."""
+    w = wl.make("tiny", seed=1, device="cuda")
+    table, lens, _ = to_dev(w)
+    n = w.q.numel()
+    big = torch.full((n + 2048,), 7.0, dtype=w.dtype, device="cuda")
+    out = big[1024:1024 + n].view_as(w.q)
+    need = pkv.paged_decode_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, 3)
+    wsbig = torch.full((need + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws = wsbig[:need]
+    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws,
+                               num_workers=3)
+    torch.cuda.synchronize()
+    assert (big[:1024] == 7.0).all() and (big[1024 + n:] == 7.0).all()
+    assert (wsbig[need:] == 0xA5).all()
+    assert_close(out, oracle_full(w, append=False), strict=True)
+
+
+def test_workspace_too_small_is_rejected():
+    w = wl.make("tiny", seed=1, device="cuda")
+    table, lens, _ = to_dev(w)
+    need = pkv.paged_decode_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale,
+                                   torch.empty_like(w.q), ws)
+    assert e.value.name == "PKV_ERR_WORKSPACE"
+
+
+def test_split_steps_equal_fused_call():
+    """plan + run + combine called one by one == paged_decode_attention."""
+    w = wl.make("llama3_8b", seed=4, device="cuda", batch=8)
+    table, lens, _ = to_dev(w)
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    a = torch.empty_like(w.q)
+    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, a, ws)
+    b = torch.empty_like(w.q)
+    pkv.paged_decode_plan(lens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size,
+                          table.shape[1], ws)
+    pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, b, ws)
+    pkv.paged_decode_combine(b, w.n_kv_heads, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_pool_owned_memory_roundtrip():
+    pool = pkv.kv_pool_create(64, 16, 2, 128, torch.bfloat16)
+    assert pool.k_ptr() and pool.v_ptr() and pool.k_ptr() != pool.v_ptr()
+    ids = pool.alloc_pages(10)
+    assert len(set(ids)) == 10 and pool.free_count() == 54
+    pool.release_pages(ids)
+    assert pool.free_count() == 64
+    pool.destroy()
