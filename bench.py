@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-workers", type=int, default=0)
+    ap.add_argument("--profile-only", action="store_true",
+                    help="only the warm-up and timed steps (for profiler captures): no copy "
+                         "peak, clock sampling, end-to-end leg or CPU baseline")
     return ap.parse_args()
 
 
@@ -323,6 +326,19 @@ def run_ours(args):
         pkv.paged_decode_combine(out, w.n_kv_heads, ws, nw)
 
     peak, peak_kind = measured_peak()
+    if args.profile_only:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        status = pkv.pkv_read_device_status(ws)
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "workload": args.workload,
+                              "steps": args.steps, "warmup": args.warmup,
+                              "device_status": status}))
+        pool.destroy()
+        if dist:
+            dist.destroy_process_group()
+        return 0 if status == 0 else 1
     same_run_copy = copy_peak_gbs(torch, dev)
     sampler = ClockSampler(local)
 

@@ -109,7 +109,7 @@ WsLayout ws_layout(int batch, long long units, int gs, int head_dim, int workers
     w.prefix = off;
     off += align256((size_t)(batch + 1) * 4);
     w.partials = off;
-    off += align256((size_t)(units + workers) * gs * (head_dim + 2) * 4);
+    off += align256((size_t)(units + workers) * pkv::partial_slot_floats(gs, head_dim) * 4);
     w.total = off;
     return w;
 }

@@ -151,6 +151,13 @@ __host__ __device__ constexpr int next_pow2(int x) {
 
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
+// Floats in one partial-state slot: o [gs][D], then m [gs], then l [gs],
+// padded to a multiple of 4 floats so every slot (and every o row) starts on
+// a 16-byte boundary for the float4 stores.
+__host__ __device__ constexpr int partial_slot_floats(int gs, int d) {
+    return (gs * (d + 2) + 3) / 4 * 4;
+}
+
 // Parameters of the decode kernel (one struct, passed by value).
 struct DecodeParams {
     const void* q;            // [B][Hq][D]
@@ -161,7 +168,7 @@ struct DecodeParams {
     const int32_t* prefix;    // [B+1] chunk prefix sums (workspace)
     const WsHeader* hdr;      // total chunks, worker count
     uint32_t* status;
-    float* partials;          // [slots][GS*(D+2)]
+    float* partials;          // [slots][partial_slot_floats(GS, D)]
     void* out;                // [B][Hq][D]
     int table_stride;
     int batch, n_q_heads, n_kv_heads, page_size, num_pages;

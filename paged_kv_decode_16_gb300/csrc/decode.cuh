@@ -397,7 +397,7 @@ decode_kernel(const DecodeParams p) {
                     }
                 }
             } else {
-                float* dst = p.partials + (long long)(d.u + gw) * (GS * (D + 2));
+                float* dst = p.partials + (long long)(d.u + gw) * partial_slot_floats(GS, D);
                 if (r == 0) {
 #pragma unroll
                     for (int g = 0; g < GS; ++g) {

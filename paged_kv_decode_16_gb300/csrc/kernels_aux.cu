@@ -117,7 +117,7 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     const int w_first = (int)(((a + 1) * nw - 1) / total);
     const int w_last = (int)((e * nw - 1) / total);
     if (w_first == w_last) return;
-    const long long stride = (long long)gs * (D + 2);
+    const long long stride = partial_slot_floats(gs, D);
     for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
         const int g = idx / D;
         float M = -INFINITY;

@@ -4,8 +4,12 @@ and the oracle on host copies of the same inputs, and compare.
 Tolerance (decode outputs, fp16/bf16 inputs, fp32 accumulation, output
 rounded to the input dtype):
   * every element: |gpu - ref| <= ATOL + RTOL * |ref|      (ATOL 2e-3, RTOL 1e-2)
-  * strict form, also required on the five named workloads:
+  * strict form, also required on the five named workloads (their outputs are
+    small, |out| < 0.5, so output rounding stays below ATOL):
       max |gpu - ref| <= ATOL  and  max |gpu - ref| / max(|ref|, ATOL/RTOL) <= RTOL
+    The strict form cannot hold for bf16 outputs of magnitude >= 0.5 (half an
+    ulp of bf16 at 1.0 is 0.0039), which short contexts produce; those cases
+    use the per-element form only.
 Append, gather and page-table indexing are compared bit for bit.
 """
 from __future__ import annotations
