@@ -242,7 +242,26 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
                                   pkv_dtype dtype, float scale, void* out, void* workspace,
                                   size_t ws_bytes, int num_workers, pkv_stream stream);
 
-/* Copy the workspace's device status word to *status_out (host).  This call
+/* One whole decode step: the KV append of the step's new rows fused into the
+ * plan launch, then the decode and combine kernels (three launches on
+ * `stream`, chained with programmatic dependent launch).  Equivalent to
+ * kv_append(...) followed by paged_decode_attention(...) on the same stream,
+ * with k_pool / v_pool written in place.  k_new, v_new [batch][n_kv_heads]
+ * [head_dim] and positions int32 [batch] (device) as for kv_append; every
+ * other argument as for paged_decode_attention.  Append errors (bad page id
+ * or position beyond the table row) are reported through the workspace status
+ * read by pkv_read_device_status.  (CacheIR, "Compiler Example": the new K/V
+ * are written into the cache, then paged_attention_decode runs.) */
+pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t* positions,
+                             const void* q, void* k_pool, void* v_pool,
+                             const int32_t* page_table, int table_stride,
+                             const int32_t* context_lens, int batch, int n_q_heads,
+                             int n_kv_heads, int head_dim, int page_size, int num_pages,
+                             pkv_dtype dtype, float scale, void* out, void* workspace,
+                             size_t ws_bytes, int num_workers, pkv_stream stream);
+
+/* Copy the status of the last plan/decode/step call on this workspace to
+ * *status_out (host): the OR of the PKV_DEV_* bits of its kernels.  This call
  * synchronises with the device.  Returns DEVICE_CHECK when any bit is set,
  * OK otherwise (CUDA on a failed copy). */
 pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out);

@@ -22,6 +22,7 @@ __all__ = [
     "PagedKVError", "load_library", "library_path", "pkv_status_string", "pkv_version",
     "Pool", "kv_pool_create", "kv_append", "kv_gather", "paged_decode_workspace_size",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
+    "paged_decode_step",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
 ]
 
@@ -78,6 +79,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "paged_decode_run": ([V, V, V, V, I, I, I, I, I, I, I, I, F, V, V, Z, I, V], I),
         "paged_decode_combine": ([I, I, I, I, I, V, V, Z, I, V], I),
         "paged_decode_attention": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, V], I),
+        "paged_decode_step": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, V],
+                              I),
         "pkv_read_device_status": ([V, ctypes.POINTER(ctypes.c_uint32)], I),
     }
     for name, (args, res) in sig.items():
@@ -297,6 +300,29 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1],
         _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace),
         workspace.numel(), int(num_workers), _stream(stream)), "paged_decode_attention")
+    return out
+
+
+def paged_decode_step(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
+                      q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                      page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                      out: torch.Tensor, workspace: torch.Tensor, num_workers: int = 0,
+                      stream=None) -> torch.Tensor:
+    """One decode step: append k_new/v_new [B, Hkv, D] at positions[b] (fused
+    into the plan launch), then decode attention into out."""
+    B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8)
+    _dev(k_new, "k_new", q.dtype, 3)
+    _dev(v_new, "v_new", q.dtype, 3)
+    _dev(positions, "positions", torch.int32, 1)
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    _check(load_library().paged_decode_step(
+        _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(num_workers),
+        _stream(stream)), "paged_decode_step")
     return out
 
 

@@ -153,13 +153,21 @@ pkv_status check_workspace(const void* workspace, size_t ws_bytes, const DecodeS
 inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
 pkv_status do_plan(const int32_t* context_lens, int batch, int page_size, int table_stride,
-                   int num_workers, void* workspace, const DecodeSetup& s, cudaStream_t stream) {
+                   int num_workers, void* workspace, const DecodeSetup& s,
+                   const pkv::AppendArgs* append, cudaStream_t stream) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    return cuda_status(pkv::launch_plan(
-        context_lens, batch, s.units_per_b, (long long)table_stride * page_size,
-        num_workers > 0 ? s.workers : 0, s.workers_auto, kMinChunksPerWorker,
-        reinterpret_cast<int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<int32_t*>(ws + s.ws.prefix),
-        reinterpret_cast<WsHeader*>(ws), stream));
+    pkv::PlanArgs pa;
+    pa.lens = context_lens;
+    pa.batch = batch;
+    pa.units_per_b = s.units_per_b;
+    pa.cap = (long long)table_stride * page_size;
+    pa.workers_req = num_workers > 0 ? s.workers : 0;
+    pa.workers_auto = s.workers_auto;
+    pa.min_chunks = kMinChunksPerWorker;
+    pa.lens_eff = reinterpret_cast<int32_t*>(ws + s.ws.lens_eff);
+    pa.prefix = reinterpret_cast<int32_t*>(ws + s.ws.prefix);
+    pa.hdr = reinterpret_cast<WsHeader*>(ws);
+    return cuda_status(pkv::launch_plan(pa, append, stream));
 }
 
 pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
@@ -188,8 +196,8 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.sub_groups = s.sub_groups;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int blocks = (s.workers + s.info.warps - 1) / s.info.warps;
-    s.info.fn<<<blocks, s.info.warps * 32, s.info.smem_bytes, stream>>>(p);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(pkv::launch_pdl(s.info.fn, dim3(blocks), dim3(s.info.warps * 32),
+                                       s.info.smem_bytes, stream, p));
 }
 
 pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, void* out,
@@ -201,6 +209,24 @@ pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, v
         reinterpret_cast<const int32_t*>(ws + s.ws.prefix),
         reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<const WsHeader*>(ws),
         out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.group, n_q_heads, stream));
+}
+
+pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t* positions,
+                            const int32_t* table, int table_stride, void* k_pool, void* v_pool,
+                            int n_kv_heads, int head_dim, int page_size, int num_pages) {
+    pkv::AppendArgs a;
+    a.k_new = static_cast<const uint4*>(k_new);
+    a.v_new = static_cast<const uint4*>(v_new);
+    a.positions = positions;
+    a.table = table;
+    a.table_stride = table_stride;
+    a.k_pool = static_cast<uint4*>(k_pool);
+    a.v_pool = static_cast<uint4*>(v_pool);
+    a.n_kv_heads = n_kv_heads;
+    a.vecs = head_dim / 8;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    return a;
 }
 
 }  // namespace
@@ -240,9 +266,10 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
         overlaps(v_new, row_bytes, pool->k, pool_bytes) ||
         overlaps(v_new, row_bytes, pool->v, pool_bytes))
         return PKV_ERR_ALIAS;
-    return cuda_status(pkv::launch_append(k_new, v_new, page_table, table_stride, positions, batch,
-                                          pool->n_kv_heads, pool->head_dim, pool->page_size,
-                                          pool->num_pages, pool->k, pool->v, dev_status,
+    const pkv::AppendArgs a = make_append(k_new, v_new, positions, page_table, table_stride,
+                                          pool->k, pool->v, pool->n_kv_heads, pool->head_dim,
+                                          pool->page_size, pool->num_pages);
+    return cuda_status(pkv::launch_append(a, batch, dev_status,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -331,7 +358,7 @@ pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_hea
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     return do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
-                   reinterpret_cast<cudaStream_t>(stream));
+                   nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_pool,
@@ -393,6 +420,47 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if ((st = do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
+                      nullptr, cs)) != PKV_OK)
+        return st;
+    if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
+                     page_size, num_pages, scale, out, workspace, s, cs)) != PKV_OK)
+        return st;
+    return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
+}
+
+pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t* positions,
+                             const void* q, void* k_pool, void* v_pool,
+                             const int32_t* page_table, int table_stride,
+                             const int32_t* context_lens, int batch, int n_q_heads,
+                             int n_kv_heads, int head_dim, int page_size, int num_pages,
+                             pkv_dtype dtype, float scale, void* out, void* workspace,
+                             size_t ws_bytes, int num_workers, pkv_stream stream) {
+    pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
+                                         context_lens, true, batch, n_q_heads, n_kv_heads,
+                                         head_dim, page_size, num_pages, dtype, scale, out,
+                                         workspace, ws_bytes, num_workers);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!k_new || !v_new || !positions) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    const size_t pool_bytes = (size_t)num_pages * n_kv_heads * page_size * head_dim * 2;
+    const size_t row_bytes = (size_t)batch * n_kv_heads * head_dim * 2;
+    if (overlaps(k_new, row_bytes, k_pool, pool_bytes) ||
+        overlaps(k_new, row_bytes, v_pool, pool_bytes) ||
+        overlaps(v_new, row_bytes, k_pool, pool_bytes) ||
+        overlaps(v_new, row_bytes, v_pool, pool_bytes) ||
+        overlaps(out, (size_t)batch * n_q_heads * head_dim * 2, k_new, row_bytes) ||
+        overlaps(out, (size_t)batch * n_q_heads * head_dim * 2, v_new, row_bytes))
+        return PKV_ERR_ALIAS;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           &s)) != PKV_OK)
+        return st;
+    if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const pkv::AppendArgs a = make_append(k_new, v_new, positions, page_table, table_stride,
+                                          k_pool, v_pool, n_kv_heads, head_dim, page_size,
+                                          num_pages);
+    if ((st = do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s, &a,
                       cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
@@ -403,9 +471,13 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
 
 pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
     if (!workspace || !status_out) return PKV_ERR_INVALID_ARG;
-    uint32_t v = 0;
-    if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    WsHeader h;
+    if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
         return PKV_ERR_CUDA;
+    uint32_t v = h.status;
+    const int n = h.append_slots < 0 ? 0
+                  : (h.append_slots > pkv::kMaxAppendCtas ? pkv::kMaxAppendCtas : h.append_slots);
+    for (int i = 0; i < n; ++i) v |= h.append_status[i];
     *status_out = v;
     return v ? PKV_ERR_DEVICE_CHECK : PKV_OK;
 }

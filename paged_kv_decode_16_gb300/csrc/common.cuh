@@ -18,13 +18,16 @@ namespace pkv {
 constexpr int kChunk = 16;               // tokens per pipeline stage
 constexpr unsigned kFull = 0xffffffffu;  // full-warp shuffle mask
 constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr int kMaxAppendCtas = 32;       // CTAs of the append fused into the plan launch
 
 // Workspace header (first 256 bytes of the decode workspace).
 struct WsHeader {
-    uint32_t status;         // PKV_DEV_* bits of the current call
+    uint32_t status;         // PKV_DEV_* bits of the current call (plan, decode)
     int32_t total_chunks;    // chunks over all (sequence, KV head, sub-group) units
     int32_t num_workers;     // workers that received a non-empty range
-    int32_t pad[61];
+    int32_t append_slots;    // append_status entries written by this call
+    uint32_t append_status[kMaxAppendCtas];  // PKV_DEV_* bits of each fused-append CTA
+    int32_t pad[64 - 4 - kMaxAppendCtas];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -102,6 +105,16 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return pol;
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel in the
+// stream still runs; pdl_wait() blocks until that kernel has completed and its
+// memory is visible (a no-op for a normal launch).  pdl_trigger() lets the
+// next kernel in the stream be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -176,6 +189,25 @@ struct DecodeParams {
     int sub_groups;           // units per KV head (G = sub_groups * GS)
     float scale_log2;         // scale * log2(e)
 };
+
+// Launch a kernel on `stream` with programmatic stream serialization, so that
+// it can be scheduled while the previous kernel of the stream finishes; every
+// kernel of this library calls pdl_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Launch configuration of one decode-kernel instantiation.
 struct DecodeKernelInfo {

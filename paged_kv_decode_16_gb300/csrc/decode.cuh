@@ -159,14 +159,6 @@ decode_kernel(const DecodeParams p) {
     float* pm = reinterpret_cast<float*>(wsm + Lay::kOffM);
     uint64_t* bar = reinterpret_cast<uint64_t*>(wsm + Lay::kOffBar);
 
-    const int total = p.hdr->total_chunks;
-    const int nw = p.hdr->num_workers;
-    const int gw = blockIdx.x * WARPS + warp;
-    if (gw >= nw) return;
-    const int f0 = (int)((long long)gw * total / nw);
-    const int f1 = (int)((long long)(gw + 1) * total / nw);
-    const int n = f1 - f0;
-    if (n <= 0) return;
 
     const int units_per_b = p.n_kv_heads * p.sub_groups;
     const int c = lane & (LPT - 1);     // D slice
@@ -186,6 +178,18 @@ decode_kernel(const DecodeParams p) {
         fence_barrier_init();
     }
     __syncwarp();
+    // the plan (previous kernel of the stream) must be complete from here on
+    pdl_wait();
+    pdl_trigger();
+
+    const int total = p.hdr->total_chunks;
+    const int nw = p.hdr->num_workers;
+    const int gw = blockIdx.x * WARPS + warp;
+    if (gw >= nw) return;
+    const int f0 = (int)((long long)gw * total / nw);
+    const int f1 = (int)((long long)(gw + 1) * total / nw);
+    const int n = f1 - f0;
+    if (n <= 0) return;
 
     // Descriptor windows: wa covers chunks [wbase, wbase+32), wb the next 32.
     int wbase = 0;

@@ -9,19 +9,39 @@
 
 namespace pkv {
 
-cudaError_t launch_plan(const int32_t* lens, int batch, int units_per_b, long long cap,
-                        int workers_req, int workers_auto, int min_chunks, int32_t* lens_eff,
-                        int32_t* prefix, WsHeader* hdr, cudaStream_t stream);
+struct PlanArgs {
+    const int32_t* lens;   // [B] context lengths (caller)
+    int batch;
+    int units_per_b;       // Hkv * sub_groups
+    long long cap;         // table_stride * page_size
+    int workers_req;       // > 0: caller's worker count
+    int workers_auto;      // automatic worker count of this kernel on this device
+    int min_chunks;        // automatic mode: at least this many chunks per worker
+    int32_t* lens_eff;     // [B] clamped lengths (workspace)
+    int32_t* prefix;       // [B+1] chunk prefix sums (workspace)
+    WsHeader* hdr;
+};
+
+struct AppendArgs {
+    const uint4* k_new;    // [B][Hkv][D] as 16-byte vectors
+    const uint4* v_new;
+    const int32_t* positions;
+    const int32_t* table;
+    int table_stride;
+    uint4* k_pool;
+    uint4* v_pool;
+    int n_kv_heads, vecs, page_size, num_pages;  // vecs = D / 8
+};
+
+// Plan, optionally with the append fused into the same launch.
+cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream_t stream);
 
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
                            int group, int n_q_heads, cudaStream_t stream);
 
-cudaError_t launch_append(const void* k_new, const void* v_new, const int32_t* table,
-                          int table_stride, const int32_t* positions, int batch, int n_kv_heads,
-                          int head_dim, int page_size, int num_pages, void* k_pool, void* v_pool,
-                          uint32_t* status, cudaStream_t stream);
+cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status, cudaStream_t stream);
 
 cudaError_t launch_gather(const void* k_pool, const void* v_pool, const int32_t* table,
                           int table_stride, const int32_t* lens, int batch, int n_kv_heads,

@@ -267,3 +267,49 @@ def test_pool_owned_memory_roundtrip():
     pool.release_pages(ids)
     assert pool.free_count() == 64
     pool.destroy()
+
+
+def test_fused_step_equals_append_then_attention():
+    """paged_decode_step == kv_append + paged_decode_attention, bit for bit
+    (output and both pools), and matches the oracle."""
+    w1 = wl.make("mixed_append", seed=6, device="cuda", batch=48)
+    w2 = wl.make("mixed_append", seed=6, device="cuda", batch=48)
+    before = (wl.to_bits(w1.k_pool), wl.to_bits(w1.v_pool))
+    out1, _, st1 = run_gpu(w1)  # separate calls
+    assert st1 == 0
+    table, lens, pos = to_dev(w2)
+    out2 = torch.empty_like(w2.q)
+    ws = pkv.alloc_workspace(w2.batch, w2.n_q_heads, w2.n_kv_heads, w2.head_dim)
+    pkv.paged_decode_step(w2.k_new, w2.v_new, pos, w2.q, w2.k_pool, w2.v_pool, table, lens,
+                          w2.scale, out2, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(ws) == 0
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(w1.k_pool.view(torch.int16), w2.k_pool.view(torch.int16))
+    assert torch.equal(w1.v_pool.view(torch.int16), w2.v_pool.view(torch.int16))
+    assert_close(out2, oracle_full(w2, before), strict=True)
+
+
+def test_fused_step_reports_bad_append_and_skips_padding():
+    w = wl.make_random(21, batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16,
+                       dtype=torch.bfloat16, lens=[5, 17, 40, 3], device="cuda")
+    before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+    w.positions[1] = -1                        # padded slot: no write
+    w.positions[2] = w.page_table.shape[1] * 16 + 3  # beyond the table row: flagged, skipped
+    table, lens, pos = to_dev(w)
+    out = torch.empty_like(w.q)
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    pkv.paged_decode_step(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens, w.scale,
+                          out, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(ws) & pkv.DEV_BAD_LEN
+    pos_ok = w.positions.copy()
+    pos_ok[2] = -1
+    kp, vp = oracle.kv_append(*before, wl.to_bits(w.k_new), wl.to_bits(w.v_new), w.page_table,
+                              pos_ok)
+    assert np.array_equal(wl.to_bits(w.k_pool), kp) and np.array_equal(wl.to_bits(w.v_pool), vp)
+    # a clean call on the same workspace clears the status
+    pkv.paged_decode_step(w.k_new, w.v_new, torch.from_numpy(pos_ok).cuda(), w.q, w.k_pool,
+                          w.v_pool, table, lens, w.scale, out, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(ws) == 0
