@@ -49,6 +49,7 @@ UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ["paged_kv_decode_16_gb300/csrc/decode.cuh",
+                  "paged_kv_decode_16_gb300/csrc/decode_mma.cuh",
                   "paged_kv_decode_16_gb300/csrc/common.cuh"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama3_8b_shape.md")
 
@@ -64,6 +65,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-workers", type=int, default=0)
+    ap.add_argument("--variant", choices=["auto", "cuda_cores", "tensor_cores"], default="auto",
+                    help="decode kernel (auto = tensor cores)")
     ap.add_argument("--profile-only", action="store_true",
                     help="only the warm-up and timed steps (for profiler captures): no copy "
                          "peak, clock sampling, end-to-end leg or CPU baseline")
@@ -312,24 +315,27 @@ def run_ours(args):
                               w.k_pool, w.v_pool)
     out = torch.empty_like(w.q)
     nw = args.num_workers
-    ws = pkv.alloc_workspace(B, w.n_q_heads, w.n_kv_heads, w.head_dim, nw, device=dev)
+    var = {"auto": pkv.VARIANT_AUTO, "cuda_cores": pkv.VARIANT_CUDA_CORES,
+           "tensor_cores": pkv.VARIANT_TENSOR_CORES}[args.variant]
+    ws = pkv.alloc_workspace(B, w.n_q_heads, w.n_kv_heads, w.head_dim, nw, device=dev,
+                             variant=var)
     stream = torch.cuda.current_stream(dev)
     by = step_bytes(w)
 
     def step():
         # one C-ABI call: append fused into the plan launch, decode, combine
         pkv.paged_decode_step(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens,
-                              w.scale, out, ws, nw)
+                              w.scale, out, ws, nw, variant=var)
 
     def split_step(ev0, ev1):
         # the same work as separate calls, with events around the decode kernel
         pkv.kv_append(pool, w.k_new, w.v_new, table, pos)
         pkv.paged_decode_plan(lens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size,
-                              table.shape[1], ws, nw)
+                              table.shape[1], ws, nw, variant=var)
         ev0.record(stream)
-        pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, out, ws, nw)
+        pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, out, ws, nw, variant=var)
         ev1.record(stream)
-        pkv.paged_decode_combine(out, w.n_kv_heads, ws, nw)
+        pkv.paged_decode_combine(out, w.n_kv_heads, ws, nw, variant=var)
 
     peak, peak_kind = measured_peak()
     if args.profile_only:
@@ -404,7 +410,7 @@ def run_ours(args):
                          (ps_d, ps_h)):
             dst.copy_(src, non_blocking=True)
         pkv.paged_decode_step(kn_d, vn_d, ps_d, q_d, w.k_pool, w.v_pool, tb_d, ln_d, w.scale,
-                              out, ws, nw)
+                              out, ws, nw, variant=var)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -436,7 +442,7 @@ def run_ours(args):
             "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
             "context_lens": f"uniform [512, 4096], mean {float(w.context_lens.mean()):.0f}"
             if args.workload == "llama3_8b" else f"mean {float(w.context_lens.mean()):.0f}",
-            "seed": args.seed, "num_workers": nw or "auto",
+            "seed": args.seed, "num_workers": nw or "auto", "variant": args.variant,
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": (f"inputs larger than L2: {by['kv_unique'] / 2**20:.0f} MiB of K/V per step "
                    f"vs 129 MB L2; no flush") if by["kv_unique"] > L2_BYTES
@@ -453,7 +459,9 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "pkv::decode_kernel", "algorithmic_bytes": by["decode"],
+                     "kernel": "pkv::decode_kernel (CUDA cores)"
+                     if var == pkv.VARIANT_CUDA_CORES else "pkv::decode_mma_kernel (tensor cores)",
+                     "algorithmic_bytes": by["decode"],
                      "timing": f"CUDA events around paged_decode_run on its stream, mean of "
                                f"{KD} steps run right after the timed region"},
         "e2e": {"value": world * by["step"] / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,

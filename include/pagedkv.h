@@ -193,54 +193,73 @@ pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_
  * count, never on physical page ids, so permuting pages gives bitwise equal
  * results.
  *
- * num_workers: 0 = automatic (a multiple of the GPU's SM count, capped so
- * each worker gets several chunks); n > 0 = at most n workers (n = 1: one
- * worker walks the whole batch, no partial states).
+ * num_workers: 0 = automatic (the GPU's SM count x resident warps of the
+ * kernel, capped so each worker gets at least 4 chunks); n > 0 = at most n
+ * workers (n = 1: one worker walks the whole batch, no partial states).
+ *
+ * variant: which decode kernel computes the chunks.  Every call of one decode
+ * (workspace size, plan, run, combine) must pass the same num_workers and
+ * variant: both fix the worker count and the query sub-group size.
  * ------------------------------------------------------------------------ */
+typedef enum pkv_decode_variant {
+    PKV_VARIANT_AUTO = 0,          /* the tensor-core kernel */
+    PKV_VARIANT_CUDA_CORES = 1,    /* fp32 FMA on CUDA cores; K/V chunks by 1-D bulk copies;
+                                      query sub-groups of at most 8 heads */
+    PKV_VARIANT_TENSOR_CORES = 2   /* q.k and p.v by warp MMA (m16n8k16, fp32 accumulate);
+                                      K/V chunks by swizzled 2-D tensor copies; query
+                                      sub-groups of at most 16 heads; P enters the p.v
+                                      product in the input dtype (bf16: as a high part
+                                      plus a bf16 residual, two MMAs) */
+} pkv_decode_variant;
 
 /* Bytes of device workspace paged_decode_attention needs for these shapes on
- * the current device with this num_workers.  *bytes receives the size.
- * Errors: INVALID_ARG, UNSUPPORTED, CUDA (device query failed). */
+ * the current device with this num_workers and variant.  *bytes receives the
+ * size.  Errors: INVALID_ARG, UNSUPPORTED, CUDA (device query failed). */
 pkv_status paged_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                       int num_workers, size_t* bytes);
+                                       int num_workers, pkv_decode_variant variant,
+                                       size_t* bytes);
 
 /* Plan step: validates context_lens on the device (clamping to the table row,
- * flagging PKV_DEV_BAD_LEN), clears the status word, and writes the chunk
+ * flagging PKV_DEV_BAD_LEN), resets the status word, and writes the chunk
  * prefix sums and the worker count into the workspace.  One kernel (one CTA). */
 pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_heads,
                              int n_kv_heads, int head_dim, int page_size, int table_stride,
-                             int num_workers, void* workspace, size_t ws_bytes,
-                             pkv_stream stream);
+                             int num_workers, pkv_decode_variant variant, void* workspace,
+                             size_t ws_bytes, pkv_stream stream);
 
-/* Main step on a workspace prepared by paged_decode_plan with the same shapes:
- * the decode kernel (persistent grid of workers; TMA bulk copies of K/V chunks
- * into shared memory, fp32 online softmax).  Writes out for every (sequence,
- * KV head) finished by one worker and partial states for the rest. */
+/* Main step on a workspace prepared by paged_decode_plan with the same shapes,
+ * num_workers and variant: the decode kernel (persistent grid of workers;
+ * asynchronous copies of K/V chunks into shared memory, fp32 online softmax).
+ * Writes out for every (sequence, KV head) finished by one worker and partial
+ * states for the rest.  Pools of more than 2^31 - 1 rows (num_pages *
+ * n_kv_heads * page_size) are UNSUPPORTED by the tensor-core variant. */
 pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* page_table, int table_stride, int batch,
                             int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                             int num_pages, pkv_dtype dtype, float scale, void* out,
                             void* workspace, size_t ws_bytes, int num_workers,
-                            pkv_stream stream);
+                            pkv_decode_variant variant, pkv_stream stream);
 
 /* Combine step: for every (sequence, KV head) split over several workers,
  * out = sum_i w_i o_i / sum_i w_i l_i with w_i = 2^(m_i - max m) (partials
  * keep m in base-2 units); writes zeros for sequences with no tokens. */
 pkv_status paged_decode_combine(int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                 pkv_dtype dtype, void* out, void* workspace, size_t ws_bytes,
-                                int num_workers, pkv_stream stream);
+                                int num_workers, pkv_decode_variant variant, pkv_stream stream);
 
-/* The whole decode: plan + run + combine (three kernels on `stream`).
- * q, k_pool, v_pool, page_table, context_lens, out, workspace (device).
- * out must not overlap q, the pools, the table, the lengths or the workspace
- * (ALIAS).  ws_bytes >= paged_decode_workspace_size(...) (else WORKSPACE).
- * scale multiplies q.k before the softmax (usually 1/sqrt(head_dim)). */
+/* The whole decode: plan + run + combine (three kernels on `stream`, chained
+ * with programmatic dependent launch).  q, k_pool, v_pool, page_table,
+ * context_lens, out, workspace (device).  out must not overlap q, the pools,
+ * the table, the lengths or the workspace (ALIAS).  ws_bytes >=
+ * paged_decode_workspace_size(...) (else WORKSPACE).  scale multiplies q.k
+ * before the softmax (usually 1/sqrt(head_dim)). */
 pkv_status paged_decode_attention(const void* q, const void* k_pool, const void* v_pool,
                                   const int32_t* page_table, int table_stride,
                                   const int32_t* context_lens, int batch, int n_q_heads,
                                   int n_kv_heads, int head_dim, int page_size, int num_pages,
                                   pkv_dtype dtype, float scale, void* out, void* workspace,
-                                  size_t ws_bytes, int num_workers, pkv_stream stream);
+                                  size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                                  pkv_stream stream);
 
 /* One whole decode step: the KV append of the step's new rows fused into the
  * plan launch, then the decode and combine kernels (three launches on
@@ -258,7 +277,8 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                              const int32_t* context_lens, int batch, int n_q_heads,
                              int n_kv_heads, int head_dim, int page_size, int num_pages,
                              pkv_dtype dtype, float scale, void* out, void* workspace,
-                             size_t ws_bytes, int num_workers, pkv_stream stream);
+                             size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                             pkv_stream stream);
 
 /* Copy the status of the last plan/decode/step call on this workspace to
  * *status_out (host): the OR of the PKV_DEV_* bits of its kernels.  This call

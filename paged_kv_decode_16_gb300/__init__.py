@@ -24,6 +24,7 @@ __all__ = [
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
+    "VARIANT_AUTO", "VARIANT_CUDA_CORES", "VARIANT_TENSOR_CORES",
 ]
 
 PKV_OK = 0
@@ -31,6 +32,8 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 3: "PKV_ERR_ALIAS", 4: "PKV_ERR_OUT_OF_PAGES", 5: "PKV_ERR_WORKSPACE",
                 6: "PKV_ERR_CUDA", 7: "PKV_ERR_DEVICE_CHECK", 8: "PKV_ERR_REFCOUNT"}
 DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
+# decode kernels (pkv_decode_variant)
+VARIANT_AUTO, VARIANT_CUDA_CORES, VARIANT_TENSOR_CORES = 0, 1, 2
 _DT = {torch.float16: 0, torch.bfloat16: 1}
 
 _lib = None
@@ -74,13 +77,14 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "kv_pool_info": ([V, V, V, V, V, V], I),
         "kv_append": ([V, V, V, V, I, V, I, V, V], I),
         "kv_gather": ([V, V, I, V, I, I, V, V, V, V], I),
-        "paged_decode_workspace_size": ([I, I, I, I, I, ctypes.POINTER(Z)], I),
-        "paged_decode_plan": ([V, I, I, I, I, I, I, I, V, Z, V], I),
-        "paged_decode_run": ([V, V, V, V, I, I, I, I, I, I, I, I, F, V, V, Z, I, V], I),
-        "paged_decode_combine": ([I, I, I, I, I, V, V, Z, I, V], I),
-        "paged_decode_attention": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, V], I),
-        "paged_decode_step": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, V],
-                              I),
+        "paged_decode_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
+        "paged_decode_plan": ([V, I, I, I, I, I, I, I, I, V, Z, V], I),
+        "paged_decode_run": ([V, V, V, V, I, I, I, I, I, I, I, I, F, V, V, Z, I, I, V], I),
+        "paged_decode_combine": ([I, I, I, I, I, V, V, Z, I, I, V], I),
+        "paged_decode_attention": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, I, V],
+                                   I),
+        "paged_decode_step": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, I,
+                               V], I),
         "pkv_read_device_status": ([V, ctypes.POINTER(ctypes.c_uint32)], I),
     }
     for name, (args, res) in sig.items():
@@ -256,18 +260,18 @@ def kv_gather(pool: Pool, page_table: torch.Tensor, context_lens: torch.Tensor, 
 
 
 def paged_decode_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
-                                num_workers: int = 0) -> int:
+                                num_workers: int = 0, variant: int = VARIANT_AUTO) -> int:
     n = ctypes.c_size_t()
     _check(load_library().paged_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
-                                                      num_workers, ctypes.byref(n)),
+                                                      num_workers, variant, ctypes.byref(n)),
            "paged_decode_workspace_size")
     return n.value
 
 
 def alloc_workspace(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
-                    num_workers: int = 0, device=None) -> torch.Tensor:
+                    num_workers: int = 0, device=None, variant: int = VARIANT_AUTO) -> torch.Tensor:
     """A torch uint8 buffer of the size paged_decode_attention needs (256-B aligned)."""
-    n = paged_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, num_workers)
+    n = paged_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, num_workers, variant)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
 
@@ -290,7 +294,7 @@ def _decode_shapes(q, k_pool, v_pool, page_table, out):
 def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                            page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
                            out: torch.Tensor, workspace: torch.Tensor, num_workers: int = 0,
-                           stream=None) -> torch.Tensor:
+                           stream=None, variant: int = VARIANT_AUTO) -> torch.Tensor:
     """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over context_lens[b]
     tokens read through page_table[b] (plan + decode + combine kernels)."""
     B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
@@ -299,7 +303,8 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     _check(load_library().paged_decode_attention(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1],
         _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace),
-        workspace.numel(), int(num_workers), _stream(stream)), "paged_decode_attention")
+        workspace.numel(), int(num_workers), int(variant), _stream(stream)),
+        "paged_decode_attention")
     return out
 
 
@@ -307,7 +312,7 @@ def paged_decode_step(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch
                       q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                       page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
                       out: torch.Tensor, workspace: torch.Tensor, num_workers: int = 0,
-                      stream=None) -> torch.Tensor:
+                      stream=None, variant: int = VARIANT_AUTO) -> torch.Tensor:
     """One decode step: append k_new/v_new [B, Hkv, D] at positions[b] (fused
     into the plan launch), then decode attention into out."""
     B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
@@ -322,39 +327,39 @@ def paged_decode_step(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch
         _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q), _ptr(k_pool), _ptr(v_pool),
         _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
         float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(num_workers),
-        _stream(stream)), "paged_decode_step")
+        int(variant), _stream(stream)), "paged_decode_step")
     return out
 
 
 def paged_decode_plan(context_lens: torch.Tensor, n_q_heads: int, n_kv_heads: int,
                       head_dim: int, page_size: int, table_stride: int, workspace: torch.Tensor,
-                      num_workers: int = 0, stream=None) -> None:
+                      num_workers: int = 0, stream=None, variant: int = VARIANT_AUTO) -> None:
     _dev(context_lens, "context_lens", torch.int32, 1)
     _dev(workspace, "workspace", torch.uint8)
     _check(load_library().paged_decode_plan(
         _ptr(context_lens), context_lens.shape[0], n_q_heads, n_kv_heads, head_dim, page_size,
-        table_stride, int(num_workers), _ptr(workspace), workspace.numel(), _stream(stream)),
-        "paged_decode_plan")
+        table_stride, int(num_workers), int(variant), _ptr(workspace), workspace.numel(),
+        _stream(stream)), "paged_decode_plan")
 
 
 def paged_decode_run(q, k_pool, v_pool, page_table, scale: float, out, workspace,
-                     num_workers: int = 0, stream=None) -> None:
+                     num_workers: int = 0, stream=None, variant: int = VARIANT_AUTO) -> None:
     B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
     _dev(workspace, "workspace", torch.uint8)
     _check(load_library().paged_decode_run(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1], B, Hq, Hkv,
         D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
-        int(num_workers), _stream(stream)), "paged_decode_run")
+        int(num_workers), int(variant), _stream(stream)), "paged_decode_run")
 
 
 def paged_decode_combine(out: torch.Tensor, n_kv_heads: int, workspace: torch.Tensor,
-                         num_workers: int = 0, stream=None) -> None:
+                         num_workers: int = 0, stream=None, variant: int = VARIANT_AUTO) -> None:
     _dev(out, "out", None, 3)
     _dev(workspace, "workspace", torch.uint8)
     B, Hq, D = out.shape
     _check(load_library().paged_decode_combine(
         B, Hq, n_kv_heads, D, _dtype_code(out), _ptr(out), _ptr(workspace), workspace.numel(),
-        int(num_workers), _stream(stream)), "paged_decode_combine")
+        int(num_workers), int(variant), _stream(stream)), "paged_decode_combine")
 
 
 def pkv_read_device_status(workspace: torch.Tensor) -> int:

@@ -1,17 +1,20 @@
 // api.cu -- the C ABI (include/pagedkv.h): host-side validation, workspace
-// layout, and the stream-ordered launches of the plan, decode and combine
-// kernels, the KV append and the gather.
+// layout, tensor-map encoding, and the stream-ordered launches of the plan,
+// decode and combine kernels, the KV append and the gather.
 //
 // Conventions follow Experimental LibTorch prefix cache, "Identity, ownership
 // and output behavior": work is ordered on the caller's stream, the caller
 // owns every buffer, the host validates shapes and rejects aliased output
 // before anything is launched, and failures are reported, never thrown.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "common.cuh"
@@ -21,6 +24,7 @@
 namespace {
 
 using pkv::DecodeKernelInfo;
+using pkv::DecodeMmaInfo;
 using pkv::WsHeader;
 
 constexpr int kMinChunksPerWorker = 4;  // automatic worker count: at least this many chunks each
@@ -35,10 +39,12 @@ inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// G = sub_groups * gs with gs <= 8 (the widest group one warp serves); the
-// smallest number of sub-groups that divides G.
-inline bool split_group(int group, int* sub_groups, int* gs) {
-    for (int ns = (group + 7) / 8; ns <= group; ++ns) {
+inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// G = sub_groups * gs with gs <= max_gs (the widest group one warp serves):
+// the smallest number of sub-groups that divides G.
+inline bool split_group(int group, int max_gs, int* sub_groups, int* gs) {
+    for (int ns = (group + max_gs - 1) / max_gs; ns <= group; ++ns) {
         if (group % ns == 0) {
             *sub_groups = ns;
             *gs = group / ns;
@@ -57,9 +63,40 @@ pkv_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     return PKV_OK;
 }
 
-DecodeKernelInfo decode_info(pkv_dtype dtype, int head_dim, int gs) {
-    return dtype == PKV_BF16 ? pkv::decode_info_bf16(head_dim, gs)
-                             : pkv::decode_info_f16(head_dim, gs);
+inline bool valid_variant(int v) {
+    return v == PKV_VARIANT_AUTO || v == PKV_VARIANT_CUDA_CORES || v == PKV_VARIANT_TENSOR_CORES;
+}
+
+// The decode kernel chosen for a call: an entry of either instantiation table.
+struct KernelPick {
+    int variant = 0;  // PKV_VARIANT_CUDA_CORES or PKV_VARIANT_TENSOR_CORES
+    DecodeKernelInfo cc{};
+    DecodeMmaInfo mma{};
+    const void* fn() const {
+        return variant == PKV_VARIANT_TENSOR_CORES ? reinterpret_cast<const void*>(mma.fn)
+                                                   : reinterpret_cast<const void*>(cc.fn);
+    }
+    int warps() const { return variant == PKV_VARIANT_TENSOR_CORES ? mma.warps : cc.warps; }
+    int smem() const {
+        return variant == PKV_VARIANT_TENSOR_CORES ? mma.smem_bytes : cc.smem_bytes;
+    }
+};
+
+KernelPick pick_kernel(pkv_dtype dtype, int head_dim, int variant, int gs) {
+    KernelPick k;
+    k.variant = variant;
+    if (variant == PKV_VARIANT_TENSOR_CORES) {
+        if (dtype == PKV_BF16)
+            k.mma = head_dim == 128 ? pkv::decode_mma_info_bf16_d128(gs)
+                                    : pkv::decode_mma_info_bf16_d64(gs);
+        else
+            k.mma = head_dim == 128 ? pkv::decode_mma_info_f16_d128(gs)
+                                    : pkv::decode_mma_info_f16_d64(gs);
+    } else {
+        k.cc = dtype == PKV_BF16 ? pkv::decode_info_bf16(head_dim, gs)
+                                 : pkv::decode_info_f16(head_dim, gs);
+    }
+    return k;
 }
 
 // Per (device, kernel): dynamic shared memory opt-in done, and the automatic
@@ -67,10 +104,10 @@ DecodeKernelInfo decode_info(pkv_dtype dtype, int head_dim, int gs) {
 std::mutex g_mu;
 std::map<std::pair<int, const void*>, int> g_auto_workers;
 
-pkv_status prepare_kernel(const DecodeKernelInfo& info, int* auto_workers) {
+pkv_status prepare_kernel(const KernelPick& k, int* auto_workers) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(info.fn));
+    const auto key = std::make_pair(dev, k.fn());
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_auto_workers.find(key);
@@ -82,15 +119,13 @@ pkv_status prepare_kernel(const DecodeKernelInfo& info, int* auto_workers) {
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PKV_ERR_CUDA;
-    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(info.fn),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             info.smem_bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(k.fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem()) !=
+        cudaSuccess)
         return PKV_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, reinterpret_cast<const void*>(info.fn), info.warps * 32,
-            info.smem_bytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn(), k.warps() * 32,
+                                                      k.smem()) != cudaSuccess)
         return PKV_ERR_CUDA;
-    const int workers = sms * (per_sm > 0 ? per_sm : 1) * info.warps;
+    const int workers = sms * (per_sm > 0 ? per_sm : 1) * k.warps();
     std::lock_guard<std::mutex> lk(g_mu);
     g_auto_workers[key] = workers;
     *auto_workers = workers;
@@ -114,29 +149,36 @@ WsLayout ws_layout(int batch, long long units, int gs, int head_dim, int workers
     return w;
 }
 
-// Everything the three decode steps derive from the shapes.
+// Everything the decode steps derive from the shapes and the variant.
 struct DecodeSetup {
     int group, sub_groups, gs, units_per_b;
     long long units;
     int workers;       // launched workers (upper bound of the plan's count)
     int workers_auto;  // automatic count for this kernel on this device
-    DecodeKernelInfo info;
+    KernelPick kernel;
     WsLayout ws;
 };
 
+// AUTO picks the tensor-core kernel; CUDA cores on request.
+int resolve_variant(int variant) {
+    return variant == PKV_VARIANT_AUTO ? PKV_VARIANT_TENSOR_CORES : variant;
+}
+
 pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
-                        pkv_dtype dtype, int num_workers, DecodeSetup* s) {
+                        pkv_dtype dtype, int num_workers, int variant, DecodeSetup* s) {
     pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
     if (st != PKV_OK) return st;
     if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-    if (num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if (num_workers < 0 || !valid_variant(variant)) return PKV_ERR_INVALID_ARG;
+    const int v = resolve_variant(variant);
     s->group = n_q_heads / n_kv_heads;
-    if (!split_group(s->group, &s->sub_groups, &s->gs)) return PKV_ERR_UNSUPPORTED;
+    const int max_gs = v == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
+    if (!split_group(s->group, max_gs, &s->sub_groups, &s->gs)) return PKV_ERR_UNSUPPORTED;
     s->units_per_b = n_kv_heads * s->sub_groups;
     s->units = (long long)batch * s->units_per_b;
-    s->info = decode_info(dtype, head_dim, s->gs);
-    if (!s->info.fn) return PKV_ERR_UNSUPPORTED;
-    st = prepare_kernel(s->info, &s->workers_auto);
+    s->kernel = pick_kernel(dtype, head_dim, v, s->gs);
+    if (!s->kernel.fn()) return PKV_ERR_UNSUPPORTED;
+    st = prepare_kernel(s->kernel, &s->workers_auto);
     if (st != PKV_OK) return st;
     s->workers = num_workers > 0 ? num_workers : s->workers_auto;
     s->ws = ws_layout(batch, s->units, s->gs, head_dim, s->workers);
@@ -150,7 +192,64 @@ pkv_status check_workspace(const void* workspace, size_t ws_bytes, const DecodeS
     return PKV_OK;
 }
 
-inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+// --- tensor maps of the pools (tensor-core variant) ------------------------
+// A pool [NP][Hkv][P][D] is seen as a 2-D tensor of NP*Hkv*P rows of D
+// elements; a box is 16 rows x 64 elements (128 bytes) with the 128-byte
+// swizzle.  Encoded through the driver entry point (no libcuda link), cached
+// per (address, rows, D, dtype).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+std::mutex g_map_mu;
+std::map<std::tuple<const void*, long long, int, int>, CUtensorMap> g_maps;
+
+pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dtype,
+                    CUtensorMap* out) {
+    const auto key = std::make_tuple(pool, rows, head_dim, (int)dtype);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return PKV_OK;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    CUtensorMap m;
+    memset(&m, 0, sizeof(m));
+    const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)pkv::kChunk};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (fn(&m, dt, 2, const_cast<void*>(pool), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() > 256) g_maps.clear();
+    g_maps[key] = m;
+    *out = m;
+    return PKV_OK;
+}
 
 pkv_status do_plan(const int32_t* context_lens, int batch, int page_size, int table_stride,
                    int num_workers, void* workspace, const DecodeSetup& s,
@@ -171,9 +270,9 @@ pkv_status do_plan(const int32_t* context_lens, int batch, int page_size, int ta
 }
 
 pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
-                  int table_stride, int batch, int n_q_heads, int n_kv_heads, int page_size,
-                  int num_pages, float scale, void* out, void* workspace, const DecodeSetup& s,
-                  cudaStream_t stream) {
+                  int table_stride, int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                  int page_size, int num_pages, pkv_dtype dtype, float scale, void* out,
+                  void* workspace, const DecodeSetup& s, cudaStream_t stream) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     pkv::DecodeParams p;
     p.q = q;
@@ -195,9 +294,20 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.group = s.group;
     p.sub_groups = s.sub_groups;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int blocks = (s.workers + s.info.warps - 1) / s.info.warps;
-    return cuda_status(pkv::launch_pdl(s.info.fn, dim3(blocks), dim3(s.info.warps * 32),
-                                       s.info.smem_bytes, stream, p));
+    const int blocks = (s.workers + s.kernel.warps() - 1) / s.kernel.warps();
+    if (s.kernel.variant == PKV_VARIANT_TENSOR_CORES) {
+        const long long rows = (long long)num_pages * n_kv_heads * page_size;
+        if (rows > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // 32-bit tensor row coordinate
+        CUtensorMap km, vm;
+        pkv_status st = pool_map(k_pool, rows, head_dim, dtype, &km);
+        if (st == PKV_OK) st = pool_map(v_pool, rows, head_dim, dtype, &vm);
+        if (st != PKV_OK) return st;
+        return cuda_status(pkv::launch_pdl(s.kernel.mma.fn, dim3(blocks),
+                                           dim3(s.kernel.mma.warps * 32), s.kernel.mma.smem_bytes,
+                                           stream, p, km, vm));
+    }
+    return cuda_status(pkv::launch_pdl(s.kernel.cc.fn, dim3(blocks), dim3(s.kernel.cc.warps * 32),
+                                       s.kernel.cc.smem_bytes, stream, p));
 }
 
 pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, void* out,
@@ -229,6 +339,39 @@ pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t*
     return a;
 }
 
+// Host-only argument checks of a decode call (no CUDA call is made), in the
+// order: shapes, scalars, pointers, alignment, aliasing of out.
+pkv_status validate_decode_args(const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* page_table, int table_stride,
+                                const int32_t* context_lens, bool need_lens, int batch,
+                                int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                                int num_pages, pkv_dtype dtype, float scale, const void* out,
+                                const void* workspace, size_t ws_bytes, int num_workers,
+                                int variant) {
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
+    if (st != PKV_OK) return st;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (num_pages <= 0 || table_stride <= 0 || num_workers < 0 || !valid_variant(variant))
+        return PKV_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_pool || !v_pool || !page_table || !out || (need_lens && !context_lens))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    const size_t qo_bytes = (size_t)batch * n_q_heads * head_dim * 2;
+    const size_t pool_bytes = (size_t)num_pages * n_kv_heads * page_size * head_dim * 2;
+    const size_t table_bytes = (size_t)batch * table_stride * 4;
+    if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_pool, pool_bytes) ||
+        overlaps(out, qo_bytes, v_pool, pool_bytes) ||
+        overlaps(out, qo_bytes, page_table, table_bytes) ||
+        (need_lens && overlaps(out, qo_bytes, context_lens, (size_t)batch * 4)) ||
+        overlaps(out, qo_bytes, workspace, ws_bytes))
+        return PKV_ERR_ALIAS;
+    return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -248,7 +391,7 @@ const char* pkv_status_string(pkv_status s) {
     return "unknown status";
 }
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 200; }
 
 pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
                      const int32_t* page_table, int table_stride, const int32_t* positions,
@@ -287,7 +430,8 @@ pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_
     if (overlaps(k_out, out_bytes, pool->k, pool_bytes) ||
         overlaps(k_out, out_bytes, pool->v, pool_bytes) ||
         overlaps(v_out, out_bytes, pool->k, pool_bytes) ||
-        overlaps(v_out, out_bytes, pool->v, pool_bytes) || overlaps(k_out, out_bytes, v_out, out_bytes))
+        overlaps(v_out, out_bytes, pool->v, pool_bytes) ||
+        overlaps(k_out, out_bytes, v_out, out_bytes))
         return PKV_ERR_ALIAS;
     return cuda_status(pkv::launch_gather(pool->k, pool->v, page_table, table_stride, context_lens,
                                           batch, pool->n_kv_heads, pool->head_dim, pool->page_size,
@@ -296,65 +440,35 @@ pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_
 }
 
 pkv_status paged_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                       int num_workers, size_t* bytes) {
+                                       int num_workers, pkv_decode_variant variant,
+                                       size_t* bytes) {
     if (!bytes) return PKV_ERR_INVALID_ARG;
     *bytes = 0;
     pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, 16);
     if (st != PKV_OK) return st;
-    if (num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if (num_workers < 0 || !valid_variant(variant)) return PKV_ERR_INVALID_ARG;
     DecodeSetup s;
     if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, PKV_BF16, num_workers,
-                           &s)) != PKV_OK)
+                           variant, &s)) != PKV_OK)
         return st;
     *bytes = s.ws.total;
     return PKV_OK;
 }
 
-// Host-only argument checks of a decode call (no CUDA call is made), in the
-// order: shapes, scalars, pointers, alignment, aliasing of out.
-static pkv_status validate_decode_args(const void* q, const void* k_pool, const void* v_pool,
-                                       const int32_t* page_table, int table_stride,
-                                       const int32_t* context_lens, bool need_lens, int batch,
-                                       int n_q_heads, int n_kv_heads, int head_dim, int page_size,
-                                       int num_pages, pkv_dtype dtype, float scale,
-                                       const void* out, const void* workspace, size_t ws_bytes,
-                                       int num_workers) {
-    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
-    if (st != PKV_OK) return st;
-    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-    if (num_pages <= 0 || table_stride <= 0 || num_workers < 0) return PKV_ERR_INVALID_ARG;
-    if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
-    if (batch == 0) return PKV_OK;
-    if (!q || !k_pool || !v_pool || !page_table || !out || (need_lens && !context_lens))
-        return PKV_ERR_INVALID_ARG;
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
-    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
-        return PKV_ERR_INVALID_ARG;
-    const size_t qo_bytes = (size_t)batch * n_q_heads * head_dim * 2;
-    const size_t pool_bytes = (size_t)num_pages * n_kv_heads * page_size * head_dim * 2;
-    const size_t table_bytes = (size_t)batch * table_stride * 4;
-    if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_pool, pool_bytes) ||
-        overlaps(out, qo_bytes, v_pool, pool_bytes) ||
-        overlaps(out, qo_bytes, page_table, table_bytes) ||
-        (need_lens && overlaps(out, qo_bytes, context_lens, (size_t)batch * 4)) ||
-        overlaps(out, qo_bytes, workspace, ws_bytes))
-        return PKV_ERR_ALIAS;
-    return PKV_OK;
-}
-
 pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_heads,
                              int n_kv_heads, int head_dim, int page_size, int table_stride,
-                             int num_workers, void* workspace, size_t ws_bytes,
-                             pkv_stream stream) {
+                             int num_workers, pkv_decode_variant variant, void* workspace,
+                             size_t ws_bytes, pkv_stream stream) {
     pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
     if (st != PKV_OK) return st;
-    if (table_stride <= 0 || num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if (table_stride <= 0 || num_workers < 0 || !valid_variant(variant))
+        return PKV_ERR_INVALID_ARG;
     if (batch == 0) return PKV_OK;
     if (!context_lens) return PKV_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
     DecodeSetup s;
     if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, PKV_BF16,
-                           num_workers, &s)) != PKV_OK)
+                           num_workers, variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     return do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
@@ -366,36 +480,37 @@ pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_poo
                             int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                             int num_pages, pkv_dtype dtype, float scale, void* out,
                             void* workspace, size_t ws_bytes, int num_workers,
-                            pkv_stream stream) {
+                            pkv_decode_variant variant, pkv_stream stream) {
     pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride, nullptr,
                                          false, batch, n_q_heads, n_kv_heads, head_dim,
                                          page_size, num_pages, dtype, scale, out, workspace,
-                                         ws_bytes, num_workers);
+                                         ws_bytes, num_workers, variant);
     if (st != PKV_OK || batch == 0) return st;
     DecodeSetup s;
     if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
-                           &s)) != PKV_OK)
+                           variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     return do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                  page_size, num_pages, scale, out, workspace, s,
+                  head_dim, page_size, num_pages, dtype, scale, out, workspace, s,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 pkv_status paged_decode_combine(int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                 pkv_dtype dtype, void* out, void* workspace, size_t ws_bytes,
-                                int num_workers, pkv_stream stream) {
+                                int num_workers, pkv_decode_variant variant, pkv_stream stream) {
     pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, 16);
     if (st != PKV_OK) return st;
-    if ((dtype != PKV_F16 && dtype != PKV_BF16) || num_workers < 0) return PKV_ERR_INVALID_ARG;
+    if ((dtype != PKV_F16 && dtype != PKV_BF16) || num_workers < 0 || !valid_variant(variant))
+        return PKV_ERR_INVALID_ARG;
     if (batch == 0) return PKV_OK;
     if (!out || !aligned16(out)) return PKV_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_WORKSPACE;
     if (overlaps(out, (size_t)batch * n_q_heads * head_dim * 2, workspace, ws_bytes))
         return PKV_ERR_ALIAS;
     DecodeSetup s;
-    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, dtype, num_workers, &s)) !=
-        PKV_OK)
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, dtype, num_workers,
+                           variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s,
@@ -407,15 +522,16 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
                                   const int32_t* context_lens, int batch, int n_q_heads,
                                   int n_kv_heads, int head_dim, int page_size, int num_pages,
                                   pkv_dtype dtype, float scale, void* out, void* workspace,
-                                  size_t ws_bytes, int num_workers, pkv_stream stream) {
+                                  size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                                  pkv_stream stream) {
     pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
                                          context_lens, true, batch, n_q_heads, n_kv_heads,
                                          head_dim, page_size, num_pages, dtype, scale, out,
-                                         workspace, ws_bytes, num_workers);
+                                         workspace, ws_bytes, num_workers, variant);
     if (st != PKV_OK || batch == 0) return st;
     DecodeSetup s;
     if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
-                           &s)) != PKV_OK)
+                           variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -423,7 +539,8 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
                       nullptr, cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                     page_size, num_pages, scale, out, workspace, s, cs)) != PKV_OK)
+                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, cs)) !=
+        PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
 }
@@ -434,26 +551,27 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                              const int32_t* context_lens, int batch, int n_q_heads,
                              int n_kv_heads, int head_dim, int page_size, int num_pages,
                              pkv_dtype dtype, float scale, void* out, void* workspace,
-                             size_t ws_bytes, int num_workers, pkv_stream stream) {
+                             size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                             pkv_stream stream) {
     pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
                                          context_lens, true, batch, n_q_heads, n_kv_heads,
                                          head_dim, page_size, num_pages, dtype, scale, out,
-                                         workspace, ws_bytes, num_workers);
+                                         workspace, ws_bytes, num_workers, variant);
     if (st != PKV_OK || batch == 0) return st;
     if (!k_new || !v_new || !positions) return PKV_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
     const size_t pool_bytes = (size_t)num_pages * n_kv_heads * page_size * head_dim * 2;
     const size_t row_bytes = (size_t)batch * n_kv_heads * head_dim * 2;
+    const size_t qo_bytes = (size_t)batch * n_q_heads * head_dim * 2;
     if (overlaps(k_new, row_bytes, k_pool, pool_bytes) ||
         overlaps(k_new, row_bytes, v_pool, pool_bytes) ||
         overlaps(v_new, row_bytes, k_pool, pool_bytes) ||
         overlaps(v_new, row_bytes, v_pool, pool_bytes) ||
-        overlaps(out, (size_t)batch * n_q_heads * head_dim * 2, k_new, row_bytes) ||
-        overlaps(out, (size_t)batch * n_q_heads * head_dim * 2, v_new, row_bytes))
+        overlaps(out, qo_bytes, k_new, row_bytes) || overlaps(out, qo_bytes, v_new, row_bytes))
         return PKV_ERR_ALIAS;
     DecodeSetup s;
     if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
-                           &s)) != PKV_OK)
+                           variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -464,7 +582,8 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                       cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                     page_size, num_pages, scale, out, workspace, s, cs)) != PKV_OK)
+                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, cs)) !=
+        PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
 }
@@ -476,7 +595,8 @@ pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
         return PKV_ERR_CUDA;
     uint32_t v = h.status;
     const int n = h.append_slots < 0 ? 0
-                  : (h.append_slots > pkv::kMaxAppendCtas ? pkv::kMaxAppendCtas : h.append_slots);
+                  : (h.append_slots > pkv::kMaxAppendCtas ? pkv::kMaxAppendCtas
+                                                          : h.append_slots);
     for (int i = 0; i < n; ++i) v |= h.append_status[i];
     *status_out = v;
     return v ? PKV_ERR_DEVICE_CHECK : PKV_OK;

@@ -6,6 +6,7 @@
 // gets `false` and reports PKV_DEV_TIMEOUT instead of spinning forever.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -208,6 +209,16 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Launch configuration of one tensor-core decode instantiation (the kernel
+// also takes the K and V tensor maps).
+struct DecodeMmaInfo {
+    void (*fn)(DecodeParams, CUtensorMap, CUtensorMap);
+    int warps;
+    int stages;
+    int smem_bytes;
+    int gs;
+};
 
 // Launch configuration of one decode-kernel instantiation.
 struct DecodeKernelInfo {

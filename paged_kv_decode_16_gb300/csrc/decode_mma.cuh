@@ -1,0 +1,447 @@
+// decode_mma.cuh -- tensor-core variant of the paged GQA decode kernel.
+//
+// Same operation, work split, partial-state format and chunk pipeline as
+// decode.cuh (one warp per balanced range of 16-token chunks, a STAGES-deep
+// ring of chunk buffers per warp, one mbarrier per stage), with the two
+// contractions of a chunk done by warp-level tensor-core MMA
+// (mma.sync m16n8k16, bf16/fp16 in, fp32 accumulate):
+//
+//   S[g][t]  = sum_d Q[g][d] K[t][d]      rows = the query group (padded to 16),
+//                                          n = 16 tokens, k = D
+//   O[g][d] += sum_t P[g][t] V[t][d]      P = exp2(S*scale*log2e - m) in the input
+//                                          dtype (bf16: as hi + lo, two MMAs),
+//                                          k = 16 tokens, n = D
+//
+// The S accumulator fragments are exactly the A fragments of the P.V product,
+// so P never leaves registers.  K and V chunks are brought in by 2-D tensor
+// copies (cp.async.bulk.tensor) of [16 rows x 64 elements] boxes with the
+// 128-byte swizzle, which makes the ldmatrix reads of both operands free of
+// bank conflicts.  A chunk costs ~32 MMAs + 16 ldmatrix + the softmax, about an
+// eighth of the instructions of the CUDA-core kernel, so the warps stay far
+// from issue-bound and the kernel is limited by HBM.
+//
+// Rows of a ragged last chunk past the context length are still copied (a box
+// is always 16 rows, all inside the same page); their scores are masked to
+// -inf and their V rows are zeroed in shared memory before the P.V product, so
+// stale or NaN data there never reaches a result.
+#pragma once
+
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "decode.cuh"
+
+namespace pkv {
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+template <typename T>
+struct Mma;
+
+template <>
+struct Mma<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+template <>
+struct Mma<__half> {
+    static __device__ __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+// P in two bf16 pieces: hi = bf16(p), lo = bf16(p - hi).  bf16 keeps 8
+// significant bits, too few for P (an output that cancels would carry ~2^-9
+// relative error); hi + lo carries ~16.  fp16 P (11 bits) is used as is.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = Cvt<__nv_bfloat16>::pack2(a, b);
+    const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xffff0000u);
+    lo = Cvt<__nv_bfloat16>::pack2(a - ha, b - hb);
+}
+
+// Byte offset of (row r, 16-byte column j) inside one [16 x 128 B] box written
+// by a 128-byte-swizzled tensor copy into a 1024-byte aligned buffer.
+__device__ __forceinline__ uint32_t swz128(int r, int j) {
+    return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4));
+}
+
+// Shared memory of one CTA: every warp's ring of K/V stages first (each stage a
+// multiple of 1 KiB, as the 128-byte swizzle needs), then every warp's q slots,
+// then the mbarriers.
+template <int D, int GS, int STAGES, int WARPS>
+struct MmaLayout {
+    static constexpr int kBoxes = D / 64;                       // [16 x 64] boxes per K or V chunk
+    static constexpr int kBoxBytes = kChunk * 128;              // 2 KiB
+    static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
+    static constexpr int kWarpKV = STAGES * kStageBytes;
+    static constexpr int kQBytes = GS * D * 2;
+    static constexpr int kOffQ = WARPS * kWarpKV;
+    static constexpr int kOffBar = ((kOffQ + WARPS * STAGES * kQBytes) + 15) / 16 * 16;
+    static constexpr int kBytes = kOffBar + WARPS * STAGES * 8 + 1024;  // + alignment slack
+};
+
+template <typename T, int D, int GS, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
+    using Lay = MmaLayout<D, GS, STAGES, WARPS>;
+    constexpr int KSTEPS = D / 16;      // k-steps of the q.k product
+    constexpr int NT = D / 8;           // n-tiles of the P.V product
+    constexpr bool kTwoHalves = GS > 8; // query rows 8..15 in use
+    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;  // P as bf16 hi + lo
+    static_assert(GS <= 16, "one m16 tile of query heads");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;  // 1 KiB alignment for the swizzle
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* base = smem_raw + pad;
+    uint8_t* wsm = base + warp * Lay::kWarpKV;                 // this warp's K/V stages
+    const uint32_t wsm_u32 = raw + pad + warp * Lay::kWarpKV;
+    T* sq = reinterpret_cast<T*>(base + Lay::kOffQ + warp * STAGES * Lay::kQBytes);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + Lay::kOffBar + warp * STAGES * 8);
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+        fence_barrier_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap))
+                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap))
+                     : "memory");
+    }
+    __syncwarp();
+    pdl_wait();
+    pdl_trigger();
+
+    const int total = p.hdr->total_chunks;
+    const int nw = p.hdr->num_workers;
+    const int gw = blockIdx.x * WARPS + warp;
+    if (gw >= nw) return;
+    const int f0 = (int)((long long)gw * total / nw);
+    const int f1 = (int)((long long)(gw + 1) * total / nw);
+    const int n = f1 - f0;
+    if (n <= 0) return;
+
+    const int units_per_b = p.n_kv_heads * p.sub_groups;
+    const int g_lo = lane >> 2;          // query row of c0/c1 (c2/c3: g_lo + 8)
+    const int tq = (lane & 3) * 2;       // first token (or d) column of this lane in a tile
+    const T* __restrict__ qg = static_cast<const T*>(p.q);
+
+    int wbase = 0;
+    ChunkDesc wa, wb;
+    wa.off = wb.off = -1;
+    wa.u = wb.u = wa.k = wb.k = wa.nvalid = wb.nvalid = 0;
+    wa.nch = wb.nch = 1;
+    if (lane < n) wa = describe_chunk(p, f0 + lane, units_per_b);
+    if (32 + lane < n) wb = describe_chunk(p, f0 + 32 + lane, units_per_b);
+
+    auto fetch = [&](int j) -> ChunkDesc {
+        const bool second = (j - wbase) >= 32;
+        ChunkDesc src;
+        src.u = second ? wb.u : wa.u;
+        src.k = second ? wb.k : wa.k;
+        src.nch = second ? wb.nch : wa.nch;
+        src.nvalid = second ? wb.nvalid : wa.nvalid;
+        src.off = second ? wb.off : wa.off;
+        return shfl_desc(src, j & 31);
+    };
+
+    auto issue = [&](int j) {
+        const ChunkDesc d = fetch(j);
+        if (lane == 0) {
+            const int st = j % STAGES;
+            const bool seg_start = (j == 0) || (d.k == 0);
+            const uint32_t kv_bytes = d.off >= 0 ? (uint32_t)Lay::kStageBytes : 0u;
+            const uint32_t q_bytes = seg_start ? (uint32_t)Lay::kQBytes : 0u;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bar[st], kv_bytes + q_bytes);
+            if (kv_bytes) {
+                uint8_t* stage = wsm + st * Lay::kStageBytes;
+                const int y = (int)d.off;  // first pool row of the chunk
+#pragma unroll
+                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                    tma_load_2d(stage + bx * Lay::kBoxBytes, &kmap, bx * 64, y, &bar[st]);
+                    tma_load_2d(stage + (Lay::kBoxes + bx) * Lay::kBoxBytes, &vmap, bx * 64, y,
+                                &bar[st]);
+                }
+            }
+            if (q_bytes) {
+                const int b = d.u / units_per_b;
+                const int uidx = d.u - b * units_per_b;
+                const int h = uidx / p.sub_groups;
+                const int sg = uidx - h * p.sub_groups;
+                const long long qrow = (long long)b * p.n_q_heads + h * p.group + sg * GS;
+                bulk_g2s(sq + st * GS * D, qg + qrow * D, q_bytes, &bar[st]);
+            }
+        }
+    };
+
+    const int npro = n < STAGES ? n : STAGES;
+    for (int j = 0; j < npro; ++j) issue(j);
+
+    uint32_t qa[KSTEPS][4];     // A fragments of Q (rows g_lo, g_lo+8)
+    float o[NT][4];             // O accumulators (c0,c1: row g_lo; c2,c3: row g_lo+8)
+    float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
+    bool seg_whole_start = false;
+
+    for (int i = 0; i < n; ++i) {
+        if (i > 0 && (i & 31) == 0) {
+            wbase += 32;
+            wa = wb;
+            if (wbase + 32 + lane < n) wb = describe_chunk(p, f0 + wbase + 32 + lane, units_per_b);
+        }
+        const ChunkDesc d = fetch(i);
+        const int st = i % STAGES;
+        if (!mbar_wait_bounded(&bar[st], (uint32_t)((i / STAGES) & 1))) {
+            if (lane == 0) set_status(p.status, PKV_DEV_TIMEOUT);
+            const int last = (i + STAGES < n ? i + STAGES : n);
+            for (int j = i + 1; j < last; ++j)
+                mbar_wait_bounded(&bar[j % STAGES], (uint32_t)((j / STAGES) & 1));
+            return;
+        }
+        const bool seg_start = (i == 0) || (d.k == 0);
+        if (seg_start) {
+            // A fragments of Q: a0 (row g, k tq..tq+1), a1 (row g+8), a2 (k+8), a3
+            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(sq + st * GS * D);
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int c0 = (kk * 16 + tq) / 2, c1 = (kk * 16 + 8 + tq) / 2;
+                qa[kk][0] = g_lo < GS ? q32[g_lo * (D / 2) + c0] : 0u;
+                qa[kk][2] = g_lo < GS ? q32[g_lo * (D / 2) + c1] : 0u;
+                if constexpr (kTwoHalves) {
+                    qa[kk][1] = g_lo + 8 < GS ? q32[(g_lo + 8) * (D / 2) + c0] : 0u;
+                    qa[kk][3] = g_lo + 8 < GS ? q32[(g_lo + 8) * (D / 2) + c1] : 0u;
+                } else {
+                    qa[kk][1] = 0u;
+                    qa[kk][3] = 0u;
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+            m_lo = m_hi = -INFINITY;
+            l_lo = l_hi = 0.f;
+            seg_whole_start = (d.k == 0);
+        }
+
+        if (d.off >= 0) {
+            const uint32_t kst = wsm_u32 + st * Lay::kStageBytes;
+            const uint32_t vst = kst + Lay::kBoxes * Lay::kBoxBytes;
+            const int nvalid = d.nvalid;
+            if (nvalid < kChunk) {
+                // zero the V rows past the context (stale or NaN page contents)
+                uint4* vrows = reinterpret_cast<uint4*>(wsm + st * Lay::kStageBytes +
+                                                        Lay::kBoxes * Lay::kBoxBytes);
+                const int nz = (kChunk - nvalid) * 8 * Lay::kBoxes;  // 16-byte vectors
+                for (int z = lane; z < nz; z += 32) {
+                    const int bx = z / ((kChunk - nvalid) * 8);
+                    const int rem = z - bx * (kChunk - nvalid) * 8;
+                    const int row = nvalid + rem / 8;
+                    vrows[(bx * Lay::kBoxBytes + row * 128) / 16 + (rem & 7)] =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            // ---- S = Q K^T : two n-tiles (tokens 0-7, 8-15), even/odd k chains ----
+            float s[2][2][4];
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int b = 0; b < 2; ++b) s[a][b][0] = s[a][b][1] = s[a][b][2] = s[a][b][3] = 0.f;
+            // ldmatrix x4 rows: lane -> matrix mi = lane/8, row r = lane%8;
+            // matrices: (tok 0-7, d+0..7), (tok 0-7, d+8..15), (tok 8-15, d+0..7), (tok 8-15, d+8..15)
+            const int mi = lane >> 3, rr = lane & 7;
+            const int k_tok = (mi >> 1) * 8 + rr;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int dcol = kk * 16 + (mi & 1) * 8;      // first element of the 16-byte row piece
+                const int bx = dcol / 64;
+                const uint32_t addr = kst + bx * Lay::kBoxBytes + swz128(k_tok, (dcol % 64) / 8);
+                uint32_t kb[4];
+                ldsm_x4(addr, kb);
+                Mma<T>::run(s[0][kk & 1], qa[kk], kb[0], kb[1]);
+                Mma<T>::run(s[1][kk & 1], qa[kk], kb[2], kb[3]);
+            }
+            // ---- online softmax (base 2) on rows g_lo (c0,c1) and g_lo+8 (c2,c3) ----
+            float sc[2][4];
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = a * 8 + tq + (e & 1);
+                    const float v = (s[a][0][e] + s[a][1][e]) * p.scale_log2;
+                    sc[a][e] = t < nvalid ? v : -INFINITY;
+                }
+            uint32_t pa[4];        // A fragments of P (its bf16 high part when split)
+            uint32_t pl[4] = {0u, 0u, 0u, 0u};  // bf16 residual p - hi (split only)
+            {
+                float mx = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+                const float m_new = fmaxf(m_lo, mx);
+                const float alpha = fast_exp2(m_lo - m_new);
+                const float p00 = fast_exp2(sc[0][0] - m_new), p01 = fast_exp2(sc[0][1] - m_new);
+                const float p10 = fast_exp2(sc[1][0] - m_new), p11 = fast_exp2(sc[1][1] - m_new);
+                float rs = (p00 + p01) + (p10 + p11);
+                rs += __shfl_xor_sync(kFull, rs, 1);
+                rs += __shfl_xor_sync(kFull, rs, 2);
+                l_lo = l_lo * alpha + rs;
+                m_lo = m_new;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    o[nt][0] *= alpha;
+                    o[nt][1] *= alpha;
+                }
+                if constexpr (kSplitP) {
+                    split_bf16x2(p00, p01, pa[0], pl[0]);
+                    split_bf16x2(p10, p11, pa[2], pl[2]);
+                } else {
+                    pa[0] = Cvt<T>::pack2(p00, p01);
+                    pa[2] = Cvt<T>::pack2(p10, p11);
+                }
+            }
+            if constexpr (kTwoHalves) {
+                float mx = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+                const float m_new = fmaxf(m_hi, mx);
+                const float alpha = fast_exp2(m_hi - m_new);
+                const float p00 = fast_exp2(sc[0][2] - m_new), p01 = fast_exp2(sc[0][3] - m_new);
+                const float p10 = fast_exp2(sc[1][2] - m_new), p11 = fast_exp2(sc[1][3] - m_new);
+                float rs = (p00 + p01) + (p10 + p11);
+                rs += __shfl_xor_sync(kFull, rs, 1);
+                rs += __shfl_xor_sync(kFull, rs, 2);
+                l_hi = l_hi * alpha + rs;
+                m_hi = m_new;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    o[nt][2] *= alpha;
+                    o[nt][3] *= alpha;
+                }
+                if constexpr (kSplitP) {
+                    split_bf16x2(p00, p01, pa[1], pl[1]);
+                    split_bf16x2(p10, p11, pa[3], pl[3]);
+                } else {
+                    pa[1] = Cvt<T>::pack2(p00, p01);
+                    pa[3] = Cvt<T>::pack2(p10, p11);
+                }
+            } else {
+                pa[1] = pa[3] = 0u;
+                pl[1] = pl[3] = 0u;
+            }
+            // ---- O += P V : ldmatrix.trans gives the V^T fragments ----
+            // x4 matrices: (tok 0-7, d 8nt..), (tok 8-15, d 8nt..), (tok 0-7, d 8nt+8..), (tok 8-15, ..)
+            const int v_tok = (mi & 1) * 8 + rr;
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int dcol = np * 16 + (mi >> 1) * 8;
+                const int bx = dcol / 64;
+                const uint32_t addr = vst + bx * Lay::kBoxBytes + swz128(v_tok, (dcol % 64) / 8);
+                uint32_t vb[4];
+                ldsm_x4_trans(addr, vb);
+                Mma<T>::run(o[2 * np], pa, vb[0], vb[1]);
+                Mma<T>::run(o[2 * np + 1], pa, vb[2], vb[3]);
+                if constexpr (kSplitP) {
+                    Mma<T>::run(o[2 * np], pl, vb[0], vb[1]);
+                    Mma<T>::run(o[2 * np + 1], pl, vb[2], vb[3]);
+                }
+            }
+        }
+
+        const bool seg_end = (i == n - 1) || (d.k == d.nch - 1);
+        if (seg_end) {
+            const bool whole = seg_whole_start && (d.k == d.nch - 1);
+            const int b = d.u / units_per_b;
+            const int uidx = d.u - b * units_per_b;
+            const int h = uidx / p.sub_groups;
+            const int sg = uidx - h * p.sub_groups;
+            const long long hq0 = (long long)b * p.n_q_heads + h * p.group + sg * GS;
+#pragma unroll
+            for (int half = 0; half < (kTwoHalves ? 2 : 1); ++half) {
+                const int g = g_lo + half * 8;
+                const float l = half ? l_hi : l_lo;
+                const float m = half ? m_hi : m_lo;
+                if (g < GS) {
+                    if (whole) {
+                        T* outp = static_cast<T*>(p.out) + (hq0 + g) * D;
+                        const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            *reinterpret_cast<uint32_t*>(outp + nt * 8 + tq) =
+                                Cvt<T>::pack2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+                        }
+                    } else {
+                        float* dst = p.partials + (long long)(d.u + gw) * partial_slot_floats(GS, D);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            *reinterpret_cast<float2*>(dst + g * D + nt * 8 + tq) =
+                                make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+                        }
+                        if ((lane & 3) == 0) {
+                            dst[GS * D + g] = m;
+                            dst[GS * D + GS + g] = l;
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (i + STAGES < n) issue(i + STAGES);
+    }
+}
+
+template <int D, int GS>
+constexpr int pick_mma_stages() {
+    // as many stages as keep a 4-warp CTA within 112 KiB (two CTAs per SM)
+    return MmaLayout<D, GS, 4, 4>::kBytes <= 112 * 1024
+               ? 4
+               : (MmaLayout<D, GS, 3, 4>::kBytes <= 112 * 1024 ? 3 : 2);
+}
+
+template <typename T, int D, int GS>
+DecodeMmaInfo make_decode_mma_info() {
+    constexpr int W = 4;
+    constexpr int S = pick_mma_stages<D, GS>();
+    DecodeMmaInfo info;
+    info.fn = decode_mma_kernel<T, D, GS, W, S>;
+    info.warps = W;
+    info.stages = S;
+    info.smem_bytes = MmaLayout<D, GS, S, W>::kBytes;
+    info.gs = GS;
+    return info;
+}
+
+}  // namespace pkv

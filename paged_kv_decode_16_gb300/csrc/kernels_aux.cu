@@ -127,8 +127,9 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
 // Combine: one CTA per unit (sequence, KV head, sub-group); units finished by
 // a single worker exit at once, empty sequences get zeros.  Partial m is in
 // base-2 units: out = sum_i 2^(m_i-M) o_i / sum_i 2^(m_i-M) l_i, M = max_i m_i.
-// Warp g reduces M and the denominator of head g over the splits; then every
-// thread owns 4 consecutive output elements and streams the splits' o.
+// Warp w reduces M and the denominator of heads w, w+8, ... over the splits;
+// then every thread owns 4 consecutive output elements and streams the
+// splits' o.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
@@ -138,7 +139,7 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
                int n_q_heads) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float sM[8], sInv[8];
+    __shared__ float sM[16], sInv[16];  // per query head of the unit (gs <= 16)
     const int u = blockIdx.x;
     const int b = u / units_per_b;
     const int uidx = u - b * units_per_b;
@@ -165,21 +166,21 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     const long long stride = partial_slot_floats(gs, D);
     const float* base = partials + (long long)(u + w_first) * stride;  // slots u+w_first..u+w_last
     const int warp = tid >> 5, lane = tid & 31;
-    if (warp < gs) {
+    for (int g = warp; g < gs; g += (int)(blockDim.x >> 5)) {
         float M = -INFINITY;
-        for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * stride + n + warp]);
+        for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * stride + n + g]);
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, m));
         float S = 0.f;
         if (M != -INFINITY) {
             for (int s = lane; s < ns; s += 32)
-                S += exp2f(base[s * stride + n + warp] - M) * base[s * stride + n + gs + warp];
+                S += exp2f(base[s * stride + n + g] - M) * base[s * stride + n + gs + g];
         }
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) S += __shfl_xor_sync(kFull, S, m);
         if (lane == 0) {
-            sM[warp] = M;
-            sInv[warp] = S > 0.f ? 1.0f / S : 0.f;
+            sM[g] = M;
+            sInv[g] = S > 0.f ? 1.0f / S : 0.f;
         }
     }
     __syncthreads();

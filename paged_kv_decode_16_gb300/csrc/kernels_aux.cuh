@@ -51,4 +51,10 @@ cudaError_t launch_gather(const void* k_pool, const void* v_pool, const int32_t*
 DecodeKernelInfo decode_info_bf16(int head_dim, int gs);
 DecodeKernelInfo decode_info_f16(int head_dim, int gs);
 
+// Tensor-core variant (decode_mma.cuh).
+DecodeMmaInfo decode_mma_info_bf16_d64(int gs);
+DecodeMmaInfo decode_mma_info_bf16_d128(int gs);
+DecodeMmaInfo decode_mma_info_f16_d64(int gs);
+DecodeMmaInfo decode_mma_info_f16_d128(int gs);
+
 }  // namespace pkv

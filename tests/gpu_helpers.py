@@ -32,7 +32,12 @@ def to_dev(w: wl.Workload, dev="cuda"):
     return table, lens, pos
 
 
-def run_gpu(w: wl.Workload, num_workers: int = 0, append: bool | None = None):
+VARIANTS = (pkv.VARIANT_CUDA_CORES, pkv.VARIANT_TENSOR_CORES)
+VARIANT_IDS = ("cuda_cores", "tensor_cores")
+
+
+def run_gpu(w: wl.Workload, num_workers: int = 0, append: bool | None = None,
+            variant: int = pkv.VARIANT_AUTO):
     """kv_append (when the workload has one) then paged_decode_attention.
     Returns (out tensor, workspace, host status)."""
     dev = w.q.device
@@ -45,9 +50,9 @@ def run_gpu(w: wl.Workload, num_workers: int = 0, append: bool | None = None):
         assert int(st.item()) == 0
     out = torch.empty_like(w.q)
     ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, num_workers,
-                             device=dev)
+                             device=dev, variant=variant)
     pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws,
-                               num_workers=num_workers)
+                               num_workers=num_workers, variant=variant)
     torch.cuda.synchronize()
     return out, ws, pkv.pkv_read_device_status(ws)
 

@@ -48,13 +48,13 @@ def test_status_strings(lib):
 def _decode(lib, **kw):
     a = dict(q=A, k=A * 8, v=A * 16, table=A * 24, stride=4, lens=A * 25, batch=2, hq=8, hkv=2,
              d=128, p=16, np_=8, dt=BF16, scale=0.088, out=A * 26, ws=A * 27, ws_bytes=1 << 20,
-             workers=0)
+             workers=0, variant=0)
     a.update(kw)
     V = ctypes.c_void_p
     return lib.paged_decode_attention(V(a["q"]), V(a["k"]), V(a["v"]), V(a["table"]), a["stride"],
                                       V(a["lens"]), a["batch"], a["hq"], a["hkv"], a["d"], a["p"],
                                       a["np_"], a["dt"], ctypes.c_float(a["scale"]), V(a["out"]),
-                                      V(a["ws"]), a["ws_bytes"], a["workers"], None)
+                                      V(a["ws"]), a["ws_bytes"], a["workers"], a["variant"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -69,6 +69,8 @@ def _decode(lib, **kw):
     (dict(stride=0), INVALID),
     (dict(dt=5), INVALID),
     (dict(workers=-2), INVALID),
+    (dict(variant=3), INVALID),
+    (dict(variant=-1), INVALID),
     (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID),
     (dict(q=0), INVALID),

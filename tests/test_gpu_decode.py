@@ -9,7 +9,8 @@ import torch
 import oracle
 import paged_kv_decode_16_gb300 as pkv
 from paged_kv_decode_16_gb300 import workloads as wl
-from gpu_helpers import (assert_close, errors, oracle_full, oracle_rows, run_gpu, to_dev)
+from gpu_helpers import (VARIANT_IDS, VARIANTS, assert_close, errors, oracle_full, oracle_rows,
+                         run_gpu, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -22,11 +23,12 @@ def _sample_rows(w, rng, n_random=48):
     return np.array(rows, dtype=np.int32)
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("name", wl.NAMES)
-def test_named_workload_matches_oracle(name):
+def test_named_workload_matches_oracle(name, variant):
     w = wl.make(name, seed=0, device="cuda")
     before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
-    out, ws, status = run_gpu(w)
+    out, ws, status = run_gpu(w, variant=variant)
     assert status == 0
     got = out.float().cpu().numpy().astype(np.float64)
     if name == "tiny":
@@ -64,42 +66,46 @@ def _sweep_cases():
     return cases
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("dt,D,P,hq,hkv,lens_name,workers", _sweep_cases())
-def test_random_sweep(dt, D, P, hq, hkv, lens_name, workers):
+def test_random_sweep(dt, D, P, hq, hkv, lens_name, workers, variant):
     seed = zlib.crc32(repr((str(dt), D, P, hq, hkv, lens_name, workers)).encode())
     lens = LENS[lens_name]
     if lens is None:
         lens = np.random.default_rng(seed).integers(1, 301, size=13)
     w = wl.make_random(seed, batch=len(lens), n_q_heads=hq, n_kv_heads=hkv, head_dim=D,
                        page_size=P, dtype=dt, lens=lens, device="cuda", poison=True)
-    out, ws, status = run_gpu(w, num_workers=workers, append=False)
+    out, ws, status = run_gpu(w, num_workers=workers, append=False, variant=variant)
     assert status == 0
     ref = oracle_full(w, append=False)
-    assert_close(out, ref, what=f"{dt} D{D} P{P} G{hq}/{hkv} {lens_name} w{workers}")
+    assert_close(out, ref, what=f"{dt} D{D} P{P} G{hq}/{hkv} {lens_name} w{workers} v{variant}")
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("workers", [1, 2, 3, 5, 64, 0])
-def test_forced_worker_counts_agree(workers):
+def test_forced_worker_counts_agree(workers, variant):
     """Every split of the same batch matches the oracle (partials + combine)."""
     w = wl.make_random(7, batch=9, n_q_heads=32, n_kv_heads=8, head_dim=128, page_size=16,
                        dtype=torch.bfloat16, lens=[1, 16, 17, 100, 257, 600, 33, 48, 1000],
                        device="cuda", poison=True)
-    out, ws, status = run_gpu(w, num_workers=workers, append=False)
+    out, ws, status = run_gpu(w, num_workers=workers, append=False, variant=variant)
     assert status == 0
     assert_close(out, oracle_full(w, append=False), what=f"workers={workers}")
 
 
-def test_long_sequence_split_many_ways():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_long_sequence_split_many_ways(variant):
     w = wl.make_random(8, batch=2, n_q_heads=28, n_kv_heads=4, head_dim=128, page_size=32,
                        dtype=torch.float16, lens=[20000, 3], device="cuda", poison=True)
     ref = oracle_full(w, append=False)
     for workers in (0, 97, 500):
-        out, _, status = run_gpu(w, num_workers=workers, append=False)
+        out, _, status = run_gpu(w, num_workers=workers, append=False, variant=variant)
         assert status == 0
         assert_close(out, ref, what=f"workers={workers}")
 
 
-def test_page_permutation_is_bitwise_invariant():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_page_permutation_is_bitwise_invariant(variant):
     """Same dense cache under two page permutations -> identical bits."""
     rng = np.random.default_rng(5)
     B, Hq, Hkv, D, P = 6, 16, 4, 128, 16
@@ -114,10 +120,10 @@ def test_page_permutation_is_bitwise_invariant():
         kt = torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).cuda()
         vt = torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16).cuda()
         out = torch.empty_like(q)
-        ws = pkv.alloc_workspace(B, Hq, Hkv, D, 37)
+        ws = pkv.alloc_workspace(B, Hq, Hkv, D, 37, variant=variant)
         pkv.paged_decode_attention(q, kt, vt, torch.from_numpy(table).cuda(),
                                    torch.from_numpy(lens.astype(np.int32)).cuda(), 0.088, out, ws,
-                                   num_workers=37)
+                                   num_workers=37, variant=variant)
         outs.append(out.cpu())
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     del rng
@@ -147,11 +153,22 @@ def test_shared_prefix_equals_private_copies_bitwise():
     assert torch.equal(out_shared.view(torch.int16), out_priv.view(torch.int16))
 
 
-def test_rerun_is_bitwise_deterministic():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_rerun_is_bitwise_deterministic(variant):
     w = wl.make("mixed_append", seed=2, device="cuda", batch=40)
-    a, _, _ = run_gpu(w, append=False)
-    b, _, _ = run_gpu(w, append=False)
+    a, _, _ = run_gpu(w, append=False, variant=variant)
+    b, _, _ = run_gpu(w, append=False, variant=variant)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_variants_agree_with_each_other():
+    """The two decode kernels differ only by rounding (P in the input dtype on
+    the tensor-core path): on the same inputs they agree within the tolerance."""
+    w = wl.make("llama3_8b", seed=9, device="cuda", batch=12)
+    a, _, sa = run_gpu(w, append=False, variant=pkv.VARIANT_CUDA_CORES)
+    b, _, sb = run_gpu(w, append=False, variant=pkv.VARIANT_TENSOR_CORES)
+    assert sa == 0 and sb == 0
+    assert_close(a, b.float().cpu().numpy().astype(np.float64), strict=True)
 
 
 def test_append_then_gather_is_bit_exact():
@@ -180,23 +197,25 @@ def test_append_then_gather_is_bit_exact():
         pool.destroy()
 
 
-def test_empty_sequences_give_zeros():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_empty_sequences_give_zeros(variant):
     w = wl.make_random(13, batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16,
                        dtype=torch.bfloat16, lens=[0, 5, 0, 40], device="cuda", poison=True)
     for workers in (0, 1, 3):
-        out, _, status = run_gpu(w, num_workers=workers, append=False)
+        out, _, status = run_gpu(w, num_workers=workers, append=False, variant=variant)
         assert status == 0
         assert_close(out, oracle_full(w, append=False))
         assert (out[0] == 0).all() and (out[2] == 0).all()
 
 
-def test_bad_page_id_is_flagged_and_skipped():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_bad_page_id_is_flagged_and_skipped(variant):
     w = wl.make_random(17, batch=3, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16,
                        dtype=torch.bfloat16, lens=[40, 20, 33], device="cuda")
     good = oracle_full(w, append=False)
     w.page_table[1, 0] = w.num_pages + 5  # outside the pool
     w.page_table[2, 1] = -3
-    out, ws, status = run_gpu(w, append=False)
+    out, ws, status = run_gpu(w, append=False, variant=variant)
     assert status & pkv.DEV_BAD_PAGE
     got = out.float().cpu().numpy().astype(np.float64)
     assert_close(got[0], good[0], what="untouched sequence")
@@ -214,18 +233,20 @@ def test_length_beyond_table_is_flagged_and_clamped():
     assert np.isfinite(out.float().cpu().numpy()).all()
 
 
-def test_guard_bands_untouched():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_guard_bands_untouched(variant):
     """Canaries around out and past the end of the workspace stay intact."""
     w = wl.make("tiny", seed=1, device="cuda")
     table, lens, _ = to_dev(w)
     n = w.q.numel()
     big = torch.full((n + 2048,), 7.0, dtype=w.dtype, device="cuda")
     out = big[1024:1024 + n].view_as(w.q)
-    need = pkv.paged_decode_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, 3)
+    need = pkv.paged_decode_workspace_size(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, 3,
+                                           variant)
     wsbig = torch.full((need + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
     ws = wsbig[:need]
     pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws,
-                               num_workers=3)
+                               num_workers=3, variant=variant)
     torch.cuda.synchronize()
     assert (big[:1024] == 7.0).all() and (big[1024 + n:] == 7.0).all()
     assert (wsbig[need:] == 0xA5).all()
