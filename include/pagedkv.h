@@ -184,14 +184,18 @@ pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_
  *  grouped and streaming block-S decode variants in the serving knob list.)
  *
  * Work split: every (sequence, KV head) is cut into chunks of 16 tokens; the
- * chunks of the whole batch are laid end to end and divided into equal
- * contiguous ranges, one per worker (a warp); a worker reads each chunk's K
- * and V once for the whole query group.  A (sequence, KV head) that lies in a
- * single worker's range is finished by that worker; one spread over several
- * workers leaves fp32 partial states (m, l, o) that paged_decode_combine
- * merges.  The split depends only on the context lengths and the worker
- * count, never on physical page ids, so permuting pages gives bitwise equal
- * results.
+ * chunks of the whole batch are laid end to end; 80% of them are divided into
+ * equal contiguous static ranges, one per worker (a warp), and the rest into
+ * small tiles that workers take from a shared counter when their range is
+ * done (this absorbs SMs that get less memory bandwidth than others).  A
+ * worker reads each chunk's K and V once for the whole query group.  A
+ * (sequence, KV head) that lies in one worker's range or one tile is finished
+ * there; one spread over several pieces leaves fp32 partial states (m, l, o)
+ * that paged_decode_combine merges.  Which worker takes which dynamic tile
+ * varies from run to run, but the pieces, the merge order and so the result
+ * bits depend only on the context lengths and the worker count, never on
+ * physical page ids or timing: permuting pages or rerunning gives bitwise
+ * equal results.
  *
  * num_workers: 0 = automatic (the GPU's SM count x resident warps of the
  * kernel, capped so each worker gets at least 4 chunks); n > 0 = at most n
@@ -228,7 +232,8 @@ pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_hea
                              size_t ws_bytes, pkv_stream stream);
 
 /* Main step on a workspace prepared by paged_decode_plan with the same shapes,
- * num_workers and variant: the decode kernel (persistent grid of workers;
+ * num_workers and variant; every run needs a plan of its own (the plan resets
+ * the counter that hands out the dynamic tiles).  The decode kernel (persistent grid of workers;
  * asynchronous copies of K/V chunks into shared memory, fp32 online softmax).
  * Writes out for every (sequence, KV head) finished by one worker and partial
  * states for the rest.  Pools of more than 2^31 - 1 rows (num_pages *

@@ -132,19 +132,32 @@ pkv_status prepare_kernel(const KernelPick& k, int* auto_workers) {
     return PKV_OK;
 }
 
+// Static ranges take this share of the chunks; the rest goes out in dynamic
+// tiles, at most kDynTilesPerWorker per worker.
+constexpr int kStaticPercent = 80;
+constexpr int kDynTilesPerWorker = 4;
+
 struct WsLayout {
-    size_t lens_eff, prefix, partials, total;
+    size_t lens_eff, prefix, wstart, tile_b, partials, total;
+    int dyn_tiles_max;
 };
 
+// Partial slots: static segments u + w < U + NW; dynamic U + NW + u + t < 2U + NW + NT.
 WsLayout ws_layout(int batch, long long units, int gs, int head_dim, int workers) {
     WsLayout w;
+    w.dyn_tiles_max = kDynTilesPerWorker * workers;
     size_t off = sizeof(WsHeader);
     w.lens_eff = off;
     off += align256((size_t)batch * 4);
     w.prefix = off;
     off += align256((size_t)(batch + 1) * 4);
+    w.wstart = off;
+    off += align256((size_t)(workers + 1) * 4);
+    w.tile_b = off;
+    off += align256((size_t)(w.dyn_tiles_max + 1) * 4);
     w.partials = off;
-    off += align256((size_t)(units + workers) * pkv::partial_slot_floats(gs, head_dim) * 4);
+    const size_t slots = (size_t)(2 * units + workers + w.dyn_tiles_max);
+    off += align256(slots * pkv::partial_slot_floats(gs, head_dim) * 4);
     w.total = off;
     return w;
 }
@@ -251,8 +264,8 @@ pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dt
     return PKV_OK;
 }
 
-pkv_status do_plan(const int32_t* context_lens, int batch, int page_size, int table_stride,
-                   int num_workers, void* workspace, const DecodeSetup& s,
+pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch, int page_size,
+                   int table_stride, int num_workers, void* workspace, const DecodeSetup& s,
                    const pkv::AppendArgs* append, cudaStream_t stream) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     pkv::PlanArgs pa;
@@ -265,7 +278,14 @@ pkv_status do_plan(const int32_t* context_lens, int batch, int page_size, int ta
     pa.min_chunks = kMinChunksPerWorker;
     pa.lens_eff = reinterpret_cast<int32_t*>(ws + s.ws.lens_eff);
     pa.prefix = reinterpret_cast<int32_t*>(ws + s.ws.prefix);
+    pa.wstart = reinterpret_cast<int32_t*>(ws + s.ws.wstart);
+    pa.tile_b = reinterpret_cast<int32_t*>(ws + s.ws.tile_b);
+    pa.static_pct = kStaticPercent;
+    pa.dyn_tiles_max = s.ws.dyn_tiles_max;
     pa.hdr = reinterpret_cast<WsHeader*>(ws);
+    pa.table = table;
+    pa.table_stride = table_stride;
+    pa.page_size = page_size;
     return cuda_status(pkv::launch_plan(pa, append, stream));
 }
 
@@ -281,6 +301,10 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.table = table;
     p.lens_eff = reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff);
     p.prefix = reinterpret_cast<const int32_t*>(ws + s.ws.prefix);
+    p.wstart = reinterpret_cast<const int32_t*>(ws + s.ws.wstart);
+    p.tile_b = reinterpret_cast<const int32_t*>(ws + s.ws.tile_b);
+    p.dyn_next = &reinterpret_cast<WsHeader*>(ws)->dyn_next;
+    p.units = (int)s.units;
     p.hdr = reinterpret_cast<const WsHeader*>(ws);
     p.status = &reinterpret_cast<WsHeader*>(ws)->status;
     p.partials = reinterpret_cast<float*>(ws + s.ws.partials);
@@ -471,8 +495,8 @@ pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_hea
                            num_workers, variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
-    return do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
-                   nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return do_plan(context_lens, nullptr, batch, page_size, table_stride, num_workers,
+                   workspace, s, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_pool,
@@ -535,8 +559,8 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if ((st = do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s,
-                      nullptr, cs)) != PKV_OK)
+    if ((st = do_plan(context_lens, page_table, batch, page_size, table_stride, num_workers,
+                      workspace, s, nullptr, cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
                      head_dim, page_size, num_pages, dtype, scale, out, workspace, s, cs)) !=
@@ -578,8 +602,8 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
     const pkv::AppendArgs a = make_append(k_new, v_new, positions, page_table, table_stride,
                                           k_pool, v_pool, n_kv_heads, head_dim, page_size,
                                           num_pages);
-    if ((st = do_plan(context_lens, batch, page_size, table_stride, num_workers, workspace, s, &a,
-                      cs)) != PKV_OK)
+    if ((st = do_plan(context_lens, page_table, batch, page_size, table_stride, num_workers,
+                      workspace, s, &a, cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
                      head_dim, page_size, num_pages, dtype, scale, out, workspace, s, cs)) !=

@@ -28,7 +28,12 @@ struct WsHeader {
     int32_t num_workers;     // workers that received a non-empty range
     int32_t append_slots;    // append_status entries written by this call
     uint32_t append_status[kMaxAppendCtas];  // PKV_DEV_* bits of each fused-append CTA
-    int32_t pad[64 - 4 - kMaxAppendCtas];
+    int32_t static_per_worker;  // chunks in each worker's static range
+    int32_t static_total;       // static_per_worker * num_workers
+    int32_t dyn_tile;           // chunks per dynamic tile
+    int32_t dyn_tiles;          // dynamic tiles
+    int32_t dyn_next;           // next dynamic tile to hand out (counter, reset by the plan)
+    int32_t pad[64 - 9 - kMaxAppendCtas];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -180,6 +185,10 @@ struct DecodeParams {
     const int32_t* table;     // [B][stride]
     const int32_t* lens_eff;  // [B] lengths after the plan's clamp (workspace)
     const int32_t* prefix;    // [B+1] chunk prefix sums (workspace)
+    const int32_t* wstart;    // [workers+1] sequence holding each worker's first static chunk
+    const int32_t* tile_b;    // [dyn tiles+1] sequence holding each dynamic tile's first chunk
+    int32_t* dyn_next;        // dynamic tile counter (in the header)
+    int units;                // U = batch * Hkv * sub_groups
     const WsHeader* hdr;      // total chunks, worker count
     uint32_t* status;
     float* partials;          // [slots][partial_slot_floats(GS, D)]

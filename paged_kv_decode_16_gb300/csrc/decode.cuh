@@ -14,12 +14,13 @@
 //   cp.async.bulk) for K and one for V; ragged last chunks copy only their
 //   valid rows.  Rows past the context length are never loaded nor touched.
 // * Balanced split (flash-decoding split-K, stream-K style): all chunks of the
-//   batch are laid end to end (sequence-major, then KV head, then chunk) and
-//   each worker -- one warp -- takes an equal contiguous range.  Long contexts
-//   are split over many warps, short ones packed into one; every warp gets
-//   total/NW chunks whatever the length mix.  A (sequence, KV head) inside one
-//   range is finished in place; one that straddles ranges leaves fp32 partial
-//   states (m, l, o) per warp, merged by the combine kernel.
+//   batch are laid end to end (sequence-major, then KV head, then chunk); each
+//   worker -- one warp -- takes an equal contiguous static range of most of
+//   them, then small dynamic tiles of the rest from a shared counter
+//   (schedule.cuh).  Long contexts are split over many warps, short ones packed
+//   into one.  A (sequence, KV head) inside one piece is finished in place; one
+//   that straddles pieces leaves fp32 partial states (m, l, o), merged by the
+//   combine kernel.
 // * Warps never wait on each other: each owns a STAGES-deep ring of chunk
 //   buffers in shared memory with one mbarrier per stage; lane 0 refills a
 //   stage (K, V, and q when a new unit starts) right after the warp consumed
@@ -34,6 +35,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "schedule.cuh"
 
 namespace pkv {
 
@@ -87,54 +89,6 @@ struct DecodeLayout {
     static_assert(kQBytes % 16 == 0 && kChunkBytes % 16 == 0, "bulk copies need 16 B sizes");
 };
 
-// One chunk's description, computed by the lane that owns it in a window.
-struct ChunkDesc {
-    int u;        // unit = (b * Hkv + h) * sub_groups + sg
-    int k;        // chunk index within the unit
-    int nch;      // chunks of the unit
-    int nvalid;   // valid tokens in the chunk (1..16)
-    long long off;  // first pool row of the chunk ([page][h][slot] rows of D), -1 if the page id is bad
-};
-
-__device__ __forceinline__ ChunkDesc describe_chunk(const DecodeParams& p, int f, int units_per_b) {
-    // sequence b: largest b with prefix[b] <= f (empty sequences are skipped)
-    int lo = 0, hi = p.batch;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.prefix + mid) <= f) lo = mid; else hi = mid;
-    }
-    const int b = lo;
-    const int rem = f - __ldg(p.prefix + b);
-    const int L = __ldg(p.lens_eff + b);
-    const int nch = (L + kChunk - 1) / kChunk;
-    const int uidx = rem / nch;
-    ChunkDesc d;
-    d.k = rem - uidx * nch;
-    d.nch = nch;
-    d.u = b * units_per_b + uidx;
-    d.nvalid = min(kChunk, L - d.k * kChunk);
-    const int h = uidx / p.sub_groups;
-    const int tok = d.k * kChunk;
-    const int page = __ldg(p.table + (long long)b * p.table_stride + tok / p.page_size);
-    if (page >= 0 && page < p.num_pages) {
-        d.off = (((long long)page * p.n_kv_heads + h) * p.page_size + (tok % p.page_size));
-    } else {
-        d.off = -1;
-        set_status(p.status, PKV_DEV_BAD_PAGE);
-    }
-    return d;
-}
-
-__device__ __forceinline__ ChunkDesc shfl_desc(const ChunkDesc& a, int src) {
-    ChunkDesc d;
-    d.u = __shfl_sync(kFull, a.u, src);
-    d.k = __shfl_sync(kFull, a.k, src);
-    d.nch = __shfl_sync(kFull, a.nch, src);
-    d.nvalid = __shfl_sync(kFull, a.nvalid, src);
-    d.off = __shfl_sync(kFull, a.off, src);
-    return d;
-}
-
 template <typename T, int D, int GS, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32)
 decode_kernel(const DecodeParams p) {
@@ -145,6 +99,7 @@ decode_kernel(const DecodeParams p) {
     constexpr int GP = Lay::kGP;
     constexpr int RLOG = ilog2(GP);
     static_assert(GP <= LPT, "group too large for this head dim");
+    static_assert(STAGES <= 4, "tiles of the schedule are at least 4 chunks long");
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -159,8 +114,6 @@ decode_kernel(const DecodeParams p) {
     float* pm = reinterpret_cast<float*>(wsm + Lay::kOffM);
     uint64_t* bar = reinterpret_cast<uint64_t*>(wsm + Lay::kOffBar);
 
-
-    const int units_per_b = p.n_kv_heads * p.sub_groups;
     const int c = lane & (LPT - 1);     // D slice
     const int r = lane / LPT;           // token within a step
     int gsel = 0;
@@ -182,40 +135,22 @@ decode_kernel(const DecodeParams p) {
     pdl_wait();
     pdl_trigger();
 
-    const int total = p.hdr->total_chunks;
     const int nw = p.hdr->num_workers;
     const int gw = blockIdx.x * WARPS + warp;
     if (gw >= nw) return;
-    const int f0 = (int)((long long)gw * total / nw);
-    const int f1 = (int)((long long)(gw + 1) * total / nw);
-    const int n = f1 - f0;
-    if (n <= 0) return;
+    WorkStream ws;
+    ws.init(p, lane, gw);
+    if (ws.stream_end == 0) return;
+    const int units_per_b = ws.units_per_b;
 
-    // Descriptor windows: wa covers chunks [wbase, wbase+32), wb the next 32.
-    int wbase = 0;
-    ChunkDesc wa, wb;
-    wa.off = wb.off = -1;
-    wa.u = wb.u = wa.k = wb.k = wa.nvalid = wb.nvalid = 0;
-    wa.nch = wb.nch = 1;
-    if (lane < n) wa = describe_chunk(p, f0 + lane, units_per_b);
-    if (32 + lane < n) wb = describe_chunk(p, f0 + 32 + lane, units_per_b);
-
-    auto fetch = [&](int j) -> ChunkDesc {
-        const bool second = (j - wbase) >= 32;
-        ChunkDesc src;
-        src.u = second ? wb.u : wa.u;
-        src.k = second ? wb.k : wa.k;
-        src.nch = second ? wb.nch : wa.nch;
-        src.nvalid = second ? wb.nvalid : wa.nvalid;
-        src.off = second ? wb.off : wa.off;
-        return shfl_desc(src, j & 31);
-    };
-
-    auto issue = [&](int j) {
-        const ChunkDesc d = fetch(j);
+    // Issue the copies of stream position j into stage j % STAGES; false past
+    // the end of the stream.
+    auto issue = [&](int j) -> bool {
+        if (!ws.covered(p, j)) return false;
+        const ChunkDesc d = ws.fetch(j);
+        const bool seg_start = ws.seg_start(j, d);
         if (lane == 0) {
             const int st = j % STAGES;
-            const bool seg_start = (j == 0) || (d.k == 0);
             const uint32_t kv_bytes = d.off >= 0 ? (uint32_t)d.nvalid * D * 2 : 0u;
             const uint32_t q_bytes = seg_start ? (uint32_t)Lay::kQBytes : 0u;
             fence_proxy_async_smem();
@@ -233,35 +168,33 @@ decode_kernel(const DecodeParams p) {
                 bulk_g2s(sq + st * GS * D, qg + qrow * D, q_bytes, &bar[st]);
             }
         }
+        return true;
     };
 
-    const int npro = n < STAGES ? n : STAGES;
-    for (int j = 0; j < npro; ++j) issue(j);
+    int issued = 0;
+    while (issued < STAGES && issue(issued)) ++issued;
 
     float qf[GS][8];
     float o[GS][8];
     float m_run = -INFINITY, l_run = 0.f;
     bool seg_whole_start = false;
+    int seg_slot = 0;
 
-    for (int i = 0; i < n; ++i) {
-        if (i > 0 && (i & 31) == 0) {
-            wbase += 32;
-            wa = wb;
-            if (wbase + 32 + lane < n) wb = describe_chunk(p, f0 + wbase + 32 + lane, units_per_b);
-        }
-        const ChunkDesc d = fetch(i);
+    for (int i = 0; i < ws.stream_end; ++i) {
+        ws.consumer_at(p, i, STAGES + 1);
+        const ChunkDesc d = ws.fetch(i);
         const int st = i % STAGES;
         if (!mbar_wait_bounded(&bar[st], (uint32_t)((i / STAGES) & 1))) {
             // A copy never landed.  Report it, wait (bounded) for the copies
             // still in flight into this warp's buffers, and stop.
             if (lane == 0) set_status(p.status, PKV_DEV_TIMEOUT);
-            const int last = (i + STAGES < n ? i + STAGES : n);
-            for (int j = i + 1; j < last; ++j)
+            for (int j = i + 1; j < issued; ++j)
                 mbar_wait_bounded(&bar[j % STAGES], (uint32_t)((j / STAGES) & 1));
             return;
         }
-        const bool seg_start = (i == 0) || (d.k == 0);
+        const bool seg_start = ws.seg_start(i, d);
         if (seg_start) {
+            seg_slot = ws.slot_base(i) + d.u;
             const T* qs = sq + st * GS * D;
 #pragma unroll
             for (int g = 0; g < GS; ++g) {
@@ -362,7 +295,7 @@ decode_kernel(const DecodeParams p) {
             __syncwarp();
         }
 
-        const bool seg_end = (i == n - 1) || (d.k == d.nch - 1);
+        const bool seg_end = ws.seg_end(i, d);
         if (seg_end) {
             const bool whole = seg_whole_start && (d.k == d.nch - 1);
             // tokens were split over the r lanes: sum their o
@@ -401,7 +334,7 @@ decode_kernel(const DecodeParams p) {
                     }
                 }
             } else {
-                float* dst = p.partials + (long long)(d.u + gw) * partial_slot_floats(GS, D);
+                float* dst = p.partials + (long long)seg_slot * partial_slot_floats(GS, D);
                 if (r == 0) {
 #pragma unroll
                     for (int g = 0; g < GS; ++g) {
@@ -418,7 +351,8 @@ decode_kernel(const DecodeParams p) {
             __syncwarp();
         }
         __syncwarp();
-        if (i + STAGES < n) issue(i + STAGES);
+        // refill: positions up to i + STAGES (stage i % STAGES is free again)
+        while (issued <= i + STAGES && issue(issued)) ++issued;
     }
 }
 

@@ -31,6 +31,7 @@
 #include <type_traits>
 
 #include "decode.cuh"
+#include "schedule.cuh"
 
 namespace pkv {
 
@@ -122,6 +123,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
     constexpr bool kTwoHalves = GS > 8; // query rows 8..15 in use
     constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;  // P as bf16 hi + lo
     static_assert(GS <= 16, "one m16 tile of query heads");
+    static_assert(STAGES <= 4, "tiles of the schedule are at least 4 chunks long");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -147,44 +149,26 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
     pdl_wait();
     pdl_trigger();
 
-    const int total = p.hdr->total_chunks;
     const int nw = p.hdr->num_workers;
     const int gw = blockIdx.x * WARPS + warp;
     if (gw >= nw) return;
-    const int f0 = (int)((long long)gw * total / nw);
-    const int f1 = (int)((long long)(gw + 1) * total / nw);
-    const int n = f1 - f0;
-    if (n <= 0) return;
+    WorkStream ws;
+    ws.init(p, lane, gw);
+    if (ws.stream_end == 0) return;
 
-    const int units_per_b = p.n_kv_heads * p.sub_groups;
+    const int units_per_b = ws.units_per_b;
     const int g_lo = lane >> 2;          // query row of c0/c1 (c2/c3: g_lo + 8)
     const int tq = (lane & 3) * 2;       // first token (or d) column of this lane in a tile
     const T* __restrict__ qg = static_cast<const T*>(p.q);
 
-    int wbase = 0;
-    ChunkDesc wa, wb;
-    wa.off = wb.off = -1;
-    wa.u = wb.u = wa.k = wb.k = wa.nvalid = wb.nvalid = 0;
-    wa.nch = wb.nch = 1;
-    if (lane < n) wa = describe_chunk(p, f0 + lane, units_per_b);
-    if (32 + lane < n) wb = describe_chunk(p, f0 + 32 + lane, units_per_b);
-
-    auto fetch = [&](int j) -> ChunkDesc {
-        const bool second = (j - wbase) >= 32;
-        ChunkDesc src;
-        src.u = second ? wb.u : wa.u;
-        src.k = second ? wb.k : wa.k;
-        src.nch = second ? wb.nch : wa.nch;
-        src.nvalid = second ? wb.nvalid : wa.nvalid;
-        src.off = second ? wb.off : wa.off;
-        return shfl_desc(src, j & 31);
-    };
-
-    auto issue = [&](int j) {
-        const ChunkDesc d = fetch(j);
+    // Issue the copies of stream position j into stage j % STAGES; false past
+    // the end of the stream.
+    auto issue = [&](int j) -> bool {
+        if (!ws.covered(p, j)) return false;
+        const ChunkDesc d = ws.fetch(j);
+        const bool seg_start = ws.seg_start(j, d);
         if (lane == 0) {
             const int st = j % STAGES;
-            const bool seg_start = (j == 0) || (d.k == 0);
             const uint32_t kv_bytes = d.off >= 0 ? (uint32_t)Lay::kStageBytes : 0u;
             const uint32_t q_bytes = seg_start ? (uint32_t)Lay::kQBytes : 0u;
             fence_proxy_async_smem();
@@ -208,33 +192,33 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 bulk_g2s(sq + st * GS * D, qg + qrow * D, q_bytes, &bar[st]);
             }
         }
+        return true;
     };
 
-    const int npro = n < STAGES ? n : STAGES;
-    for (int j = 0; j < npro; ++j) issue(j);
+    int issued = 0;
+    while (issued < STAGES && issue(issued)) ++issued;
 
     uint32_t qa[KSTEPS][4];     // A fragments of Q (rows g_lo, g_lo+8)
     float o[NT][4];             // O accumulators (c0,c1: row g_lo; c2,c3: row g_lo+8)
     float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
     bool seg_whole_start = false;
+    int seg_slot = 0;
 
-    for (int i = 0; i < n; ++i) {
-        if (i > 0 && (i & 31) == 0) {
-            wbase += 32;
-            wa = wb;
-            if (wbase + 32 + lane < n) wb = describe_chunk(p, f0 + wbase + 32 + lane, units_per_b);
-        }
-        const ChunkDesc d = fetch(i);
+    for (int i = 0; i < ws.stream_end; ++i) {
+        ws.consumer_at(p, i, STAGES + 1);
+        const ChunkDesc d = ws.fetch(i);
         const int st = i % STAGES;
         if (!mbar_wait_bounded(&bar[st], (uint32_t)((i / STAGES) & 1))) {
+            // A copy never landed.  Report it, wait (bounded) for the copies
+            // still in flight into this warp's buffers, and stop.
             if (lane == 0) set_status(p.status, PKV_DEV_TIMEOUT);
-            const int last = (i + STAGES < n ? i + STAGES : n);
-            for (int j = i + 1; j < last; ++j)
+            for (int j = i + 1; j < issued; ++j)
                 mbar_wait_bounded(&bar[j % STAGES], (uint32_t)((j / STAGES) & 1));
             return;
         }
-        const bool seg_start = (i == 0) || (d.k == 0);
+        const bool seg_start = ws.seg_start(i, d);
         if (seg_start) {
+            seg_slot = ws.slot_base(i) + d.u;
             // A fragments of Q: a0 (row g, k tq..tq+1), a1 (row g+8), a2 (k+8), a3
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(sq + st * GS * D);
 #pragma unroll
@@ -381,7 +365,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
             }
         }
 
-        const bool seg_end = (i == n - 1) || (d.k == d.nch - 1);
+        const bool seg_end = ws.seg_end(i, d);
         if (seg_end) {
             const bool whole = seg_whole_start && (d.k == d.nch - 1);
             const int b = d.u / units_per_b;
@@ -404,7 +388,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                                 Cvt<T>::pack2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
                         }
                     } else {
-                        float* dst = p.partials + (long long)(d.u + gw) * partial_slot_floats(GS, D);
+                        float* dst = p.partials + (long long)seg_slot * partial_slot_floats(GS, D);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             *reinterpret_cast<float2*>(dst + g * D + nt * 8 + tq) =
@@ -419,7 +403,8 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
             }
         }
         __syncwarp();
-        if (i + STAGES < n) issue(i + STAGES);
+        // refill: positions up to i + STAGES (stage i % STAGES is free again)
+        while (issued <= i + STAGES && issue(issued)) ++issued;
     }
 }
 

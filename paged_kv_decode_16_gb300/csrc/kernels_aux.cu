@@ -74,6 +74,12 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
             if (L > pa.cap) { L = pa.cap; atomicOr(&flags, PKV_DEV_BAD_LEN); }
             pa.lens_eff[b] = (int32_t)L;
             cnt = (int)((L + kChunk - 1) / kChunk) * pa.units_per_b;
+            if (pa.table) {  // the decode kernel reads this row right away: bring it into L2
+                const int pages = (int)((L + pa.page_size - 1) / pa.page_size);
+                const int32_t* row = pa.table + (long long)b * pa.table_stride;
+                for (int e = 0; e < pages; e += 32)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + e));
+            }
         }
         int x = cnt;  // inclusive warp scan
 #pragma unroll
@@ -99,6 +105,7 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
         if (tid == 0) running += warp_tot[nwarps - 1];
         __syncthreads();
     }
+    __shared__ int s_total, s_nw, s_sw, s_K, s_nt;
     if (tid == 0) {
         long long total = running;
         uint32_t f = flags;
@@ -116,11 +123,53 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
                 nw = (int)min((long long)pa.workers_auto, want < 1 ? 1LL : want);
             }
         }
+        // static ranges: static_pct % of the chunks, equal per worker; the rest
+        // in dynamic tiles of K chunks (K grows so that the tiles fit the slots)
+        long long sw = nw > 0 ? (total * pa.static_pct / 100) / nw : 0;
+        // a tile holds at most 32 chunks (one descriptor per lane): when the
+        // tail would need longer tiles, the static ranges grow instead
+        const long long dyn_cap = (long long)kMaxDynTile * pa.dyn_tiles_max;
+        if (nw > 0 && total - sw * nw > dyn_cap) sw = (total - dyn_cap + nw - 1) / nw;
+        // ranges shorter than kMinStaticChunks go dynamic (unless the tail is full)
+        if (sw < kMinStaticChunks) sw = total > dyn_cap ? kMinStaticChunks : 0;
+        const long long ts = sw * nw;
+        const long long dyn = total - ts;
+        long long K = (dyn + pa.dyn_tiles_max - 1) / pa.dyn_tiles_max;
+        if (K < kMinDynTile) K = kMinDynTile;
+        const int nt = dyn > 0 ? (int)((dyn + K - 1) / K) : 0;
         pa.hdr->total_chunks = (int32_t)total;
         pa.hdr->num_workers = nw;
+        pa.hdr->static_per_worker = (int32_t)sw;
+        pa.hdr->static_total = (int32_t)ts;
+        pa.hdr->dyn_tile = (int32_t)K;
+        pa.hdr->dyn_tiles = nt;
+        pa.hdr->dyn_next = 0;
         pa.hdr->append_slots = append_ctas;
         pa.hdr->status = f;
+        s_total = (int)total;
+        s_nw = nw;
+        s_sw = (int)sw;
+        s_K = (int)K;
+        s_nt = nt;
     }
+    __syncthreads();
+    // sequence holding each worker's first static chunk (w * sw; for w = NW the
+    // last static chunk) and each dynamic tile's first chunk (for t = NT the
+    // last chunk), so that a worker searches only the sequences of its piece
+    const int T = s_total, nw = s_nw, sw = s_sw, K = s_K, nt = s_nt;
+    const int ts = sw * nw;
+    auto seq_of = [&](int f) {
+        int lo = 0, hi = pa.batch;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pa.prefix[mid] <= f) lo = mid; else hi = mid;
+        }
+        return lo;
+    };
+    for (int w = tid; w <= nw && T > 0; w += blockDim.x)
+        pa.wstart[w] = sw > 0 ? seq_of(w < nw ? w * sw : ts - 1) : 0;
+    for (int t = tid; t <= nt && T > 0; t += blockDim.x)
+        pa.tile_b[t] = seq_of(t < nt ? ts + t * K : T - 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -154,27 +203,44 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
         for (int idx = tid; idx < n; idx += blockDim.x) o[idx] = T(0.f);
         return;
     }
-    const long long total = hdr->total_chunks;
-    const long long nw = hdr->num_workers;
+    const int total = hdr->total_chunks;
+    const int nw = hdr->num_workers;
     if (total <= 0 || nw <= 0) return;
-    const long long a = (long long)prefix[b] + (long long)uidx * nch;
-    const long long e = a + nch;
-    const int w_first = (int)(((a + 1) * nw - 1) / total);
-    const int w_last = (int)((e * nw - 1) / total);
-    if (w_first == w_last) return;
-    const int ns = w_last - w_first + 1;
+    // segments of unit u: one per worker whose static range meets its chunks
+    // [a, e), one per dynamic tile that does (schedule.cuh)
+    const int sw = hdr->static_per_worker, ts = hdr->static_total, K = hdr->dyn_tile;
+    const int a = prefix[b] + uidx * nch;
+    const int e = a + nch;
+    int s_first = 0, s_count = 0, t_first = 0, t_count = 0;
+    if (a < ts) {
+        s_first = a / sw;
+        s_count = (min(e, ts) - 1) / sw - s_first + 1;
+    }
+    if (e > ts) {
+        t_first = (max(a, ts) - ts) / K;
+        t_count = (e - 1 - ts) / K - t_first + 1;
+    }
+    const int ns = s_count + t_count;
+    if (ns <= 1) return;  // finished in place by its worker
+    const int units = gridDim.x;
     const long long stride = partial_slot_floats(gs, D);
-    const float* base = partials + (long long)(u + w_first) * stride;  // slots u+w_first..u+w_last
+    // slot of the s-th segment: static u + w, dynamic U + NW + u + t
+    auto slot_of = [&](int s) -> long long {
+        return s < s_count ? (long long)(u + s_first + s)
+                           : (long long)units + nw + u + t_first + (s - s_count);
+    };
     const int warp = tid >> 5, lane = tid & 31;
     for (int g = warp; g < gs; g += (int)(blockDim.x >> 5)) {
         float M = -INFINITY;
-        for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * stride + n + g]);
+        for (int s = lane; s < ns; s += 32) M = fmaxf(M, partials[slot_of(s) * stride + n + g]);
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, m));
         float S = 0.f;
         if (M != -INFINITY) {
-            for (int s = lane; s < ns; s += 32)
-                S += exp2f(base[s * stride + n + g] - M) * base[s * stride + n + gs + g];
+            for (int s = lane; s < ns; s += 32) {
+                const float* pp = partials + slot_of(s) * stride;
+                S += exp2f(pp[n + g] - M) * pp[n + gs + g];
+            }
         }
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) S += __shfl_xor_sync(kFull, S, m);
@@ -192,7 +258,7 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
         if (M != -INFINITY) {
 #pragma unroll 4
             for (int s = 0; s < ns; ++s) {
-                const float* pp = base + s * stride;
+                const float* pp = partials + slot_of(s) * stride;
                 const float w = exp2f(pp[n + g] - M);
                 const float4 v = *reinterpret_cast<const float4*>(pp + g * D + d4 * 4);
                 acc.x = fmaf(w, v.x, acc.x);

@@ -19,7 +19,14 @@ struct PlanArgs {
     int min_chunks;        // automatic mode: at least this many chunks per worker
     int32_t* lens_eff;     // [B] clamped lengths (workspace)
     int32_t* prefix;       // [B+1] chunk prefix sums (workspace)
+    int32_t* wstart;       // [workers+1] sequence of each worker's first static chunk
+    int32_t* tile_b;       // [dyn_tiles_max+1] sequence of each dynamic tile's first chunk
+    int static_pct;        // share of the chunks given out as static ranges (percent)
+    int dyn_tiles_max;     // upper bound on the dynamic tiles (workspace slots)
     WsHeader* hdr;
+    const int32_t* table;  // page table (nullable), prefetched into L2 for the decode kernel
+    int table_stride;
+    int page_size;
 };
 
 struct AppendArgs {
@@ -40,6 +47,12 @@ cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
                            int group, int n_q_heads, cudaStream_t stream);
+
+// smallest static range worth giving a worker (shorter ranges become dynamic)
+constexpr int kMinStaticChunks = 4;
+// chunks per dynamic tile: at least the decode kernels' stages, at most one per lane
+constexpr int kMinDynTile = 4;
+constexpr int kMaxDynTile = 32;
 
 cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status, cudaStream_t stream);
 
