@@ -285,6 +285,43 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                              size_t ws_bytes, int num_workers, pkv_decode_variant variant,
                              pkv_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Decode without a caller-provided workspace.
+ * (No counterpart on the source pages: an addition of this library.)
+ *
+ * Some callers cannot allocate device memory at the point where they decode:
+ * a serving loop that forbids allocation after warm-up (cudaMalloc / cudaFree
+ * may synchronise the device and stall every stream), a plugin or custom op
+ * inside a host framework that owns all device memory through its own arena
+ * and offers no workspace hook, or an embedded runtime with a fixed memory
+ * budget.  This entry point needs no workspace from them: it computes exactly
+ * what paged_decode_attention computes (same arguments without workspace and
+ * ws_bytes, same kernels), with its workspace taken from a fixed array of
+ * PKV_NO_ALLOC_SCRATCH_BYTES bytes that the library defines in device memory.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   - Size limit: shapes whose workspace (paged_decode_workspace_size with the
+ *     same num_workers and variant) exceeds PKV_NO_ALLOC_SCRATCH_BYTES are
+ *     rejected with PKV_ERR_WORKSPACE before anything is launched.
+ *   - Every GPU that loads the library holds the array until the process exits.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; the
+ *     plan kernel of each call rewrites every field that must start fresh (the
+ *     header, counters and the status word), so nothing needs clearing by the
+ *     caller.  Calls that overlap on the GPU (on different streams, or from
+ *     different threads without ordering) race on the array: order them. */
+#define PKV_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+
+pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool,
+                                           const int32_t* page_table, int table_stride,
+                                           const int32_t* context_lens, int batch,
+                                           int n_q_heads, int n_kv_heads, int head_dim,
+                                           int page_size, int num_pages, pkv_dtype dtype,
+                                           float scale, void* out, int num_workers,
+                                           pkv_decode_variant variant, pkv_stream stream);
+
 /* Copy the status of the last plan/decode/step call on this workspace to
  * *status_out (host): the OR of the PKV_DEV_* bits of its kernels.  This call
  * synchronises with the device.  Returns DEVICE_CHECK when any bit is set,

@@ -22,7 +22,7 @@ __all__ = [
     "PagedKVError", "load_library", "library_path", "pkv_status_string", "pkv_version",
     "Pool", "kv_pool_create", "kv_append", "kv_gather", "paged_decode_workspace_size",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
-    "paged_decode_step",
+    "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
     "VARIANT_AUTO", "VARIANT_CUDA_CORES", "VARIANT_TENSOR_CORES",
 ]
@@ -34,6 +34,8 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
 DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 # decode kernels (pkv_decode_variant)
 VARIANT_AUTO, VARIANT_CUDA_CORES, VARIANT_TENSOR_CORES = 0, 1, 2
+# size of the library's fixed device scratch (PKV_NO_ALLOC_SCRATCH_BYTES)
+NO_ALLOC_SCRATCH_BYTES = 32 << 20
 _DT = {torch.float16: 0, torch.bfloat16: 1}
 
 _lib = None
@@ -85,6 +87,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
                                    I),
         "paged_decode_step": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, I,
                                V], I),
+        "paged_decode_attention_no_alloc": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, I, I,
+                                             V], I),
         "pkv_read_device_status": ([V, ctypes.POINTER(ctypes.c_uint32)], I),
     }
     for name, (args, res) in sig.items():
@@ -305,6 +309,25 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
         _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace),
         workspace.numel(), int(num_workers), int(variant), _stream(stream)),
         "paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                    page_table: torch.Tensor, context_lens: torch.Tensor,
+                                    scale: float, out: torch.Tensor, num_workers: int = 0,
+                                    stream=None, variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """paged_decode_attention without a workspace argument: the library uses its
+    own fixed device scratch of NO_ALLOC_SCRATCH_BYTES bytes and allocates
+    nothing.  For callers that must not allocate device memory at decode time.
+    Calls share that scratch, so calls that overlap on the GPU race; make the
+    first call on a device before any stream capture (it looks the scratch up)."""
+    B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _check(load_library().paged_decode_attention_no_alloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1],
+        _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), int(num_workers),
+        int(variant), _stream(stream)),
+        "paged_decode_attention_no_alloc")
     return out
 
 

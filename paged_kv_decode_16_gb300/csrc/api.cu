@@ -345,6 +345,31 @@ pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, v
         out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.group, n_q_heads, stream));
 }
 
+// --- fixed device scratch for paged_decode_attention_no_alloc -------------
+// Callers that may not allocate device memory (see pagedkv.h) get the
+// decode workspace from this file-scope array.  In host code the symbol is
+// only a host-side stand-in, so its device address is looked up once per
+// device with cudaGetSymbolAddress (with that device current) and cached.
+static __device__ __align__(256) uint8_t g_no_alloc_scratch[PKV_NO_ALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+pkv_status no_alloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || !p) return PKV_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return PKV_OK;
+}
+
 pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t* positions,
                             const int32_t* table, int table_stride, void* k_pool, void* v_pool,
                             int n_kv_heads, int head_dim, int page_size, int num_pages) {
@@ -610,6 +635,41 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
         PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
+}
+
+pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool,
+                                           const int32_t* page_table, int table_stride,
+                                           const int32_t* context_lens, int batch,
+                                           int n_q_heads, int n_kv_heads, int head_dim,
+                                           int page_size, int num_pages, pkv_dtype dtype,
+                                           float scale, void* out, int num_workers,
+                                           pkv_decode_variant variant, pkv_stream stream) {
+    // shape / pointer / alias checks first (the scratch address is only needed
+    // once the call is known to be well formed)
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
+    if (st != PKV_OK) return st;
+    if (batch == 0) return PKV_OK;
+    void* scratch = nullptr;
+    if ((st = no_alloc_scratch(&scratch)) != PKV_OK) return st;
+    st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride, context_lens, true,
+                              batch, n_q_heads, n_kv_heads, head_dim, page_size, num_pages, dtype,
+                              scale, out, scratch, PKV_NO_ALLOC_SCRATCH_BYTES, num_workers,
+                              variant);
+    if (st != PKV_OK) return st;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           variant, &s)) != PKV_OK)
+        return st;
+    // the workspace these shapes need must fit the fixed array
+    if (s.ws.total > (size_t)PKV_NO_ALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = do_plan(context_lens, page_table, batch, page_size, table_stride, num_workers,
+                      scratch, s, nullptr, cs)) != PKV_OK)
+        return st;
+    if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
+                     head_dim, page_size, num_pages, dtype, scale, out, scratch, s, cs)) != PKV_OK)
+        return st;
+    return do_combine(batch, n_q_heads, head_dim, dtype, out, scratch, s, cs);
 }
 
 pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {

@@ -210,3 +210,23 @@ def test_allocator_threads(lib):
         assert all(lib.kv_pool_refcount(h, i) == 0 for i in range(512))
     finally:
         lib.kv_pool_destroy(h)
+
+
+def test_no_alloc_scratch_size_matches_header(lib):
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+PKV_NO_ALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "PKV_NO_ALLOC_SCRATCH_BYTES not found"
+    assert int(m.group(1)) << int(m.group(2)) == pkv.NO_ALLOC_SCRATCH_BYTES
+
+
+def test_no_alloc_shape_checks_on_host(lib):
+    V = ctypes.c_void_p
+
+    def call(d=128, batch=2, hq=8, hkv=2):
+        return lib.paged_decode_attention_no_alloc(V(A), V(A * 8), V(A * 16), V(A * 24), 4,
+                                                   V(A * 25), batch, hq, hkv, d, 16, 8, BF16,
+                                                   ctypes.c_float(0.088), V(A * 26), 0, 0, None)
+    assert call(d=96) == UNSUPPORTED
+    assert call(hq=6, hkv=4) == INVALID
+    assert call(batch=-1) == INVALID
+    assert call(batch=0) == OK
