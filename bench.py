@@ -50,6 +50,8 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ["paged_kv_decode_16_gb300/csrc/decode.cuh",
                   "paged_kv_decode_16_gb300/csrc/decode_mma.cuh",
+                  "paged_kv_decode_16_gb300/csrc/schedule.cuh",
+                  "paged_kv_decode_16_gb300/csrc/merge.cuh",
                   "paged_kv_decode_16_gb300/csrc/common.cuh"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama3_8b_shape.md")
 

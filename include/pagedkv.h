@@ -184,18 +184,16 @@ pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_
  *  grouped and streaming block-S decode variants in the serving knob list.)
  *
  * Work split: every (sequence, KV head) is cut into chunks of 16 tokens; the
- * chunks of the whole batch are laid end to end; 80% of them are divided into
- * equal contiguous static ranges, one per worker (a warp), and the rest into
- * small tiles that workers take from a shared counter when their range is
- * done (this absorbs SMs that get less memory bandwidth than others).  A
- * worker reads each chunk's K and V once for the whole query group.  A
- * (sequence, KV head) that lies in one worker's range or one tile is finished
- * there; one spread over several pieces leaves fp32 partial states (m, l, o)
- * that paged_decode_combine merges.  Which worker takes which dynamic tile
- * varies from run to run, but the pieces, the merge order and so the result
- * bits depend only on the context lengths and the worker count, never on
- * physical page ids or timing: permuting pages or rerunning gives bitwise
- * equal results.
+ * chunks of the whole batch are laid end to end and divided into contiguous
+ * ranges, one per worker (a warp), equal to within one chunk.  A worker reads
+ * each chunk's K and V once for the whole query group.  A (sequence, KV head)
+ * that lies in one worker's range is finished there; one spread over several
+ * ranges leaves fp32 partial states (m, l, o) that are merged either by the
+ * worker that finishes its last piece (a per-unit counter of finished chunks,
+ * in the decode kernel) or by paged_decode_combine (see paged_decode_run's
+ * merge).  The ranges, the merge order and so the result bits depend only on
+ * the context lengths and the worker count, never on physical page ids or
+ * timing: permuting pages or rerunning gives bitwise equal results.
  *
  * num_workers: 0 = automatic (the GPU's SM count x resident warps of the
  * kernel, capped so each worker gets at least 4 chunks); n > 0 = at most n
@@ -224,8 +222,9 @@ pkv_status paged_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                                        size_t* bytes);
 
 /* Plan step: validates context_lens on the device (clamping to the table row,
- * flagging PKV_DEV_BAD_LEN), resets the status word, and writes the chunk
- * prefix sums and the worker count into the workspace.  One kernel (one CTA). */
+ * flagging PKV_DEV_BAD_LEN), resets the status word and the merge counters,
+ * and writes the chunk prefix sums, the worker count and the ranges into the
+ * workspace.  One kernel (one CTA). */
 pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_heads,
                              int n_kv_heads, int head_dim, int page_size, int table_stride,
                              int num_workers, pkv_decode_variant variant, void* workspace,
@@ -233,27 +232,33 @@ pkv_status paged_decode_plan(const int32_t* context_lens, int batch, int n_q_hea
 
 /* Main step on a workspace prepared by paged_decode_plan with the same shapes,
  * num_workers and variant; every run needs a plan of its own (the plan resets
- * the counter that hands out the dynamic tiles).  The decode kernel (persistent grid of workers;
- * asynchronous copies of K/V chunks into shared memory, fp32 online softmax).
- * Writes out for every (sequence, KV head) finished by one worker and partial
- * states for the rest.  Pools of more than 2^31 - 1 rows (num_pages *
- * n_kv_heads * page_size) are UNSUPPORTED by the tensor-core variant. */
+ * the status word and the merge counters).  The decode kernel (persistent
+ * grid of workers; asynchronous copies of K/V chunks into shared memory, fp32
+ * online softmax).  Writes out for every (sequence, KV head) finished by one
+ * worker, zeros for sequences with no tokens, and partial states for the
+ * rest.  merge = 1: the worker that finishes the last piece of a split
+ * (sequence, KV head) merges it into out, so out is complete when the kernel
+ * ends; merge = 0: split units are left to paged_decode_combine.  Both give
+ * bitwise equal out.  merge other than 0 or 1 is INVALID_ARG.  Pools of more
+ * than 2^31 - 1 rows (num_pages * n_kv_heads * page_size) are UNSUPPORTED by
+ * the tensor-core variant. */
 pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* page_table, int table_stride, int batch,
                             int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                             int num_pages, pkv_dtype dtype, float scale, void* out,
                             void* workspace, size_t ws_bytes, int num_workers,
-                            pkv_decode_variant variant, pkv_stream stream);
+                            pkv_decode_variant variant, int merge, pkv_stream stream);
 
-/* Combine step: for every (sequence, KV head) split over several workers,
- * out = sum_i w_i o_i / sum_i w_i l_i with w_i = 2^(m_i - max m) (partials
- * keep m in base-2 units); writes zeros for sequences with no tokens. */
+/* Combine step after paged_decode_run with merge = 0: for every (sequence,
+ * KV head) split over several workers, out = sum_i w_i o_i / sum_i w_i l_i
+ * with w_i = 2^(m_i - max m) (partials keep m in base-2 units).  One CTA per
+ * (sequence, KV head); unsplit ones exit at once. */
 pkv_status paged_decode_combine(int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                 pkv_dtype dtype, void* out, void* workspace, size_t ws_bytes,
                                 int num_workers, pkv_decode_variant variant, pkv_stream stream);
 
-/* The whole decode: plan + run + combine (three kernels on `stream`, chained
- * with programmatic dependent launch).  q, k_pool, v_pool, page_table,
+/* The whole decode: plan + run (merge = 0) + combine (three kernels on
+ * `stream`, chained with programmatic dependent launch).  q, k_pool, v_pool, page_table,
  * context_lens, out, workspace (device).  out must not overlap q, the pools,
  * the table, the lengths or the workspace (ALIAS).  ws_bytes >=
  * paged_decode_workspace_size(...) (else WORKSPACE).  scale multiplies q.k

@@ -81,7 +81,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "kv_gather": ([V, V, I, V, I, I, V, V, V, V], I),
         "paged_decode_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_plan": ([V, I, I, I, I, I, I, I, I, V, Z, V], I),
-        "paged_decode_run": ([V, V, V, V, I, I, I, I, I, I, I, I, F, V, V, Z, I, I, V], I),
+        "paged_decode_run": ([V, V, V, V, I, I, I, I, I, I, I, I, F, V, V, Z, I, I, I, V], I),
         "paged_decode_combine": ([I, I, I, I, I, V, V, Z, I, I, V], I),
         "paged_decode_attention": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I, I, V],
                                    I),
@@ -366,13 +366,15 @@ def paged_decode_plan(context_lens: torch.Tensor, n_q_heads: int, n_kv_heads: in
 
 
 def paged_decode_run(q, k_pool, v_pool, page_table, scale: float, out, workspace,
-                     num_workers: int = 0, stream=None, variant: int = VARIANT_AUTO) -> None:
+                     num_workers: int = 0, stream=None, variant: int = VARIANT_AUTO,
+                     merge: bool = False) -> None:
+    """The decode kernel; merge=True also merges split units (no combine needed)."""
     B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
     _dev(workspace, "workspace", torch.uint8)
     _check(load_library().paged_decode_run(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1], B, Hq, Hkv,
         D, P, NP, dt, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
-        int(num_workers), int(variant), _stream(stream)), "paged_decode_run")
+        int(num_workers), int(variant), int(bool(merge)), _stream(stream)), "paged_decode_run")
 
 
 def paged_decode_combine(out: torch.Tensor, n_kv_heads: int, workspace: torch.Tensor,

@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "kernels_aux.cuh"
+#include "merge.cuh"
 #include "pool_impl.hpp"
 
 namespace {
@@ -80,6 +81,7 @@ struct KernelPick {
     int smem() const {
         return variant == PKV_VARIANT_TENSOR_CORES ? mma.smem_bytes : cc.smem_bytes;
     }
+    int stages() const { return variant == PKV_VARIANT_TENSOR_CORES ? mma.stages : cc.stages; }
 };
 
 KernelPick pick_kernel(pkv_dtype dtype, int head_dim, int variant, int gs) {
@@ -132,20 +134,13 @@ pkv_status prepare_kernel(const KernelPick& k, int* auto_workers) {
     return PKV_OK;
 }
 
-// Static ranges take this share of the chunks; the rest goes out in dynamic
-// tiles, at most kDynTilesPerWorker per worker.
-constexpr int kStaticPercent = 80;
-constexpr int kDynTilesPerWorker = 4;
-
 struct WsLayout {
-    size_t lens_eff, prefix, wstart, tile_b, partials, total;
-    int dyn_tiles_max;
+    size_t lens_eff, prefix, wstart, unit_done, partials, total;
 };
 
-// Partial slots: static segments u + w < U + NW; dynamic U + NW + u + t < 2U + NW + NT.
+// Partial slots: the segment of unit u in worker w's range uses slot u + w < U + NW.
 WsLayout ws_layout(int batch, long long units, int gs, int head_dim, int workers) {
     WsLayout w;
-    w.dyn_tiles_max = kDynTilesPerWorker * workers;
     size_t off = sizeof(WsHeader);
     w.lens_eff = off;
     off += align256((size_t)batch * 4);
@@ -153,10 +148,10 @@ WsLayout ws_layout(int batch, long long units, int gs, int head_dim, int workers
     off += align256((size_t)(batch + 1) * 4);
     w.wstart = off;
     off += align256((size_t)(workers + 1) * 4);
-    w.tile_b = off;
-    off += align256((size_t)(w.dyn_tiles_max + 1) * 4);
+    w.unit_done = off;
+    off += align256((size_t)units * 4);
     w.partials = off;
-    const size_t slots = (size_t)(2 * units + workers + w.dyn_tiles_max);
+    const size_t slots = (size_t)(units + workers);
     off += align256(slots * pkv::partial_slot_floats(gs, head_dim) * 4);
     w.total = off;
     return w;
@@ -170,6 +165,7 @@ struct DecodeSetup {
     int workers_auto;  // automatic count for this kernel on this device
     KernelPick kernel;
     WsLayout ws;
+    int merge_batch;   // partial slots per merge batch: as many as a warp's stage buffers hold
 };
 
 // AUTO picks the tensor-core kernel; CUDA cores on request.
@@ -195,6 +191,12 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     if (st != PKV_OK) return st;
     s->workers = num_workers > 0 ? num_workers : s->workers_auto;
     s->ws = ws_layout(batch, s->units, s->gs, head_dim, s->workers);
+    // a warp's stage buffers: stages x (K + V) chunks of 16 rows x head_dim x 2 bytes
+    const int stage_bytes = s->kernel.stages() * 64 * head_dim;
+    s->merge_batch = (stage_bytes - pkv::merge_smem_bytes(0, s->gs, head_dim)) /
+                     (pkv::partial_slot_floats(s->gs, head_dim) * 4);
+    if (s->merge_batch > 32) s->merge_batch = 32;
+    if (s->merge_batch < 1) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
 
@@ -279,10 +281,9 @@ pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch,
     pa.lens_eff = reinterpret_cast<int32_t*>(ws + s.ws.lens_eff);
     pa.prefix = reinterpret_cast<int32_t*>(ws + s.ws.prefix);
     pa.wstart = reinterpret_cast<int32_t*>(ws + s.ws.wstart);
-    pa.tile_b = reinterpret_cast<int32_t*>(ws + s.ws.tile_b);
-    pa.static_pct = kStaticPercent;
-    pa.dyn_tiles_max = s.ws.dyn_tiles_max;
     pa.hdr = reinterpret_cast<WsHeader*>(ws);
+    pa.unit_done = reinterpret_cast<int32_t*>(ws + s.ws.unit_done);
+    pa.units = s.units;
     pa.table = table;
     pa.table_stride = table_stride;
     pa.page_size = page_size;
@@ -292,7 +293,7 @@ pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch,
 pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
                   int table_stride, int batch, int n_q_heads, int n_kv_heads, int head_dim,
                   int page_size, int num_pages, pkv_dtype dtype, float scale, void* out,
-                  void* workspace, const DecodeSetup& s, cudaStream_t stream) {
+                  void* workspace, const DecodeSetup& s, bool merge, cudaStream_t stream) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     pkv::DecodeParams p;
     p.q = q;
@@ -302,12 +303,12 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.lens_eff = reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff);
     p.prefix = reinterpret_cast<const int32_t*>(ws + s.ws.prefix);
     p.wstart = reinterpret_cast<const int32_t*>(ws + s.ws.wstart);
-    p.tile_b = reinterpret_cast<const int32_t*>(ws + s.ws.tile_b);
-    p.dyn_next = &reinterpret_cast<WsHeader*>(ws)->dyn_next;
     p.units = (int)s.units;
     p.hdr = reinterpret_cast<const WsHeader*>(ws);
     p.status = &reinterpret_cast<WsHeader*>(ws)->status;
     p.partials = reinterpret_cast<float*>(ws + s.ws.partials);
+    p.unit_done = merge ? reinterpret_cast<int32_t*>(ws + s.ws.unit_done) : nullptr;
+    p.merge_batch = s.merge_batch;
     p.out = out;
     p.table_stride = table_stride;
     p.batch = batch;
@@ -342,7 +343,8 @@ pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, v
         dtype, head_dim, reinterpret_cast<const float*>(ws + s.ws.partials),
         reinterpret_cast<const int32_t*>(ws + s.ws.prefix),
         reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<const WsHeader*>(ws),
-        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.group, n_q_heads, stream));
+        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.group, n_q_heads, s.merge_batch,
+        stream));
 }
 
 // --- fixed device scratch for paged_decode_attention_no_alloc -------------
@@ -529,19 +531,21 @@ pkv_status paged_decode_run(const void* q, const void* k_pool, const void* v_poo
                             int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                             int num_pages, pkv_dtype dtype, float scale, void* out,
                             void* workspace, size_t ws_bytes, int num_workers,
-                            pkv_decode_variant variant, pkv_stream stream) {
+                            pkv_decode_variant variant, int merge, pkv_stream stream) {
     pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride, nullptr,
                                          false, batch, n_q_heads, n_kv_heads, head_dim,
                                          page_size, num_pages, dtype, scale, out, workspace,
                                          ws_bytes, num_workers, variant);
-    if (st != PKV_OK || batch == 0) return st;
+    if (st != PKV_OK) return st;
+    if (merge != 0 && merge != 1) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
     DecodeSetup s;
     if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
                            variant, &s)) != PKV_OK)
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     return do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                  head_dim, page_size, num_pages, dtype, scale, out, workspace, s,
+                  head_dim, page_size, num_pages, dtype, scale, out, workspace, s, merge != 0,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -588,7 +592,7 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
                       workspace, s, nullptr, cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, cs)) !=
+                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, false, cs)) !=
         PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
@@ -631,7 +635,7 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                       workspace, s, &a, cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, cs)) !=
+                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, false, cs)) !=
         PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
@@ -667,7 +671,8 @@ pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, co
                       scratch, s, nullptr, cs)) != PKV_OK)
         return st;
     if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                     head_dim, page_size, num_pages, dtype, scale, out, scratch, s, cs)) != PKV_OK)
+                     head_dim, page_size, num_pages, dtype, scale, out, scratch, s, false, cs)) !=
+        PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, scratch, s, cs);
 }

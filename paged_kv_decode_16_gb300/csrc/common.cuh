@@ -28,14 +28,21 @@ struct WsHeader {
     int32_t num_workers;     // workers that received a non-empty range
     int32_t append_slots;    // append_status entries written by this call
     uint32_t append_status[kMaxAppendCtas];  // PKV_DEV_* bits of each fused-append CTA
-    int32_t static_per_worker;  // chunks in each worker's static range
-    int32_t static_total;       // static_per_worker * num_workers
-    int32_t dyn_tile;           // chunks per dynamic tile
-    int32_t dyn_tiles;          // dynamic tiles
-    int32_t dyn_next;           // next dynamic tile to hand out (counter, reset by the plan)
-    int32_t pad[64 - 9 - kMaxAppendCtas];
+    int32_t chunks_per_worker;  // sw: every worker's range holds sw or sw + 1 chunks
+    int32_t extra_chunks;       // r: workers 0 .. r-1 hold sw + 1 chunks
+    int32_t pad[64 - 6 - kMaxAppendCtas];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// First chunk of worker w's range (workers 0 .. r-1 hold sw + 1 chunks, the
+// others sw), and the worker whose range holds chunk f.
+__host__ __device__ __forceinline__ int range_begin(int w, int sw, int r) {
+    return w * sw + (w < r ? w : r);
+}
+__host__ __device__ __forceinline__ int worker_of(int f, int sw, int r) {
+    const int big = r * (sw + 1);
+    return f < big ? f / (sw + 1) : r + (f - big) / sw;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -185,13 +192,14 @@ struct DecodeParams {
     const int32_t* table;     // [B][stride]
     const int32_t* lens_eff;  // [B] lengths after the plan's clamp (workspace)
     const int32_t* prefix;    // [B+1] chunk prefix sums (workspace)
-    const int32_t* wstart;    // [workers+1] sequence holding each worker's first static chunk
-    const int32_t* tile_b;    // [dyn tiles+1] sequence holding each dynamic tile's first chunk
-    int32_t* dyn_next;        // dynamic tile counter (in the header)
+    const int32_t* wstart;    // [workers+1] sequence holding each worker's first chunk
     int units;                // U = batch * Hkv * sub_groups
     const WsHeader* hdr;      // total chunks, worker count
     uint32_t* status;
     float* partials;          // [slots][partial_slot_floats(GS, D)]
+    int32_t* unit_done;       // [U] chunks finished per unit (zeroed by the plan); null: split
+                              // units are left to the combine kernel
+    int merge_batch;          // partial slots merged per batch (fit the warp's stage buffers)
     void* out;                // [B][Hq][D]
     int table_stride;
     int batch, n_q_heads, n_kv_heads, page_size, num_pages;

@@ -35,6 +35,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "merge.cuh"
 #include "schedule.cuh"
 
 namespace pkv {
@@ -137,10 +138,17 @@ decode_kernel(const DecodeParams p) {
 
     const int nw = p.hdr->num_workers;
     const int gw = blockIdx.x * WARPS + warp;
-    if (gw >= nw) return;
+    const int all_warps = gridDim.x * WARPS;
+    if (gw >= nw) {
+        zero_empty_sequences(p, D, gw, all_warps, lane);
+        return;
+    }
     WorkStream ws;
     ws.init(p, lane, gw);
-    if (ws.stream_end == 0) return;
+    if (ws.stream_end == 0) {
+        zero_empty_sequences(p, D, gw, all_warps, lane);
+        return;
+    }
     const int units_per_b = ws.units_per_b;
 
     // Issue the copies of stream position j into stage j % STAGES; false past
@@ -173,12 +181,16 @@ decode_kernel(const DecodeParams p) {
 
     int issued = 0;
     while (issued < STAGES && issue(issued)) ++issued;
+    zero_empty_sequences(p, D, gw, all_warps, lane);  // while the first copies are in flight
 
     float qf[GS][8];
     float o[GS][8];
     float m_run = -INFINITY, l_run = 0.f;
     bool seg_whole_start = false;
-    int seg_slot = 0;
+    int seg_slot = 0, seg_first = 0;
+    // split segments to report after the loop (at most two: the range's first and last)
+    int npend = 0;
+    PendingMerge pend0 = {0, 0, 0, 0}, pend1 = {0, 0, 0, 0};
 
     for (int i = 0; i < ws.stream_end; ++i) {
         ws.consumer_at(p, i, STAGES + 1);
@@ -194,7 +206,8 @@ decode_kernel(const DecodeParams p) {
         }
         const bool seg_start = ws.seg_start(i, d);
         if (seg_start) {
-            seg_slot = ws.slot_base(i) + d.u;
+            seg_slot = ws.slot_base + d.u;
+            seg_first = i;
             const T* qs = sq + st * GS * D;
 #pragma unroll
             for (int g = 0; g < GS; ++g) {
@@ -347,6 +360,11 @@ decode_kernel(const DecodeParams p) {
                     dst[GS * D + lane] = pm[lane];
                     dst[GS * D + GS + lane] = pl[lane];
                 }
+                if (p.unit_done) {
+                    const PendingMerge pmg = {d.u, ws.range_f0 + i - d.k, d.nch, i - seg_first + 1};
+                    if (npend == 0) pend0 = pmg; else pend1 = pmg;
+                    ++npend;
+                }
             }
             __syncwarp();
         }
@@ -354,6 +372,9 @@ decode_kernel(const DecodeParams p) {
         // refill: positions up to i + STAGES (stage i % STAGES is free again)
         while (issued <= i + STAGES && issue(issued)) ++issued;
     }
+    // every copy has landed and been consumed: the stage buffers serve the merges
+    if (npend > 0)
+        finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, wsm + Lay::kOffK, lane);
 }
 
 template <int D, int GS>

@@ -31,6 +31,7 @@
 #include <type_traits>
 
 #include "decode.cuh"
+#include "merge.cuh"
 #include "schedule.cuh"
 
 namespace pkv {
@@ -151,10 +152,17 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
 
     const int nw = p.hdr->num_workers;
     const int gw = blockIdx.x * WARPS + warp;
-    if (gw >= nw) return;
+    const int all_warps = gridDim.x * WARPS;
+    if (gw >= nw) {
+        zero_empty_sequences(p, D, gw, all_warps, lane);
+        return;
+    }
     WorkStream ws;
     ws.init(p, lane, gw);
-    if (ws.stream_end == 0) return;
+    if (ws.stream_end == 0) {
+        zero_empty_sequences(p, D, gw, all_warps, lane);
+        return;
+    }
 
     const int units_per_b = ws.units_per_b;
     const int g_lo = lane >> 2;          // query row of c0/c1 (c2/c3: g_lo + 8)
@@ -197,12 +205,16 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
 
     int issued = 0;
     while (issued < STAGES && issue(issued)) ++issued;
+    zero_empty_sequences(p, D, gw, all_warps, lane);  // while the first copies are in flight
 
     uint32_t qa[KSTEPS][4];     // A fragments of Q (rows g_lo, g_lo+8)
     float o[NT][4];             // O accumulators (c0,c1: row g_lo; c2,c3: row g_lo+8)
     float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
     bool seg_whole_start = false;
-    int seg_slot = 0;
+    int seg_slot = 0, seg_first = 0;
+    // split segments to report after the loop (at most two: the range's first and last)
+    int npend = 0;
+    PendingMerge pend0 = {0, 0, 0, 0}, pend1 = {0, 0, 0, 0};
 
     for (int i = 0; i < ws.stream_end; ++i) {
         ws.consumer_at(p, i, STAGES + 1);
@@ -218,7 +230,8 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         }
         const bool seg_start = ws.seg_start(i, d);
         if (seg_start) {
-            seg_slot = ws.slot_base(i) + d.u;
+            seg_slot = ws.slot_base + d.u;
+            seg_first = i;
             // A fragments of Q: a0 (row g, k tq..tq+1), a1 (row g+8), a2 (k+8), a3
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(sq + st * GS * D);
 #pragma unroll
@@ -401,11 +414,19 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                     }
                 }
             }
+            if (!whole && p.unit_done) {
+                const PendingMerge pmg = {d.u, ws.range_f0 + i - d.k, d.nch, i - seg_first + 1};
+                if (npend == 0) pend0 = pmg; else pend1 = pmg;
+                ++npend;
+            }
         }
         __syncwarp();
         // refill: positions up to i + STAGES (stage i % STAGES is free again)
         while (issued <= i + STAGES && issue(issued)) ++issued;
     }
+    // every copy has landed and been consumed: the stage buffers serve the merges
+    if (npend > 0)
+        finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, wsm, lane);
 }
 
 template <int D, int GS>

@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "kernels_aux.cuh"
+#include "merge.cuh"
 
 namespace pkv {
 
@@ -47,6 +48,9 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
     __shared__ int warp_tot[32];
     __shared__ long long running;
     __shared__ uint32_t flags;
+    // the prefix sums also go to shared memory (when they fit) for the searches below
+    __shared__ int32_t s_prefix[kPlanSmemSeqs + 1];
+    const bool prefix_smem = pa.batch <= kPlanSmemSeqs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     if (tid == 0) {
@@ -65,6 +69,8 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
         if (tid == 0) pa.hdr->append_status[blockIdx.x - 1] = flags;
         return;
     }
+    if (pa.unit_done)
+        for (long long x = tid; x < pa.units; x += blockDim.x) pa.unit_done[x] = 0;
     for (int base = 0; base < pa.batch; base += blockDim.x) {
         const int b = base + tid;
         int cnt = 0;
@@ -100,12 +106,15 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
         }
         __syncthreads();
         const int excl = x - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
-        if (b < pa.batch) pa.prefix[b] = (int32_t)(running + excl);
+        if (b < pa.batch) {
+            pa.prefix[b] = (int32_t)(running + excl);
+            if (prefix_smem) s_prefix[b] = (int32_t)(running + excl);
+        }
         __syncthreads();
         if (tid == 0) running += warp_tot[nwarps - 1];
         __syncthreads();
     }
-    __shared__ int s_total, s_nw, s_sw, s_K, s_nt;
+    __shared__ int s_total, s_nw, s_sw, s_r;
     if (tid == 0) {
         long long total = running;
         uint32_t f = flags;
@@ -114,6 +123,7 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
             f |= PKV_DEV_BAD_LEN;
         }
         pa.prefix[pa.batch] = (int32_t)total;
+        if (prefix_smem) s_prefix[pa.batch] = (int32_t)total;
         int nw = 0;
         if (total > 0) {
             if (pa.workers_req > 0) {
@@ -123,155 +133,105 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
                 nw = (int)min((long long)pa.workers_auto, want < 1 ? 1LL : want);
             }
         }
-        // static ranges: static_pct % of the chunks, equal per worker; the rest
-        // in dynamic tiles of K chunks (K grows so that the tiles fit the slots)
-        long long sw = nw > 0 ? (total * pa.static_pct / 100) / nw : 0;
-        // a tile holds at most 32 chunks (one descriptor per lane): when the
-        // tail would need longer tiles, the static ranges grow instead
-        const long long dyn_cap = (long long)kMaxDynTile * pa.dyn_tiles_max;
-        if (nw > 0 && total - sw * nw > dyn_cap) sw = (total - dyn_cap + nw - 1) / nw;
-        // ranges shorter than kMinStaticChunks go dynamic (unless the tail is full)
-        if (sw < kMinStaticChunks) sw = total > dyn_cap ? kMinStaticChunks : 0;
-        const long long ts = sw * nw;
-        const long long dyn = total - ts;
-        long long K = (dyn + pa.dyn_tiles_max - 1) / pa.dyn_tiles_max;
-        if (K < kMinDynTile) K = kMinDynTile;
-        const int nt = dyn > 0 ? (int)((dyn + K - 1) / K) : 0;
+        // contiguous ranges, equal to within one chunk: sw each, one more for
+        // the first r workers
+        const int sw = nw > 0 ? (int)(total / nw) : 0;
+        const int r = nw > 0 ? (int)(total - (long long)sw * nw) : 0;
         pa.hdr->total_chunks = (int32_t)total;
         pa.hdr->num_workers = nw;
-        pa.hdr->static_per_worker = (int32_t)sw;
-        pa.hdr->static_total = (int32_t)ts;
-        pa.hdr->dyn_tile = (int32_t)K;
-        pa.hdr->dyn_tiles = nt;
-        pa.hdr->dyn_next = 0;
+        pa.hdr->chunks_per_worker = sw;
+        pa.hdr->extra_chunks = r;
         pa.hdr->append_slots = append_ctas;
         pa.hdr->status = f;
         s_total = (int)total;
         s_nw = nw;
-        s_sw = (int)sw;
-        s_K = (int)K;
-        s_nt = nt;
+        s_sw = sw;
+        s_r = r;
     }
     __syncthreads();
-    // sequence holding each worker's first static chunk (w * sw; for w = NW the
-    // last static chunk) and each dynamic tile's first chunk (for t = NT the
-    // last chunk), so that a worker searches only the sequences of its piece
-    const int T = s_total, nw = s_nw, sw = s_sw, K = s_K, nt = s_nt;
-    const int ts = sw * nw;
+    // sequence holding each worker's first chunk (for w = NW: the last chunk),
+    // so that a worker searches only the sequences of its range
+    const int T = s_total, nw = s_nw, sw = s_sw, r = s_r;
+    const int32_t* pre = prefix_smem ? s_prefix : pa.prefix;
     auto seq_of = [&](int f) {
         int lo = 0, hi = pa.batch;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (pa.prefix[mid] <= f) lo = mid; else hi = mid;
+            if (pre[mid] <= f) lo = mid; else hi = mid;
         }
         return lo;
     };
     for (int w = tid; w <= nw && T > 0; w += blockDim.x)
-        pa.wstart[w] = sw > 0 ? seq_of(w < nw ? w * sw : ts - 1) : 0;
-    for (int t = tid; t <= nt && T > 0; t += blockDim.x)
-        pa.tile_b[t] = seq_of(t < nt ? ts + t * K : T - 1);
+        pa.wstart[w] = seq_of(w < nw ? range_begin(w, sw, r) : T - 1);
 }
 
 // ---------------------------------------------------------------------------
 // Combine: one CTA per unit (sequence, KV head, sub-group); units finished by
-// a single worker exit at once, empty sequences get zeros.  Partial m is in
-// base-2 units: out = sum_i 2^(m_i-M) o_i / sum_i 2^(m_i-M) l_i, M = max_i m_i.
-// Warp w reduces M and the denominator of heads w, w+8, ... over the splits;
-// then every thread owns 4 consecutive output elements and streams the
-// splits' o.
+// a single worker and empty sequences exit at once.  The unit's partial slots
+// are staged in shared memory merge_batch at a time and folded with
+// merge_weights / merge_accumulate, the same batches and arithmetic the decode
+// kernels' own merge uses.
 // ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 8;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ prefix,
                const int32_t* __restrict__ lens_eff, const WsHeader* __restrict__ hdr,
                T* __restrict__ out, int units_per_b, int sub_groups, int gs, int group,
-               int n_q_heads) {
-    pdl_wait();
-    pdl_trigger();
-    __shared__ float sM[16], sInv[16];  // per query head of the unit (gs <= 16)
+               int n_q_heads, int merge_batch) {
+    extern __shared__ float4 sbuf4[];  // merge_batch staged partial slots
+    // Everything up to pdl_wait reads only what the plan wrote: the plan grid
+    // completed before any decode CTA passed its own wait and let this
+    // kernel launch.  The partial states are read after the wait.
     const int u = blockIdx.x;
     const int b = u / units_per_b;
     const int uidx = u - b * units_per_b;
     const int h = uidx / sub_groups;
-    const int sg = uidx - h * sub_groups;
-    T* o = out + ((long long)b * n_q_heads + h * group + sg * gs) * D;
+    const int sgi = uidx - h * sub_groups;
+    T* o = out + ((long long)b * n_q_heads + h * group + sgi * gs) * D;
     const int L = lens_eff[b];
     const int nch = (L + kChunk - 1) / kChunk;
-    const int n = gs * D;
     const int tid = threadIdx.x;
-    if (nch == 0) {
-        for (int idx = tid; idx < n; idx += blockDim.x) o[idx] = T(0.f);
-        return;
-    }
-    const int total = hdr->total_chunks;
-    const int nw = hdr->num_workers;
-    if (total <= 0 || nw <= 0) return;
-    // segments of unit u: one per worker whose static range meets its chunks
-    // [a, e), one per dynamic tile that does (schedule.cuh)
-    const int sw = hdr->static_per_worker, ts = hdr->static_total, K = hdr->dyn_tile;
-    const int a = prefix[b] + uidx * nch;
-    const int e = a + nch;
-    int s_first = 0, s_count = 0, t_first = 0, t_count = 0;
-    if (a < ts) {
-        s_first = a / sw;
-        s_count = (min(e, ts) - 1) / sw - s_first + 1;
-    }
-    if (e > ts) {
-        t_first = (max(a, ts) - ts) / K;
-        t_count = (e - 1 - ts) / K - t_first + 1;
-    }
-    const int ns = s_count + t_count;
+    if (nch == 0) return;  // the decode kernel zeroed the rows of empty sequences
+    if (hdr->total_chunks <= 0 || hdr->num_workers <= 0) return;
+    const UnitSegments segs =
+        unit_segments(hdr->chunks_per_worker, hdr->extra_chunks, u, prefix[b] + uidx * nch, nch);
+    const int ns = segs.count();
     if (ns <= 1) return;  // finished in place by its worker
-    const int units = gridDim.x;
-    const long long stride = partial_slot_floats(gs, D);
-    // slot of the s-th segment: static u + w, dynamic U + NW + u + t
-    auto slot_of = [&](int s) -> long long {
-        return s < s_count ? (long long)(u + s_first + s)
-                           : (long long)units + nw + u + t_first + (s - s_count);
-    };
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int g = warp; g < gs; g += (int)(blockDim.x >> 5)) {
-        float M = -INFINITY;
-        for (int s = lane; s < ns; s += 32) M = fmaxf(M, partials[slot_of(s) * stride + n + g]);
+    pdl_wait();
+    pdl_trigger();
+    const int stride = partial_slot_floats(gs, D);
+    constexpr int Q = D / 4;
+    constexpr int KPT = (16 * Q + kCombineWarps * 32 - 1) / (kCombineWarps * 32);
+    float* slots = reinterpret_cast<float*>(sbuf4);
+    MergeHead* heads = reinterpret_cast<MergeHead*>(slots + merge_batch * stride);
+    if (tid < gs) heads[tid] = MergeHead{-INFINITY, 0.f, 0.f, 0.f};
+    float4 acc[KPT];
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, m));
-        float S = 0.f;
-        if (M != -INFINITY) {
-            for (int s = lane; s < ns; s += 32) {
-                const float* pp = partials + slot_of(s) * stride;
-                S += exp2f(pp[n + g] - M) * pp[n + gs + g];
-            }
+    for (int k = 0; k < KPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int vps = stride / 4;  // 16-byte vectors per slot
+    for (int s0 = 0; s0 < ns; s0 += merge_batch) {
+        const int cnt = min(merge_batch, ns - s0);
+        __syncthreads();
+        for (int v = tid; v < cnt * vps; v += blockDim.x) {
+            const int s = v / vps;
+            sbuf4[v] = __ldcg(reinterpret_cast<const float4*>(partials + segs.slot(s0 + s) * stride) +
+                              (v - s * vps));
         }
+        __syncthreads();
+        if (tid < 32) merge_weights(slots, stride, cnt, gs, D, heads, tid);
+        __syncthreads();
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) S += __shfl_xor_sync(kFull, S, m);
-        if (lane == 0) {
-            sM[g] = M;
-            sInv[g] = S > 0.f ? 1.0f / S : 0.f;
+        for (int k = 0; k < KPT; ++k) {
+            const int it = k * blockDim.x + tid;
+            if (it < gs * Q) merge_accumulate<D>(slots, stride, cnt, gs, heads, it / Q, it % Q, acc[k]);
         }
     }
-    __syncthreads();
-    constexpr int Q = D / 4;
-    for (int it = tid; it < gs * Q; it += blockDim.x) {
-        const int g = it / Q, d4 = it - g * Q;
-        const float M = sM[g];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll 4
-            for (int s = 0; s < ns; ++s) {
-                const float* pp = partials + slot_of(s) * stride;
-                const float w = exp2f(pp[n + g] - M);
-                const float4 v = *reinterpret_cast<const float4*>(pp + g * D + d4 * 4);
-                acc.x = fmaf(w, v.x, acc.x);
-                acc.y = fmaf(w, v.y, acc.y);
-                acc.z = fmaf(w, v.z, acc.z);
-                acc.w = fmaf(w, v.w, acc.w);
-            }
-        }
-        const float inv = sInv[g];
-        uint2 w2;
-        w2.x = Cvt<T>::pack2(acc.x * inv, acc.y * inv);
-        w2.y = Cvt<T>::pack2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(o + g * D + d4 * 4) = w2;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const int it = k * blockDim.x + tid;
+        if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o);
     }
 }
 
@@ -340,12 +300,13 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           int group, int n_q_heads, cudaStream_t stream) {
+                           int group, int n_q_heads, int merge_batch, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
 #define PKV_COMBINE(T, D)                                                                     \
-    return launch_pdl(combine_kernel<T, D>, dim3(units), dim3(256), 0, stream, partials,      \
+    return launch_pdl(combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32),           \
+                      (size_t)merge_smem_bytes(merge_batch, gs, D), stream, partials,         \
                       prefix, lens_eff, hdr, static_cast<T*>(out), units_per_b, sub_groups,   \
-                      gs, group, n_q_heads)
+                      gs, group, n_q_heads, merge_batch)
     if (dtype == PKV_BF16) {
         if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128);
         PKV_COMBINE(__nv_bfloat16, 64);

@@ -19,11 +19,10 @@ struct PlanArgs {
     int min_chunks;        // automatic mode: at least this many chunks per worker
     int32_t* lens_eff;     // [B] clamped lengths (workspace)
     int32_t* prefix;       // [B+1] chunk prefix sums (workspace)
-    int32_t* wstart;       // [workers+1] sequence of each worker's first static chunk
-    int32_t* tile_b;       // [dyn_tiles_max+1] sequence of each dynamic tile's first chunk
-    int static_pct;        // share of the chunks given out as static ranges (percent)
-    int dyn_tiles_max;     // upper bound on the dynamic tiles (workspace slots)
+    int32_t* wstart;       // [workers+1] sequence of each worker's first chunk
     WsHeader* hdr;
+    int32_t* unit_done;    // [units] merge counters of the decode kernel (nullable), zeroed
+    long long units;
     const int32_t* table;  // page table (nullable), prefetched into L2 for the decode kernel
     int table_stride;
     int page_size;
@@ -46,13 +45,10 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           int group, int n_q_heads, cudaStream_t stream);
+                           int group, int n_q_heads, int merge_batch, cudaStream_t stream);
 
-// smallest static range worth giving a worker (shorter ranges become dynamic)
-constexpr int kMinStaticChunks = 4;
-// chunks per dynamic tile: at least the decode kernels' stages, at most one per lane
-constexpr int kMinDynTile = 4;
-constexpr int kMaxDynTile = 32;
+// batches up to this size keep their chunk prefix sums in the plan's shared memory
+constexpr int kPlanSmemSeqs = 8192;
 
 cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status, cudaStream_t stream);
 

@@ -1,25 +1,23 @@
 // schedule.cuh -- which 16-token chunks each decode worker (one warp) handles.
 //
 // All chunks of the batch are laid end to end: sequence-major, then KV head
-// (and query sub-group), then chunk.  The first part of that order is split
-// into equal contiguous static ranges, one per worker; the rest is cut into
-// small dynamic tiles that workers take from a shared counter once their
-// static range is done.  Static ranges keep the partial states few (a unit
-// that lies inside one range is finished in place); the dynamic tail evens
-// out the finishing times, which otherwise spread by ~20% because some SMs
-// get less memory bandwidth than others.
+// (and query sub-group), then chunk.  That order is cut into one contiguous
+// range per worker, as equal as possible: with T chunks and NW workers,
+// sw = T / NW and r = T % NW, workers 0 .. r-1 take sw + 1 chunks and the
+// others sw.  Every warp gets the same work to within one chunk, whatever the
+// length mix, and a unit (sequence, KV head, sub-group) that lies inside one
+// range is finished in place.
 //
-// A worker consumes its chunks as one stream: static tiles (its range cut into
-// pieces of at most 32 chunks, one descriptor per lane), then dynamic tiles.
-// Two tiles are live at a time -- the consumer's and the next one -- and the
-// producer (lane 0 issuing the copies) runs at most STAGES chunks ahead, so
-// every tile but the very last is at least STAGES chunks long.
+// A worker consumes its range as a stream of tiles of at most 32 chunks (one
+// descriptor per lane, as equal as possible).  Two tiles are live at a time --
+// the consumer's and the next one -- and the producer (lane 0 issuing the
+// copies) runs at most STAGES chunks ahead.
 //
-// Partial-state slots: a segment (the chunks of one unit processed by one
-// worker in one piece) of unit u in worker w's static range uses slot u + w;
-// one in dynamic tile t uses slot U + NW + u + t (U units, NW workers).  Along
-// either region the (u, w) or (u, t) pairs of consecutive segments grow
-// monotonically, so these slots never collide.
+// Partial-state slots: the segment (chunks of one unit in one worker's range)
+// of unit u in worker w's range uses slot u + w.  Along the order the (u, w)
+// pairs of consecutive segments grow monotonically, so slots never collide;
+// there are at most U + NW of them.  A range holds at most two segments that
+// are not a whole unit: its first and its last.
 #pragma once
 
 #include "common.cuh"
@@ -91,59 +89,33 @@ __device__ __forceinline__ ChunkDesc sel_desc(bool second, const ChunkDesc& a,
 // lanes (they shuffle).
 struct WorkStream {
     // the live tiles: a = the consumer's, b = the next one (len 0: none yet)
-    int a_start, a_len, a_slot, a_contig;
-    int b_start, b_len, b_slot, b_contig;
+    int a_start, a_len;
+    int b_start, b_len;
     ChunkDesc wa, wb;
-    int stream_end;   // first position past the last chunk (INT_MAX while unknown)
-    bool exhausted;   // no tile left to take
-    // static range of this worker
-    int s_next, s_end, s_tiles_left, s_piece, s_extra;
-    int b_lo_static, b_hi_static;
-    int lane, gw, units_per_b;
+    int stream_end;   // chunks in this worker's range
+    // the rest of the range: next chunk, tiles left, base tile length, longer tiles
+    int next_f, tiles_left, piece, extra;
+    int b_lo, b_hi;   // sequences of the range: [b_lo, b_hi)
+    int lane, gw, units_per_b, slot_base;
+    int range_f0, sw, r;  // first chunk of the range; the split (chunks_per_worker, extra)
 
     __device__ __forceinline__ int a_end() const { return a_start + a_len; }
 
-    // Fill tile b (the one after tile a): the next static piece, else a
-    // dynamic tile from the shared counter, else mark the stream exhausted.
+    // Fill tile b (the one after tile a) with the next piece of the range.
     __device__ __forceinline__ void acquire(const DecodeParams& p) {
-        const int start = a_start + a_len;
-        int f, len, slot, contig, lo, hi;
-        if (s_tiles_left > 0) {
-            len = s_piece + (s_extra > 0 ? 1 : 0);
-            s_extra -= (s_extra > 0);
-            --s_tiles_left;
-            f = s_next;
-            s_next += len;
-            slot = gw;          // static segment of unit u: slot u + w
-            contig = (start > 0);
-            lo = b_lo_static;
-            hi = b_hi_static;
-        } else {
-            int t = 0;
-            if (lane == 0) t = atomicAdd(p.dyn_next, 1);
-            t = __shfl_sync(kFull, t, 0);
-            if (t >= p.hdr->dyn_tiles) {
-                exhausted = true;
-                stream_end = start;
-                b_len = 0;
-                return;
-            }
-            const int ts = p.hdr->static_total, K = p.hdr->dyn_tile;
-            f = ts + t * K;
-            len = min(K, p.hdr->total_chunks - f);
-            slot = p.units + p.hdr->num_workers + t;  // dynamic segment: slot U + NW + u + t
-            contig = 0;
-            lo = __ldg(p.tile_b + t);
-            hi = min(p.batch, __ldg(p.tile_b + t + 1) + 1);
-        }
-        b_start = start;
+        b_start = a_start + a_len;
+        b_len = 0;
+        if (tiles_left == 0) return;
+        const int len = piece + (extra > 0 ? 1 : 0);
+        extra -= (extra > 0);
+        --tiles_left;
+        const int f = next_f;
+        next_f += len;
         b_len = len;
-        b_slot = slot;
-        b_contig = contig;
         wb.off = -1;
         wb.u = wb.k = wb.nvalid = 0;
         wb.nch = 1;
-        if (lane < len) wb = describe_chunk(p, f + lane, units_per_b, lo, hi);
+        if (lane < len) wb = describe_chunk(p, f + lane, units_per_b, b_lo, b_hi);
     }
 
     // Set up the worker's stream; afterwards tile a is its first tile (if any).
@@ -151,29 +123,27 @@ struct WorkStream {
         lane = lane_;
         gw = gw_;
         units_per_b = p.n_kv_heads * p.sub_groups;
-        stream_end = 0x7fffffff;
-        exhausted = false;
-        const int sw = p.hdr->static_per_worker;
-        s_next = gw * sw;
-        s_end = s_next + sw;
-        // cut the static range into pieces of at most 32 chunks, as equal as possible
-        s_tiles_left = (sw + 31) / 32;
-        s_piece = s_tiles_left ? sw / s_tiles_left : 0;
-        s_extra = s_tiles_left ? sw - s_piece * s_tiles_left : 0;
-        b_lo_static = __ldg(p.wstart + gw);
-        b_hi_static = min(p.batch, __ldg(p.wstart + gw + 1) + 1);
+        slot_base = gw;  // segment of unit u in this range: slot u + w
+        sw = p.hdr->chunks_per_worker;
+        r = p.hdr->extra_chunks;
+        range_f0 = range_begin(gw, sw, r);
+        next_f = range_f0;
+        stream_end = sw + (gw < r ? 1 : 0);
+        // cut the range into tiles of at most 32 chunks, as equal as possible
+        tiles_left = (stream_end + 31) / 32;
+        piece = tiles_left ? stream_end / tiles_left : 0;
+        extra = tiles_left ? stream_end - piece * tiles_left : 0;
+        b_lo = __ldg(p.wstart + gw);
+        b_hi = min(p.batch, __ldg(p.wstart + gw + 1) + 1);
         a_start = 0;
         a_len = 0;
         acquire(p);  // first tile into b, then promote it
         promote();
-        if (a_len == 0) stream_end = 0;
     }
 
     __device__ __forceinline__ void promote() {
         a_start = b_start;
         a_len = b_len;
-        a_slot = b_slot;
-        a_contig = b_contig;
         wa = wb;
         b_len = 0;
         b_start = a_start + a_len;
@@ -184,7 +154,7 @@ struct WorkStream {
     // producer never waits for it.
     __device__ __forceinline__ void consumer_at(const DecodeParams& p, int i, int lookahead) {
         if (i >= a_end() && b_len > 0) promote();
-        if (b_len == 0 && !exhausted && i + lookahead >= a_end()) acquire(p);
+        if (b_len == 0 && tiles_left > 0 && i + lookahead >= a_end()) acquire(p);
     }
 
     // Producer side: is position j covered by a live tile?  Takes the next
@@ -192,7 +162,8 @@ struct WorkStream {
     // (the producer retries after the consumer moved on) or past the end.
     __device__ __forceinline__ bool covered(const DecodeParams& p, int j) {
         if (j < a_end()) return true;
-        if (b_len == 0 && !exhausted) acquire(p);
+        if (j >= stream_end) return false;
+        if (b_len == 0 && tiles_left > 0) acquire(p);
         return b_len > 0 && j < b_start + b_len;
     }
 
@@ -202,20 +173,14 @@ struct WorkStream {
         return shfl_desc(src, j - (second ? b_start : a_start));
     }
 
-    // Partial slot base of position j's tile (slot = base + unit).
-    __device__ __forceinline__ int slot_base(int j) const { return j >= a_end() ? b_slot : a_slot; }
-
-    // Does position j (in tile a or b) start a segment?  Does i (in tile a) end one?
+    // Does position j start a segment (a unit's first chunk, or the range's
+    // first)?  Does position i end one (a unit's last chunk, or the range's
+    // last)?
     __device__ __forceinline__ bool seg_start(int j, const ChunkDesc& d) const {
-        if (d.k == 0) return true;
-        if (j == a_start) return !a_contig;
-        if (b_len > 0 && j == b_start) return !b_contig;
-        return false;
+        return d.k == 0 || j == 0;
     }
     __device__ __forceinline__ bool seg_end(int i, const ChunkDesc& d) const {
-        if (d.k == d.nch - 1 || i + 1 >= stream_end) return true;
-        if (i + 1 == a_end()) return !(b_len > 0 && b_contig);
-        return false;
+        return d.k == d.nch - 1 || i + 1 >= stream_end;
     }
 };
 

@@ -264,20 +264,45 @@ def test_workspace_too_small_is_rejected():
     assert e.value.name == "PKV_ERR_WORKSPACE"
 
 
-def test_split_steps_equal_fused_call():
-    """plan + run + combine called one by one == paged_decode_attention."""
-    w = wl.make("llama3_8b", seed=4, device="cuda", batch=8)
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("case", ["llama3_8b", "mixed_append", "with_empty", "long_split"])
+def test_split_steps_equal_fused_call(case, variant):
+    """plan + run (merge in the decode kernel) and plan + run + combine, called
+    one by one, both equal paged_decode_attention bit for bit; rows of empty
+    sequences are zeros either way."""
+    if case == "with_empty":
+        w = wl.make_random(21, batch=7, n_q_heads=16, n_kv_heads=4, head_dim=128, page_size=16,
+                           dtype=torch.bfloat16, lens=[0, 3000, 0, 17, 900, 0, 4500],
+                           device="cuda")
+    elif case == "long_split":  # one unit over many workers: several merge batches
+        w = wl.make_random(22, batch=1, n_q_heads=16, n_kv_heads=1, head_dim=128, page_size=16,
+                           dtype=torch.bfloat16, lens=[60000], device="cuda")
+    else:
+        w = wl.make(case, seed=4, device="cuda", batch=8 if case == "llama3_8b" else 40)
     table, lens, _ = to_dev(w)
-    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim)
-    a = torch.empty_like(w.q)
-    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, a, ws)
-    b = torch.empty_like(w.q)
-    pkv.paged_decode_plan(lens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size,
-                          table.shape[1], ws)
-    pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, b, ws)
-    pkv.paged_decode_combine(b, w.n_kv_heads, ws)
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, variant=variant)
+    a = torch.full_like(w.q, float("nan"))
+    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, a, ws,
+                               variant=variant)
+    outs = []
+    for merge in (True, False):
+        b = torch.full_like(w.q, float("nan"))
+        pkv.paged_decode_plan(lens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size,
+                              table.shape[1], ws, variant=variant)
+        pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, b, ws, variant=variant,
+                             merge=merge)
+        if not merge:
+            pkv.paged_decode_combine(b, w.n_kv_heads, ws, variant=variant)
+        outs.append(b)
     torch.cuda.synchronize()
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for b in outs:
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    empty = torch.from_numpy(np.asarray(w.context_lens) == 0)
+    if empty.any():
+        assert torch.count_nonzero(a[empty.cuda()].float()) == 0
+    assert pkv.pkv_read_device_status(ws) == 0
+    if case == "long_split":
+        assert_close(a, oracle_full(w), what="one sequence over many workers")
 
 
 def test_pool_owned_memory_roundtrip():
