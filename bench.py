@@ -264,7 +264,8 @@ def run_reference(args):
                                   w.positions)
         w.k_pool = torch.from_numpy(kp.view("int16")).view(w.dtype)
         w.v_pool = torch.from_numpy(vp.view("int16")).view(w.dtype)
-    budget = max(0.05, min(12.0, 150.0 / max(1, args.steps + args.warmup)))
+    # about 150 s in all: each step samples at least one sequence (a few ms)
+    budget = min(12.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_oracle_sample(w, target_s=budget)
     vals, seqs = [], []
