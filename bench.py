@@ -82,6 +82,22 @@ def dist_info():
     return ws, rank, local
 
 
+def max_over_ranks(dist, x: float, device) -> float:
+    """The largest of the ranks' values: a replicated job takes as long as its
+    slowest rank.  dist is None on one process."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world: int, bytes_per_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -380,10 +396,7 @@ def run_ours(args):
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
     ms_step = total_ms / K
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(dist, ms_step, dev)
     clocks = sampler.finish()
 
     # ---- the decode kernel alone: events around its launch on its stream ----
@@ -427,13 +440,10 @@ def run_ours(args):
     for _ in range(KE):
         e2e_step()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / KE
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(dist, e2e_ms, dev)
     status = pkv.pkv_read_device_status(ws)
 
-    value = world * by["step"] / (ms_step * 1e-3) / 1e9
+    value = aggregate_gbs(world, by["step"], ms_step)
     achieved = by["decode"] / (dec_avg * 1e-3) / 1e9
     traffic = traffic_from_profile()
     line = {
@@ -467,7 +477,7 @@ def run_ours(args):
                      "algorithmic_bytes": by["decode"],
                      "timing": f"CUDA events around paged_decode_run on its stream, mean of "
                                f"{KD} steps run right after the timed region"},
-        "e2e": {"value": world * by["step"] / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+        "e2e": {"value": aggregate_gbs(world, by["step"], e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": KE},
         "gpu_launches": 3 * K,
