@@ -113,27 +113,37 @@ def _check(code: int, where: str):
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # ctypes converts a plain int for a c_void_p argument
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
-    if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{name} must be a torch tensor")
+    """A contiguous CUDA tensor (of dtype / ndim when given), else raise."""
+    try:
+        ok = (t.is_cuda and t.is_contiguous() and (dtype is None or t.dtype == dtype)
+              and (ndim is None or t.dim() == ndim))
+    except AttributeError:
+        raise TypeError(f"{name} must be a torch tensor") from None
+    if ok:
+        return t
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if ndim is not None and t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
-    return t
+    raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
 def _dtype_code(t: torch.Tensor) -> int:

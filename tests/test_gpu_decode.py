@@ -359,3 +359,45 @@ def test_fused_step_reports_bad_append_and_skips_padding():
                           w.v_pool, table, lens, w.scale, out, ws)
     torch.cuda.synchronize()
     assert pkv.pkv_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_step_captured_in_cuda_graph_equals_eager(variant):
+    """paged_decode_step recorded into a CUDA graph (input copy, the three
+    launches, output copy) and replayed twice gives the eager call's bits, and
+    the replays pick up new inputs written into the same buffers."""
+    w = wl.make("mixed_append", seed=8, device="cuda", batch=24)
+    table, lens, pos = to_dev(w)
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, variant=variant)
+    k0, v0 = w.k_pool.clone(), w.v_pool.clone()
+    q_in = w.q.clone()
+    eager = torch.empty_like(w.q)
+    pkv.paged_decode_step(w.k_new, w.v_new, pos, q_in, w.k_pool, w.v_pool, table, lens, w.scale,
+                          eager, ws, variant=variant)
+    torch.cuda.synchronize()
+    w.k_pool.copy_(k0)
+    w.v_pool.copy_(v0)
+    out = torch.full_like(w.q, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pkv.paged_decode_step(w.k_new, w.v_new, pos, q_in, w.k_pool, w.v_pool, table, lens,
+                                  w.scale, out, ws, variant=variant)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    # new queries in the same buffer: the replay must see them
+    q_in.mul_(-1.0)
+    g.replay()
+    torch.cuda.synchronize()
+    ref = torch.empty_like(w.q)
+    pkv.paged_decode_attention(q_in, w.k_pool, w.v_pool, table, lens, w.scale, ref,
+                               pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads,
+                                                   w.head_dim, variant=variant),
+                               variant=variant)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert pkv.pkv_read_device_status(ws) == 0
