@@ -77,6 +77,10 @@ class Oracle:
         lib.pkv_oracle_kv_append.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32]
         lib.pkv_oracle_gather.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, i32, P]
         lib.pkv_oracle_set_threads.argtypes = [i32]
+        lib.pkv_oracle_encode_array.argtypes = [P, ctypes.c_int64, i32, P]
+        lib.pkv_oracle_rope.argtypes = [P, P, i32, i32, i32, ctypes.c_double, i32, P, P]
+        for name in ("pkv_oracle_encode_array", "pkv_oracle_rope"):
+            getattr(lib, name).restype = ctypes.c_int
         for name in ("pkv_oracle_decode_array", "pkv_oracle_paged_decode",
                      "pkv_oracle_paged_decode_rows", "pkv_oracle_kv_append",
                      "pkv_oracle_gather", "pkv_oracle_set_threads", "pkv_oracle_max_threads"):
@@ -135,6 +139,28 @@ class Oracle:
                                                    _ptr(rows), rows.shape[0], _ptr(out))
         _check(rc, "paged_decode_rows")
         return out
+
+    def encode(self, values, dtype: str) -> np.ndarray:
+        """Round float64 values to 16-bit patterns (to nearest, ties to even)."""
+        x = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(x.shape, dtype=np.uint16)
+        _check(self.lib.pkv_oracle_encode_array(_ptr(x), x.size, DTYPES[dtype], _ptr(out)),
+               "encode")
+        return out
+
+    def rope(self, x, positions, theta: float, dtype: str, with_f64: bool = False):
+        """Rotary embedding of rows x [B, H, D] (16-bit patterns) at positions[b].
+
+        Returns the rotated rows as 16-bit patterns, plus the float64 values
+        before rounding when with_f64."""
+        xb = _u16(x)
+        pos = _i32(positions)
+        B, H, D = xb.shape
+        out = np.empty(xb.shape, dtype=np.uint16)
+        f64 = np.empty(xb.shape, dtype=np.float64) if with_f64 else None
+        _check(self.lib.pkv_oracle_rope(_ptr(xb), _ptr(pos), B, H, D, float(theta), DTYPES[dtype],
+                                        _ptr(out), _ptr(f64) if with_f64 else None), "rope")
+        return (out, f64) if with_f64 else out
 
     def kv_append(self, k_pool, v_pool, k_new, v_new, page_table, positions):
         """Return copies of (k_pool, v_pool) with the new rows written in.
@@ -198,6 +224,14 @@ def paged_decode_rows(*a, **k) -> np.ndarray:
 
 def kv_append(*a, **k):
     return get().kv_append(*a, **k)
+
+
+def encode(*a, **k) -> np.ndarray:
+    return get().encode(*a, **k)
+
+
+def rope(*a, **k):
+    return get().rope(*a, **k)
 
 
 def gather(*a, **k) -> np.ndarray:

@@ -45,6 +45,19 @@
  *  by reading through the page table (TorchInferno, "Runtime Scaffolds",
  *  runtime.paged materialization).  Bit copy.
  *
+ *  Rotary position embedding before the append (CacheIR, "Compiler Example":
+ *  rope(q, k) produces the q and k that attention consumes; "Complete Tech
+ *  Stack": Llama/Mistral/Qwen-style blocks with RoPE; TorchInferno,
+ *  "OpenAI-Compatible Serving" knob list: a fused decode rotary + KV append
+ *  kernel).  The pages print no formula.  The plain reading, used here, is the
+ *  rotary embedding of those model families with the rotate-half pairing:
+ *  element i of the first half of a head pairs with element i + D/2, and the
+ *  pair is turned by the angle pos * theta^(-2i/D), i = 0 .. D/2-1:
+ *      y_i       = x_i cos(a_i) - x_{i+D/2} sin(a_i)
+ *      y_{i+D/2} = x_{i+D/2} cos(a_i) + x_i sin(a_i)
+ *  with theta given by the caller and pos the token's position.  The rotated
+ *  row is rounded to the storage format (round to nearest, ties to even).
+ *
  * Precision: every product, sum and exp is in IEEE double.  fp16 / bf16 inputs
  * are decoded from their sign / exponent / fraction fields (IEEE 754 binary16,
  * and bfloat16 = the upper half of binary32), which is exact in double.
@@ -90,6 +103,84 @@ static double decode_fields(uint16_t bits, int ebits, int mbits) {
 
 double pkv_oracle_decode_bits(uint16_t bits, int dtype) {
     return dtype == ORC_BF16 ? decode_fields(bits, 8, 7) : decode_fields(bits, 5, 10);
+}
+
+/* Encode x as a 16-bit float with ebits exponent and mbits fraction bits,
+ * rounding to nearest with ties to even (IEEE 754 roundTiesToEven): find the
+ * binade of |x|, express |x| in units of that binade's spacing (exact: a power
+ * of two scale), round that to an integer, and carry into the exponent when
+ * the rounding reaches the next binade.  Below the normal range the spacing is
+ * that of the subnormals; beyond the largest finite value the result is inf.
+ * NaN gives the quiet NaN with the sign kept. */
+static uint16_t encode_fields(double x, int ebits, int mbits) {
+    const uint16_t sign = signbit(x) ? (uint16_t)(1u << (ebits + mbits)) : 0;
+    const int bias = (1 << (ebits - 1)) - 1;
+    const uint16_t exp_all = (uint16_t)(((1u << ebits) - 1) << mbits);
+    if (isnan(x)) return (uint16_t)(sign | exp_all | (1u << (mbits - 1)));
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | exp_all);
+    if (a == 0.0) return sign;
+    int e2;
+    (void)frexp(a, &e2);          /* a = m * 2^e2, m in [0.5, 1) */
+    int e = e2 - 1;               /* a in [2^e, 2^(e+1)) */
+    const int emin = 1 - bias;
+    if (e < emin) {               /* subnormal: spacing 2^(emin - mbits) */
+        const double r = nearbyint(ldexp(a, mbits - emin));
+        /* r = 2^mbits lands on the smallest normal: the same bit pattern */
+        return (uint16_t)(sign | (uint16_t)r);
+    }
+    double r = nearbyint(ldexp(a, mbits - e));   /* in [2^mbits, 2^(mbits+1)] */
+    if (r == ldexp(1.0, mbits + 1)) {
+        r = ldexp(1.0, mbits);
+        e += 1;
+    }
+    if (e > bias) return (uint16_t)(sign | exp_all);  /* beyond the largest finite value */
+    return (uint16_t)(sign | ((uint16_t)(e + bias) << mbits) | (uint16_t)(r - ldexp(1.0, mbits)));
+}
+
+static uint16_t encode_dtype(double x, int dtype) {
+    return dtype == ORC_F16 ? encode_fields(x, 5, 10) : encode_fields(x, 8, 7);
+}
+
+/* Encode n doubles (used by the tests to pin the encoder). */
+int pkv_oracle_encode_array(const double* x, int64_t n, int dtype, uint16_t* out) {
+    if (!x || !out || n < 0 || (dtype != ORC_F16 && dtype != ORC_BF16)) return ORC_INVALID;
+    for (int64_t i = 0; i < n; ++i) out[i] = encode_dtype(x[i], dtype);
+    return ORC_OK;
+}
+
+/*
+ * Rotary embedding of rows x [batch][heads][head_dim] at positions[b] (every
+ * head of sequence b turns by the same angles), theta > 0, head_dim even.
+ * out: the rotated rows rounded to dtype; out_f64 (nullable): the same rows
+ * before rounding.
+ */
+int pkv_oracle_rope(const uint16_t* x, const int32_t* positions, int batch, int heads,
+                    int head_dim, double theta, int dtype, uint16_t* out, double* out_f64) {
+    if (!x || !positions || !out || batch < 0 || heads <= 0 || head_dim <= 0 ||
+        head_dim % 2 || !(theta > 0.0) || (dtype != ORC_F16 && dtype != ORC_BF16))
+        return ORC_INVALID;
+    const int half = head_dim / 2;
+    for (int b = 0; b < batch; ++b) {
+        for (int h = 0; h < heads; ++h) {
+            const int64_t row = ((int64_t)b * heads + h) * head_dim;
+            for (int i = 0; i < half; ++i) {
+                const double ang = (double)positions[b] * pow(theta, -2.0 * i / head_dim);
+                const double c = cos(ang), sn = sin(ang);
+                const double x0 = pkv_oracle_decode_bits(x[row + i], dtype);
+                const double x1 = pkv_oracle_decode_bits(x[row + half + i], dtype);
+                const double y0 = x0 * c - x1 * sn;
+                const double y1 = x1 * c + x0 * sn;
+                if (out_f64) {
+                    out_f64[row + i] = y0;
+                    out_f64[row + half + i] = y1;
+                }
+                out[row + i] = encode_dtype(y0, dtype);
+                out[row + half + i] = encode_dtype(y1, dtype);
+            }
+        }
+    }
+    return ORC_OK;
 }
 
 /* Decode n elements (used by the tests to pin the decoder). */

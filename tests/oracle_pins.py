@@ -344,6 +344,99 @@ def check_empty_context_and_errors(orc):
         raise AssertionError("append beyond the row accepted")
 
 
+
+
+# ---- rotary embedding and rounding (the fused rotary + append path) ----
+
+def check_encode_round_trips_and_matches_libraries(orc):
+    """Rounding float64 to fp16 / bf16: every finite pattern survives a
+    decode-encode round trip; random values round as numpy (fp16, from
+    float64) and torch (bf16, from values exact in float32) round them; ties
+    go to the even neighbour; overflow gives inf."""
+    rng = np.random.default_rng(11)
+    for dt in ("f16", "bf16"):
+        allb = np.arange(65536, dtype=np.uint16)
+        vals = orc.decode_bits(allb, dt)
+        back = orc.encode(vals, dt)
+        fin = np.isfinite(vals)
+        assert np.array_equal(back[fin], allb[fin]), dt
+        assert np.all(np.isnan(orc.decode_bits(back[np.isnan(vals)], dt)))
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-20, 12, 20000))
+    assert np.array_equal(orc.encode(x, "f16"), x.astype(np.float16).view(np.uint16))
+    x32 = (rng.standard_normal(20000) * np.exp(rng.uniform(-40, 40, 20000))).astype(np.float32)
+    ref = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.encode(x32.astype(np.float64), "bf16"), ref)
+    # halfway between 1 and the next fp16 (1 + 2^-10): ties to the even one, 1
+    assert orc.encode([1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11], "f16").tolist() == [0x3C00, 0x3C02]
+    assert orc.encode([70000.0, -1e300], "f16").tolist() == [0x7C00, 0xFC00]
+
+
+def check_rope_position_zero_is_identity(orc):
+    rng = np.random.default_rng(12)
+    for dt in ("f16", "bf16"):
+        x = _rand_bits(rng, (3, 5, 64), dt)
+        assert np.array_equal(orc.rope(x, [0, 0, 0], 10000.0, dt), x)
+
+
+def check_rope_one_hot_closed_form(orc):
+    """Unit vectors show the pairing (element i with i + D/2) and the angle
+    pos * theta^(-2i/D): for D = 4, theta = 100, pair 0 turns by pos and pair 1
+    by pos / 10."""
+    one = {"f16": 0x3C00, "bf16": 0x3F80}
+    for dt in ("f16", "bf16"):
+        x = np.zeros((2, 2, 4), dtype=np.uint16)
+        x[:, 0, 0] = one[dt]  # e_0
+        x[:, 1, 1] = one[dt]  # e_1
+        _, y = orc.rope(x, [1, 7], 100.0, dt, with_f64=True)
+        for b, pos in enumerate((1, 7)):
+            assert np.allclose(y[b, 0], [math.cos(pos), 0, math.sin(pos), 0], atol=1e-15)
+            assert np.allclose(y[b, 1], [0, math.cos(pos / 10), 0, math.sin(pos / 10)],
+                               atol=1e-15)
+
+
+def check_rope_is_a_rotation(orc):
+    """Each (i, i + D/2) pair keeps its length; turning by a then by b equals
+    turning by a + b; and q.k after rotation depends only on the distance of
+    the two positions (the defining property of rotary embeddings)."""
+    rng = np.random.default_rng(13)
+    dt, D, theta = "bf16", 64, 10000.0
+    x = _rand_bits(rng, (4, 3, D), dt)
+    xv = orc.decode_bits(x, dt)
+    pos = np.array([5, 100, 2047, 32767], dtype=np.int32)
+    _, y = orc.rope(x, pos, theta, dt, with_f64=True)
+    h = D // 2
+    assert np.allclose(y[..., :h] ** 2 + y[..., h:] ** 2, xv[..., :h] ** 2 + xv[..., h:] ** 2,
+                       rtol=1e-12, atol=1e-12)
+    # turn the float64 result for position a further by b and compare with a + b
+    a, b = 37, 1000
+    _, ya = orc.rope(x, np.full(4, a, np.int32), theta, dt, with_f64=True)
+    _, yab = orc.rope(x, np.full(4, a + b, np.int32), theta, dt, with_f64=True)
+    inv = theta ** (-2.0 * np.arange(h) / D)
+    c, s_ = np.cos(b * inv), np.sin(b * inv)
+    again = np.concatenate([ya[..., :h] * c - ya[..., h:] * s_, ya[..., h:] * c + ya[..., :h] * s_],
+                           axis=-1)
+    assert np.allclose(again, yab, atol=1e-9)
+    q = _rand_bits(rng, (1, 1, D), dt)
+    k = _rand_bits(rng, (1, 1, D), dt)
+    dots = []
+    for m, n in ((10, 3), (107, 100), (4007, 4000)):
+        _, qm = orc.rope(q, [m], theta, dt, with_f64=True)
+        _, kn = orc.rope(k, [n], theta, dt, with_f64=True)
+        dots.append(float((qm * kn).sum()))
+    assert np.allclose(dots, dots[0], atol=1e-9), dots
+
+
+def check_rope_rounds_its_float64_result(orc):
+    """The stored row is the float64 rotation rounded to the dtype."""
+    rng = np.random.default_rng(14)
+    for dt in ("f16", "bf16"):
+        x = _rand_bits(rng, (2, 4, 128), dt)
+        out, y = orc.rope(x, [9, 30000], 500000.0, dt, with_f64=True)
+        assert np.array_equal(out, orc.encode(y, dt))
+        if dt == "f16":  # numpy rounds float64 to float16 directly
+            assert np.array_equal(out, y.astype(np.float16).view(np.uint16))
+
+
 ALL_CHECKS = [
     check_decode_f16_all_patterns,
     check_decode_bf16_all_patterns,
@@ -358,4 +451,9 @@ ALL_CHECKS = [
     check_rows_match_full,
     check_append_then_gather_is_dense,
     check_empty_context_and_errors,
+    check_encode_round_trips_and_matches_libraries,
+    check_rope_position_zero_is_identity,
+    check_rope_one_hot_closed_form,
+    check_rope_is_a_rotation,
+    check_rope_rounds_its_float64_result,
 ]

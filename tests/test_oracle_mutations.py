@@ -42,6 +42,15 @@ MUTATIONS = [
      "if (p < -1) continue;\n        const int32_t page = table"),
     ("gather_slot_wrong", "* page_size + t % page_size) * head_dim;",
      "* page_size + t % (page_size - 1)) * head_dim;"),
+    ("rope_wrong_partner", "const double x1 = pkv_oracle_decode_bits(x[row + half + i], dtype);",
+     "const double x1 = pkv_oracle_decode_bits(x[row + (half + i + 1) % head_dim], dtype);"),
+    ("rope_sine_sign", "const double y0 = x0 * c - x1 * sn;", "const double y0 = x0 * c + x1 * sn;"),
+    ("rope_frequency_exponent", "pow(theta, -2.0 * i / head_dim)", "pow(theta, -1.0 * i / head_dim)"),
+    ("encode_ties_away", "double r = nearbyint(ldexp(a, mbits - e));",
+     "double r = round(ldexp(a, mbits - e));"),
+    ("encode_no_carry", "if (r == ldexp(1.0, mbits + 1)) {", "if (r == ldexp(1.0, mbits + 2)) {"),
+    ("encode_subnormal_spacing", "nearbyint(ldexp(a, mbits - emin))",
+     "nearbyint(ldexp(a, mbits - emin + 1))"),
 ]
 
 RUNNER = textwrap.dedent("""
