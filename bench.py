@@ -399,6 +399,31 @@ def run_ours(args):
     ms_step = max_over_ranks(dist, ms_step, dev)
     clocks = sampler.finish()
 
+    # ---- the same step with the rotary embedding of q and k_new fused into
+    # the append (paged_decode_step_rope), same timing discipline ----
+    KR = max(1, min(K, 2000))
+    rope_theta = 500000.0
+
+    def rope_step():
+        pkv.paged_decode_step_rope(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens,
+                                   w.scale, rope_theta, out, ws, nw, variant=var)
+
+    for _ in range(max(3, args.warmup)):
+        rope_step()
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    r0.record(stream)
+    for _ in range(KR):
+        rope_step()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    rope_ms = max_over_ranks(dist, r0.elapsed_time(r1) / KR, dev)
+
     # ---- the decode kernel alone: events around its launch on its stream ----
     KD = max(1, min(K, 2000))
     dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
@@ -506,6 +531,10 @@ def run_ours(args):
                         "paged_decode_step, output out, then a host sync",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": KE},
+        "rope_step": {"value": aggregate_gbs(world, by["step"], rope_ms), "unit": UNIT,
+                      "ms_per_step": rope_ms, "steps": KR, "rope_theta": rope_theta,
+                      "what": "paged_decode_step_rope: rotary embedding of q and k_new fused "
+                              "into the append CTAs of the plan launch, same bytes"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "device_status": status,

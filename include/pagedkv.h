@@ -166,6 +166,27 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
                      const int32_t* page_table, int table_stride, const int32_t* positions,
                      int batch, uint32_t* dev_status, pkv_stream stream);
 
+/* Rotary embedding of the step's queries and new keys, then the KV append
+ * (CacheIR, "Compiler Example": rope(q, k) produces the q and k that
+ * attention consumes; TorchInferno, "OpenAI-Compatible Serving" knob list: a
+ * fused decode rotary + KV-append kernel).  The pages give no formula; this
+ * library uses the rotate-half form of Llama/Mistral/Qwen-style models: in
+ * every head, element i (i < D/2) pairs with element i + D/2 and the pair
+ * turns by the angle positions[b] * rope_theta^(-2i/D):
+ *     y_i = x_i cos a - x_{i+D/2} sin a,   y_{i+D/2} = x_{i+D/2} cos a + x_i sin a.
+ * The angle is formed in double (theta^(-2i/D) computed on the host) and
+ * reduced modulo 2 pi exactly; cos/sin and the rotation run in fp32 and are
+ * rounded once to the pool's dtype (to nearest, ties to even), so each result
+ * is within one unit in the last place of the exactly rounded rotation.  q [batch][n_q_heads][D] is
+ * rotated into q_out (q_out may be q itself, no other overlap); k_new is
+ * rotated and v_new copied into the pool as kv_append does (positions[b] < 0:
+ * q is still rotated, nothing is written to the pool).  rope_theta must be
+ * finite and > 0 (INVALID_ARG).  One kernel launch. */
+pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new,
+                          const void* v_new, const int32_t* page_table, int table_stride,
+                          const int32_t* positions, int batch, int n_q_heads, double rope_theta,
+                          void* q_out, uint32_t* dev_status, pkv_stream stream);
+
 /* Materialize each sequence's cached rows as a dense block:
  * k_out[b][h][t][:] = k_pool[page_table[b][t / P]][h][t % P][:] (and v) for
  * t < min(context_lens[b], max_len); other rows of k_out/v_out are not
@@ -289,6 +310,23 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                              pkv_dtype dtype, float scale, void* out, void* workspace,
                              size_t ws_bytes, int num_workers, pkv_decode_variant variant,
                              pkv_stream stream);
+
+/* paged_decode_step with the rotary embedding of kv_append_rope applied to q
+ * and k_new before the append, in the same plan launch (TorchInferno,
+ * "OpenAI-Compatible Serving" knob list: the fused decode rotary + append
+ * kernel).  q holds the step's un-rotated queries; the rotated queries are
+ * written into `out`, which the decode reads as its query and then overwrites
+ * with the attention output (each (sequence, head) row is read before its own
+ * result is written).  Arguments otherwise as for paged_decode_step;
+ * rope_theta finite and > 0.  Three launches. */
+pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const int32_t* positions,
+                                  const void* q, void* k_pool, void* v_pool,
+                                  const int32_t* page_table, int table_stride,
+                                  const int32_t* context_lens, int batch, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                  pkv_dtype dtype, float scale, double rope_theta, void* out,
+                                  void* workspace, size_t ws_bytes, int num_workers,
+                                  pkv_decode_variant variant, pkv_stream stream);
 
 /* ------------------------------------------------------------------------
  * Decode without a caller-provided workspace.

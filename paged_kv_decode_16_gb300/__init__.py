@@ -20,7 +20,8 @@ from . import build as _build
 
 __all__ = [
     "PagedKVError", "load_library", "library_path", "pkv_status_string", "pkv_version",
-    "Pool", "kv_pool_create", "kv_append", "kv_gather", "paged_decode_workspace_size",
+    "Pool", "kv_pool_create", "kv_append", "kv_append_rope", "kv_gather",
+    "paged_decode_workspace_size", "paged_decode_step_rope",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
@@ -78,6 +79,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "kv_pool_refcount": ([V, ctypes.c_int32], I),
         "kv_pool_info": ([V, V, V, V, V, V], I),
         "kv_append": ([V, V, V, V, I, V, I, V, V], I),
+        "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, V], I),
+        "paged_decode_step_rope": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F,
+                                    ctypes.c_double, V, V, Z, I, I, V], I),
         "kv_gather": ([V, V, I, V, I, I, V, V, V, V], I),
         "paged_decode_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_plan": ([V, I, I, I, I, I, I, I, I, V, Z, V], I),
@@ -255,6 +259,34 @@ def kv_append(pool: Pool, k_new: torch.Tensor, v_new: torch.Tensor, page_table: 
                                     _stream(stream)), "kv_append")
 
 
+def kv_append_rope(pool: Pool, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   page_table: torch.Tensor, positions: torch.Tensor, rope_theta: float,
+                   q_out: torch.Tensor, dev_status: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Rotary embedding of q [B, Hq, D] (into q_out) and k_new at positions[b],
+    then the append of the rotated k_new and v_new into the pool."""
+    _dev(q, "q", pool.dtype, 3)
+    _dev(q_out, "q_out", pool.dtype, 3)
+    _dev(k_new, "k_new", pool.dtype, 3)
+    _dev(v_new, "v_new", pool.dtype, 3)
+    _dev(page_table, "page_table", torch.int32, 2)
+    _dev(positions, "positions", torch.int32, 1)
+    B = positions.shape[0]
+    if k_new.shape != v_new.shape or k_new.shape != (B, pool.n_kv_heads, pool.head_dim):
+        raise ValueError("k_new/v_new must be [B, Hkv, D] matching the pool")
+    if q.shape[0] != B or q.shape[2] != pool.head_dim or q_out.shape != q.shape:
+        raise ValueError("q/q_out must be [B, Hq, D] matching the pool")
+    if page_table.shape[0] != B:
+        raise ValueError("page_table rows != batch")
+    if dev_status is not None:
+        _dev(dev_status, "dev_status", torch.int32)
+    _check(load_library().kv_append_rope(
+        pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(page_table), page_table.shape[1],
+        _ptr(positions), B, q.shape[1], float(rope_theta), _ptr(q_out), _ptr(dev_status),
+        _stream(stream)), "kv_append_rope")
+    return q_out
+
+
 def kv_gather(pool: Pool, page_table: torch.Tensor, context_lens: torch.Tensor, max_len: int,
               k_out: torch.Tensor, v_out: torch.Tensor, dev_status: torch.Tensor | None = None,
               stream=None) -> None:
@@ -361,6 +393,31 @@ def paged_decode_step(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch
         _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
         float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(num_workers),
         int(variant), _stream(stream)), "paged_decode_step")
+    return out
+
+
+def paged_decode_step_rope(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
+                           q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           rope_theta: float, out: torch.Tensor, workspace: torch.Tensor,
+                           num_workers: int = 0, stream=None,
+                           variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """paged_decode_step with the rotary embedding of q and k_new at positions[b]
+    (angle base rope_theta) fused into the append; q stays un-rotated, the
+    rotated queries pass through out before the result overwrites them."""
+    B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8)
+    _dev(k_new, "k_new", q.dtype, 3)
+    _dev(v_new, "v_new", q.dtype, 3)
+    _dev(positions, "positions", torch.int32, 1)
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    _check(load_library().paged_decode_step_rope(
+        _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
+        float(scale), float(rope_theta), _ptr(out), _ptr(workspace), workspace.numel(),
+        int(num_workers), int(variant), _stream(stream)), "paged_decode_step_rope")
     return out
 
 

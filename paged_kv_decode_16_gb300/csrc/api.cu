@@ -387,7 +387,18 @@ pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t*
     a.vecs = head_dim / 8;
     a.page_size = page_size;
     a.num_pages = num_pages;
+    a.q_in = nullptr;  // no rotary embedding unless the caller sets it up
+    a.q_out = nullptr;
+    a.n_q_heads = 0;
+    a.bf16 = 0;
     return a;
+}
+
+// The rotary angles per position unit, theta^(-2i/D) for i < D/2, in double
+// (the kernel multiplies them by each token's position).
+void set_inv_freq(pkv::AppendArgs* a, double theta, int head_dim) {
+    for (int i = 0; i < 64; ++i)
+        a->inv_freq[i] = i < head_dim / 2 ? pow(theta, -2.0 * i / head_dim) : 0.0;
 }
 
 // Host-only argument checks of a decode call (no CUDA call is made), in the
@@ -465,6 +476,45 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
                                           pool->page_size, pool->num_pages);
     return cuda_status(pkv::launch_append(a, batch, dev_status,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new,
+                          const void* v_new, const int32_t* page_table, int table_stride,
+                          const int32_t* positions, int batch, int n_q_heads, double rope_theta,
+                          void* q_out, uint32_t* dev_status, pkv_stream stream) {
+    if (!pool || batch < 0 || table_stride <= 0 || n_q_heads <= 0) return PKV_ERR_INVALID_ARG;
+    if (!(rope_theta > 0.0 && isfinite(rope_theta))) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!q || !q_out || !k_new || !v_new || !page_table || !positions) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(q_out) || !aligned16(k_new) || !aligned16(v_new))
+        return PKV_ERR_INVALID_ARG;
+    const size_t pool_bytes =
+        (size_t)pool->num_pages * pool->n_kv_heads * pool->page_size * pool->head_dim * 2;
+    const size_t row_bytes = (size_t)batch * pool->n_kv_heads * pool->head_dim * 2;
+    const size_t q_bytes = (size_t)batch * n_q_heads * pool->head_dim * 2;
+    const void* ins[3] = {q, k_new, v_new};
+    const size_t in_bytes[3] = {q_bytes, row_bytes, row_bytes};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(ins[i], in_bytes[i], pool->k, pool_bytes) ||
+            overlaps(ins[i], in_bytes[i], pool->v, pool_bytes))
+            return PKV_ERR_ALIAS;
+    // q_out may be q itself (each element is read before it is written), but no
+    // other overlap
+    if ((q_out != q && overlaps(q_out, q_bytes, q, q_bytes)) ||
+        overlaps(q_out, q_bytes, k_new, row_bytes) || overlaps(q_out, q_bytes, v_new, row_bytes) ||
+        overlaps(q_out, q_bytes, pool->k, pool_bytes) ||
+        overlaps(q_out, q_bytes, pool->v, pool_bytes))
+        return PKV_ERR_ALIAS;
+    pkv::AppendArgs a = make_append(k_new, v_new, positions, page_table, table_stride, pool->k,
+                                    pool->v, pool->n_kv_heads, pool->head_dim, pool->page_size,
+                                    pool->num_pages);
+    a.q_in = static_cast<const uint4*>(q);
+    a.q_out = static_cast<uint4*>(q_out);
+    a.n_q_heads = n_q_heads;
+    set_inv_freq(&a, rope_theta, pool->head_dim);
+    a.bf16 = pool->dtype == PKV_BF16;
+    return cuda_status(pkv::launch_rope_append(a, batch, pool->head_dim, dev_status,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pkv_status kv_gather(const pkv_pool* pool, const int32_t* page_table, int table_stride,
@@ -598,14 +648,19 @@ pkv_status paged_decode_attention(const void* q, const void* k_pool, const void*
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
 }
 
-pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t* positions,
-                             const void* q, void* k_pool, void* v_pool,
-                             const int32_t* page_table, int table_stride,
-                             const int32_t* context_lens, int batch, int n_q_heads,
-                             int n_kv_heads, int head_dim, int page_size, int num_pages,
-                             pkv_dtype dtype, float scale, void* out, void* workspace,
-                             size_t ws_bytes, int num_workers, pkv_decode_variant variant,
-                             pkv_stream stream) {
+}  // extern "C" (reopened below)
+
+namespace {
+// One decode step; rope: the rotary embedding of q and k_new (angle base
+// rope_theta) runs in the append CTAs, and the rotated q goes through `out`.
+pkv_status step_impl(const void* k_new, const void* v_new, const int32_t* positions,
+                     const void* q, void* k_pool, void* v_pool, const int32_t* page_table,
+                     int table_stride, const int32_t* context_lens, int batch, int n_q_heads,
+                     int n_kv_heads, int head_dim, int page_size, int num_pages, pkv_dtype dtype,
+                     float scale, bool rope, double rope_theta, void* out, void* workspace,
+                     size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                     pkv_stream stream) {
+    if (rope && !(rope_theta > 0.0 && isfinite(rope_theta))) return PKV_ERR_INVALID_ARG;
     pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
                                          context_lens, true, batch, n_q_heads, n_kv_heads,
                                          head_dim, page_size, num_pages, dtype, scale, out,
@@ -628,17 +683,54 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
         return st;
     if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const pkv::AppendArgs a = make_append(k_new, v_new, positions, page_table, table_stride,
-                                          k_pool, v_pool, n_kv_heads, head_dim, page_size,
-                                          num_pages);
+    pkv::AppendArgs a = make_append(k_new, v_new, positions, page_table, table_stride, k_pool,
+                                    v_pool, n_kv_heads, head_dim, page_size, num_pages);
+    if (rope) {
+        a.q_in = static_cast<const uint4*>(q);
+        a.q_out = static_cast<uint4*>(out);  // the decode reads the rotated q from here
+        a.n_q_heads = n_q_heads;
+        set_inv_freq(&a, rope_theta, head_dim);
+        a.bf16 = dtype == PKV_BF16;
+    }
     if ((st = do_plan(context_lens, page_table, batch, page_size, table_stride, num_workers,
                       workspace, s, &a, cs)) != PKV_OK)
         return st;
-    if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
-                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, false, cs)) !=
-        PKV_OK)
+    if ((st = do_run(rope ? out : q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads,
+                     n_kv_heads, head_dim, page_size, num_pages, dtype, scale, out, workspace, s,
+                     false, cs)) != PKV_OK)
         return st;
     return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
+}
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t* positions,
+                             const void* q, void* k_pool, void* v_pool,
+                             const int32_t* page_table, int table_stride,
+                             const int32_t* context_lens, int batch, int n_q_heads,
+                             int n_kv_heads, int head_dim, int page_size, int num_pages,
+                             pkv_dtype dtype, float scale, void* out, void* workspace,
+                             size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                             pkv_stream stream) {
+    return step_impl(k_new, v_new, positions, q, k_pool, v_pool, page_table, table_stride,
+                     context_lens, batch, n_q_heads, n_kv_heads, head_dim, page_size, num_pages,
+                     dtype, scale, false, 0.0, out, workspace, ws_bytes, num_workers, variant,
+                     stream);
+}
+
+pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const int32_t* positions,
+                                  const void* q, void* k_pool, void* v_pool,
+                                  const int32_t* page_table, int table_stride,
+                                  const int32_t* context_lens, int batch, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                  pkv_dtype dtype, float scale, double rope_theta, void* out,
+                                  void* workspace, size_t ws_bytes, int num_workers,
+                                  pkv_decode_variant variant, pkv_stream stream) {
+    return step_impl(k_new, v_new, positions, q, k_pool, v_pool, page_table, table_stride,
+                     context_lens, batch, n_q_heads, n_kv_heads, head_dim, page_size, num_pages,
+                     dtype, scale, true, rope_theta, out, workspace, ws_bytes, num_workers,
+                     variant, stream);
 }
 
 pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool,

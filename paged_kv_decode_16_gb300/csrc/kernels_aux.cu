@@ -35,6 +35,149 @@ __device__ __forceinline__ uint32_t append_vec(const AppendArgs& a, long long id
 }
 
 // ---------------------------------------------------------------------------
+// Rotary embedding before the append (CacheIR, "Compiler Example": rope(q, k)
+// feeds attention; TorchInferno, "OpenAI-Compatible Serving" knob list: a
+// fused decode rotary + KV append kernel).  Rotate-half pairing: element i of
+// a head pairs with i + D/2 and turns by pos * theta^(-2i/D).  The angle is
+// formed in double (pos times the host's theta^(-2i/D)) and reduced modulo
+// 2 pi with fused multiply-adds, which keeps it exact to double precision for
+// any int32 position; cos / sin of the reduced angle and the rotation itself
+// run in fp32 (fused multiply-add) and are rounded once to the element type.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
+};
+template <>
+struct Elem<__half> {
+    static __device__ __forceinline__ float to(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ __half from(float x) { return __float2half_rn(x); }
+};
+
+// cos and sin of pos * inv: the product in double, reduced by the nearest
+// multiple of 2 pi (2 pi as a double plus its remainder), then fp32.
+__device__ __forceinline__ void rope_cos_sin(int pos, double inv, float* c, float* s) {
+    const double two_pi_hi = 6.283185307179586;       // 2 pi rounded to double
+    const double two_pi_lo = 2.4492935982947064e-16;  // 2 pi - two_pi_hi
+    const double ang = (double)pos * inv;
+    const double k = rint(ang * (1.0 / two_pi_hi));
+    double r = fma(-k, two_pi_hi, ang);
+    r = fma(-k, two_pi_lo, r);
+    sincosf((float)r, s, c);
+}
+
+// Rotate the 8 pairs held by lo (first-half elements 8j .. 8j+7) and hi (their
+// partners), with cos / sin of those pairs' angles.
+template <typename T>
+__device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* c, const float* s) {
+    T* a = reinterpret_cast<T*>(&lo);
+    T* b = reinterpret_cast<T*>(&hi);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float x0 = Elem<T>::to(a[e]), x1 = Elem<T>::to(b[e]);
+        a[e] = Elem<T>::from(fmaf(x0, c[e], -x1 * s[e]));
+        b[e] = Elem<T>::from(fmaf(x1, c[e], x0 * s[e]));
+    }
+}
+
+// One CTA pass over sequences [b0, b0 + nseq): the cos / sin table of their
+// positions (one angle per thread), then every 16-byte vector pair of their q
+// rows (rotated into q_out) and k rows (rotated into the pool), and their v
+// rows (copied).  tbl: 2 * nseq * D/2 floats of shared memory.  Returns the
+// PKV_DEV_* bits of skipped rows.  Block-collective.
+template <typename T>
+__device__ uint32_t rope_append_pass(const AppendArgs& a, int b0, int nseq, int batch,
+                                     int head_dim, float* tbl) {
+    const int half = head_dim / 2;
+    const int hv = half / 8;  // 16-byte vectors per half row
+    float* ctab = tbl;
+    float* stab = tbl + nseq * half;
+    for (int t = threadIdx.x; t < nseq * half; t += blockDim.x) {
+        const int b = b0 + t / half, i = t % half;
+        float cv = 1.f, sv = 0.f;
+        if (b < batch) rope_cos_sin(a.positions[b], a.inv_freq[i], &cv, &sv);
+        ctab[t] = cv;
+        stab[t] = sv;
+    }
+    __syncthreads();
+    uint32_t flags = 0;
+    const int qi = a.n_q_heads * hv, ki = a.n_kv_heads * hv, vi = a.n_kv_heads * a.vecs;
+    const int per_seq = qi + ki + vi;
+    for (int it = threadIdx.x; it < nseq * per_seq; it += blockDim.x) {
+        const int sq = it / per_seq, r = it - sq * per_seq;
+        const int b = b0 + sq;
+        if (b >= batch) break;
+        const float* c = ctab + sq * half;
+        const float* sn = stab + sq * half;
+        if (r < qi) {  // query row: rotate into q_out
+            const int h = r / hv, j = r % hv;
+            const long long row = ((long long)b * a.n_q_heads + h) * a.vecs;
+            uint4 lo = a.q_in[row + j], hi = a.q_in[row + hv + j];
+            rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j);
+            a.q_out[row + j] = lo;
+            a.q_out[row + hv + j] = hi;
+            continue;
+        }
+        const int p = a.positions[b];
+        if (p < 0) continue;  // padded batch slot: never writes the pool
+        const int pi = p / a.page_size;
+        const int rr = r - qi;
+        const bool first = rr == 0;  // reports a skipped row once
+        if (pi >= a.table_stride) {
+            if (first) flags |= PKV_DEV_BAD_LEN;
+            continue;
+        }
+        const int page = a.table[(long long)b * a.table_stride + pi];
+        if (page < 0 || page >= a.num_pages) {
+            if (first) flags |= PKV_DEV_BAD_PAGE;
+            continue;
+        }
+        const long long base =
+            (((long long)page * a.n_kv_heads) * a.page_size + p % a.page_size) * a.vecs;
+        if (rr < ki) {  // key row: rotate into the pool
+            const int h = rr / hv, j = rr % hv;
+            const long long src = ((long long)b * a.n_kv_heads + h) * a.vecs;
+            const long long dst = base + (long long)h * a.page_size * a.vecs;
+            uint4 lo = a.k_new[src + j], hi = a.k_new[src + hv + j];
+            rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j);
+            a.k_pool[dst + j] = lo;
+            a.k_pool[dst + hv + j] = hi;
+        } else {  // value row: bit copy
+            const int v = rr - ki;
+            const int h = v / a.vecs, j = v % a.vecs;
+            const long long src = ((long long)b * a.n_kv_heads + h) * a.vecs;
+            const long long dst = base + (long long)h * a.page_size * a.vecs;
+            a.v_pool[dst + j] = a.v_new[src + j];
+        }
+    }
+    __syncthreads();  // the table is rewritten by the next pass
+    return flags;
+}
+
+// Sequences per pass: enough CTAs for the batch (up to kMaxAppendCtas), at most
+// one angle per thread.
+__host__ __device__ inline int rope_seqs_per_pass(int batch, int head_dim) {
+    const int cap = kRopeThreads / (head_dim / 2);
+    int n = (batch + kMaxAppendCtas - 1) / kMaxAppendCtas;
+    return n < 1 ? 1 : (n > cap ? cap : n);
+}
+
+// Every pass of one CTA (CTA cta of nctas), for either element type.
+__device__ uint32_t rope_append_cta(const AppendArgs& a, int batch, int head_dim, int cta,
+                                    int nctas, float* tbl) {
+    const int seqs = rope_seqs_per_pass(batch, head_dim);
+    uint32_t flags = 0;
+    for (int b0 = cta * seqs; b0 < batch; b0 += nctas * seqs) {
+        flags |= a.bf16 ? rope_append_pass<__nv_bfloat16>(a, b0, seqs, batch, head_dim, tbl)
+                        : rope_append_pass<__half>(a, b0, seqs, batch, head_dim, tbl);
+    }
+    return flags;
+}
+
+// ---------------------------------------------------------------------------
 // Plan (CTA 0) and fused append (CTAs 1 .. append_ctas).
 // Plan: clamps each context length to [0, table_stride * P] (PKV_DEV_BAD_LEN
 // when it had to), writes the per-sequence chunk prefix sums (chunks of every
@@ -59,11 +202,16 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
     }
     __syncthreads();
     if (blockIdx.x > 0) {
-        const long long total = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
         uint32_t f = 0;
-        for (long long idx = (long long)(blockIdx.x - 1) * blockDim.x + tid; idx < total;
-             idx += (long long)append_ctas * blockDim.x)
-            f |= append_vec(aa, idx);
+        if (aa.q_in) {  // rotary embedding, then the append
+            __shared__ float s_rope[2 * kRopeThreads];
+            f = rope_append_cta(aa, pa.batch, aa.vecs * 8, blockIdx.x - 1, append_ctas, s_rope);
+        } else {
+            const long long total = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
+            for (long long idx = (long long)(blockIdx.x - 1) * blockDim.x + tid; idx < total;
+                 idx += (long long)append_ctas * blockDim.x)
+                f |= append_vec(aa, idx);
+        }
         if (f) atomicOr(&flags, f);
         __syncthreads();
         if (tid == 0) pa.hdr->append_status[blockIdx.x - 1] = flags;
@@ -289,8 +437,14 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
     int append_ctas = 0;
     if (append) {
         aa = *append;
-        const long long vecs = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
-        const long long ctas = (vecs + 1023) / 1024;
+        long long ctas;
+        if (aa.q_in) {  // rotary + append: rope_seqs_per_pass sequences per CTA pass
+            const int seqs = rope_seqs_per_pass(pa.batch, aa.vecs * 8);
+            ctas = (pa.batch + seqs - 1) / seqs;
+        } else {
+            const long long vecs = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
+            ctas = (vecs + 1023) / 1024;
+        }
         append_ctas = (int)(ctas < kMaxAppendCtas ? ctas : kMaxAppendCtas);
     }
     return launch_pdl(plan_kernel, dim3(1 + append_ctas), dim3(1024), 0, stream, pa, aa,
@@ -322,6 +476,30 @@ cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status,
     if (total == 0) return cudaSuccess;
     const int blocks = (int)((total + 255) / 256);
     return launch_pdl(append_kernel, dim3(blocks), dim3(256), 0, stream, a, batch, status);
+}
+
+// Stand-alone rotary + append: each CTA ORs its skipped-row bits into status.
+__global__ void __launch_bounds__(kRopeThreads)
+rope_append_kernel(AppendArgs a, int batch, int head_dim, uint32_t* status) {
+    __shared__ float s_rope[2 * kRopeThreads];
+    __shared__ uint32_t flags;
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) flags = 0;
+    __syncthreads();
+    const uint32_t f = rope_append_cta(a, batch, head_dim, blockIdx.x, gridDim.x, s_rope);
+    if (f) atomicOr(&flags, f);
+    __syncthreads();
+    if (threadIdx.x == 0 && flags) set_status(status, flags);
+}
+
+cudaError_t launch_rope_append(const AppendArgs& a, int batch, int head_dim, uint32_t* status,
+                               cudaStream_t stream) {
+    if (batch == 0) return cudaSuccess;
+    const int seqs = rope_seqs_per_pass(batch, head_dim);
+    const int ctas = (batch + seqs - 1) / seqs;
+    return launch_pdl(rope_append_kernel, dim3(ctas), dim3(kRopeThreads), 0, stream, a, batch,
+                      head_dim, status);
 }
 
 cudaError_t launch_gather(const void* k_pool, const void* v_pool, const int32_t* table,

@@ -37,7 +37,17 @@ struct AppendArgs {
     uint4* k_pool;
     uint4* v_pool;
     int n_kv_heads, vecs, page_size, num_pages;  // vecs = D / 8
+    // rotary embedding before the append (q_in null: plain append)
+    const uint4* q_in;     // [B][Hq][D] queries of the step
+    uint4* q_out;          // [B][Hq][D] rotated queries
+    int n_q_heads;
+    int bf16;              // element type of q / k / v: bf16, else fp16
+    double inv_freq[64];   // theta^(-2i/D), i < D/2 (computed on the host)
 };
+
+// Rotary + append: sequences handled together by one CTA of 1024 threads
+// (one angle per thread: 1024 / (D / 2)), and their cos / sin table.
+constexpr int kRopeThreads = 1024;
 
 // Plan, optionally with the append fused into the same launch.
 cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream_t stream);
@@ -48,9 +58,13 @@ cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            int group, int n_q_heads, int merge_batch, cudaStream_t stream);
 
 // batches up to this size keep their chunk prefix sums in the plan's shared memory
-constexpr int kPlanSmemSeqs = 8192;
+constexpr int kPlanSmemSeqs = 4096;
 
 cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status, cudaStream_t stream);
+
+// Rotary embedding of q and k_new, then the append (stand-alone launch).
+cudaError_t launch_rope_append(const AppendArgs& a, int batch, int head_dim, uint32_t* status,
+                               cudaStream_t stream);
 
 cudaError_t launch_gather(const void* k_pool, const void* v_pool, const int32_t* table,
                           int table_stride, const int32_t* lens, int batch, int n_kv_heads,

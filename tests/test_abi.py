@@ -230,3 +230,25 @@ def test_no_alloc_shape_checks_on_host(lib):
     assert call(hq=6, hkv=4) == INVALID
     assert call(batch=-1) == INVALID
     assert call(batch=0) == OK
+
+
+def test_rope_entry_points_check_theta_on_host(lib):
+    V = ctypes.c_void_p
+    for theta in (0.0, -1.0, float("nan"), float("inf")):
+        rc = lib.paged_decode_step_rope(V(A * 30), V(A * 31), V(A * 32), V(A), V(A * 8),
+                                        V(A * 16), V(A * 24), 4, V(A * 25), 2, 8, 2, 128, 16, 8,
+                                        BF16, ctypes.c_float(0.088), ctypes.c_double(theta),
+                                        V(A * 26), V(A * 27), 1 << 20, 0, 0, None)
+        assert rc == INVALID
+    h = V()
+    assert lib.kv_pool_create(8, 16, 2, 128, BF16, V(A), V(A * 2), ctypes.byref(h)) == OK
+    try:
+        assert lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), 2, 8,
+                                  ctypes.c_double(0.0), V(A * 9), None, None) == INVALID
+        # q_out partly over q is refused; q_out == q (in place) passes the host checks
+        assert lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), 2, 8,
+                                  ctypes.c_double(1e4), V(A * 3 + 256), None, None) == ALIAS
+        assert lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), 0, 8,
+                                  ctypes.c_double(1e4), V(A * 3), None, None) == OK
+    finally:
+        lib.kv_pool_destroy(h)
