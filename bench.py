@@ -424,6 +424,39 @@ def run_ours(args):
         dist.barrier()
     rope_ms = max_over_ranks(dist, r0.elapsed_time(r1) / KR, dev)
 
+    # ---- shared-prefix decode on the prefix-sharing workload (64 sequences,
+    # one 2048-token prefix): the cascade against the plain decode ----
+    wp = wl.make("prefix_sharing", seed=args.seed, device=dev)
+    tp = torch.from_numpy(wp.page_table).to(dev)
+    lp = torch.from_numpy(wp.context_lens).to(dev)
+    op = torch.empty_like(wp.q)
+    wsp_plain = pkv.alloc_workspace(wp.batch, wp.n_q_heads, wp.n_kv_heads, wp.head_dim, nw,
+                                    device=dev, variant=var)
+    wsp = pkv.alloc_prefix_workspace(wp.batch, wp.n_q_heads, wp.n_kv_heads, wp.head_dim, nw,
+                                     device=dev, variant=var)
+
+    def timed_loop(fn, n):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(dist, e0.elapsed_time(e1) / n, dev)
+
+    KP = max(1, min(K, 2000))
+    prefix_ms = timed_loop(lambda: pkv.paged_decode_attention_prefix(
+        wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, wp.prefix_len, op, wsp, nw,
+        variant=var), KP)
+    plain_ms = timed_loop(lambda: pkv.paged_decode_attention(
+        wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, op, wsp_plain, nw, variant=var), KP)
+    pby = step_bytes(wp)
+    del wp, tp, lp, op, wsp, wsp_plain
+
     # ---- the decode kernel alone: events around its launch on its stream ----
     KD = max(1, min(K, 2000))
     dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
@@ -535,6 +568,14 @@ def run_ours(args):
                       "ms_per_step": rope_ms, "steps": KR, "rope_theta": rope_theta,
                       "what": "paged_decode_step_rope: rotary embedding of q and k_new fused "
                               "into the append CTAs of the plan launch, same bytes"},
+        "prefix_sharing": {
+            "what": "paged_decode_attention_prefix (shared prefix attended once per KV head "
+                    "for all queries, then the suffixes, then the merge) vs "
+                    "paged_decode_attention on the prefix_sharing workload",
+            "ms_prefix": prefix_ms, "ms_plain": plain_ms, "steps": KP,
+            "gbs_unique_prefix": (pby["kv_unique"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
+            "gbs_logical_prefix": (pby["kv_logical"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
+            "gbs_logical_plain": (pby["kv_logical"] + pby["qo"]) / (plain_ms * 1e-3) / 1e9},
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "device_status": status,

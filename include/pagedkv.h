@@ -87,6 +87,7 @@ typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEV_BAD_PAGE 0x1u   /* a page id outside [0, num_pages) was skipped */
 #define PKV_DEV_BAD_LEN  0x2u   /* a length/position beyond the table row was clamped/skipped */
 #define PKV_DEV_TIMEOUT  0x4u   /* a bounded wait on a copy gave up (copy never landed) */
+#define PKV_DEV_BAD_PREFIX 0x8u /* a table row does not start with the shared prefix's pages */
 
 typedef struct CUstream_st* pkv_stream; /* same type as cudaStream_t */
 typedef struct pkv_pool pkv_pool;       /* opaque */
@@ -327,6 +328,37 @@ pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const in
                                   pkv_dtype dtype, float scale, double rope_theta, void* out,
                                   void* workspace, size_t ws_bytes, int num_workers,
                                   pkv_decode_variant variant, pkv_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Shared-prefix decode (CacheIR, "Current Capabilities": batched decode over
+ * shared page tables; Experimental LibTorch prefix cache, "Short shared prefix
+ * qualification": related requests should share immutable block storage).
+ *
+ * For a batch whose rows all begin with the same prefix_tokens tokens stored
+ * in the same pages (columns 0 .. prefix_tokens/P - 1 of every table row equal
+ * to row 0's), the prefix is attended once per KV head for all B*G query rows
+ * (tensor-core tiles of up to 16 rows read each prefix chunk once), each
+ * sequence's own tokens are attended as usual, and the two partial states of
+ * every (sequence, head) are merged: out equals paged_decode_attention's
+ * within the decode tolerance.  prefix_tokens > 0, a multiple of page_size, at
+ * most table_stride * page_size (INVALID_ARG); every context_lens[b] >=
+ * prefix_tokens (else PKV_DEV_BAD_LEN); rows that do not start with row 0's
+ * prefix pages set PKV_DEV_BAD_PREFIX (their results are then wrong).  Both
+ * read through pkv_read_device_status(workspace).  Six launches (two plans, a
+ * query gather, two decodes, the merge).
+ * ------------------------------------------------------------------------ */
+pkv_status paged_decode_prefix_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                              int head_dim, int num_workers,
+                                              pkv_decode_variant variant, size_t* bytes);
+
+pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* page_table, int table_stride,
+                                         const int32_t* context_lens, int batch, int n_q_heads,
+                                         int n_kv_heads, int head_dim, int page_size,
+                                         int num_pages, pkv_dtype dtype, float scale,
+                                         int prefix_tokens, void* out, void* workspace,
+                                         size_t ws_bytes, int num_workers,
+                                         pkv_decode_variant variant, pkv_stream stream);
 
 /* ------------------------------------------------------------------------
  * Decode without a caller-provided workspace.

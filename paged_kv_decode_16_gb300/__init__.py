@@ -21,7 +21,8 @@ from . import build as _build
 __all__ = [
     "PagedKVError", "load_library", "library_path", "pkv_status_string", "pkv_version",
     "Pool", "kv_pool_create", "kv_append", "kv_append_rope", "kv_gather",
-    "paged_decode_workspace_size", "paged_decode_step_rope",
+    "paged_decode_workspace_size", "paged_decode_step_rope", "paged_decode_attention_prefix",
+    "paged_decode_prefix_workspace_size", "alloc_prefix_workspace", "DEV_BAD_PREFIX",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
@@ -32,7 +33,7 @@ PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 3: "PKV_ERR_ALIAS", 4: "PKV_ERR_OUT_OF_PAGES", 5: "PKV_ERR_WORKSPACE",
                 6: "PKV_ERR_CUDA", 7: "PKV_ERR_DEVICE_CHECK", 8: "PKV_ERR_REFCOUNT"}
-DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
+DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT, DEV_BAD_PREFIX = 0x1, 0x2, 0x4, 0x8
 # decode kernels (pkv_decode_variant)
 VARIANT_AUTO, VARIANT_CUDA_CORES, VARIANT_TENSOR_CORES = 0, 1, 2
 # size of the library's fixed device scratch (PKV_NO_ALLOC_SCRATCH_BYTES)
@@ -80,6 +81,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "kv_pool_info": ([V, V, V, V, V, V], I),
         "kv_append": ([V, V, V, V, I, V, I, V, V], I),
         "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, V], I),
+        "paged_decode_prefix_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
+        "paged_decode_attention_prefix": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, I, V, V, Z,
+                                           I, I, V], I),
         "paged_decode_step_rope": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F,
                                     ctypes.c_double, V, V, Z, I, I, V], I),
         "kv_gather": ([V, V, I, V, I, I, V, V, V, V], I),
@@ -370,6 +374,43 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
         _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), int(num_workers),
         int(variant), _stream(stream)),
         "paged_decode_attention_no_alloc")
+    return out
+
+
+def paged_decode_prefix_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int,
+                                       head_dim: int, num_workers: int = 0,
+                                       variant: int = VARIANT_AUTO) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().paged_decode_prefix_workspace_size(
+        batch, n_q_heads, n_kv_heads, head_dim, int(num_workers), int(variant), ctypes.byref(n)),
+        "paged_decode_prefix_workspace_size")
+    return n.value
+
+
+def alloc_prefix_workspace(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                           num_workers: int = 0, device=None,
+                           variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """A torch uint8 buffer of the size paged_decode_attention_prefix needs."""
+    n = paged_decode_prefix_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, num_workers,
+                                           variant)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_attention_prefix(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                  page_table: torch.Tensor, context_lens: torch.Tensor,
+                                  scale: float, prefix_tokens: int, out: torch.Tensor,
+                                  workspace: torch.Tensor, num_workers: int = 0, stream=None,
+                                  variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """Decode attention for a batch whose rows share their first prefix_tokens
+    tokens (the same pages): the prefix is attended once for all queries."""
+    B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8)
+    _check(load_library().paged_decode_attention_prefix(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1],
+        _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), int(prefix_tokens), _ptr(out),
+        _ptr(workspace), workspace.numel(), int(num_workers), int(variant), _stream(stream)),
+        "paged_decode_attention_prefix")
     return out
 
 

@@ -174,7 +174,8 @@ int resolve_variant(int variant) {
 }
 
 pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
-                        pkv_dtype dtype, int num_workers, int variant, DecodeSetup* s) {
+                        pkv_dtype dtype, int num_workers, int variant, DecodeSetup* s,
+                        int force_gs = 0) {
     pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
     if (st != PKV_OK) return st;
     if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
@@ -182,7 +183,13 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     const int v = resolve_variant(variant);
     s->group = n_q_heads / n_kv_heads;
     const int max_gs = v == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
-    if (!split_group(s->group, max_gs, &s->sub_groups, &s->gs)) return PKV_ERR_UNSUPPORTED;
+    if (force_gs > 0) {  // a sub-group size chosen by the caller (divides the group)
+        if (force_gs > max_gs || s->group % force_gs) return PKV_ERR_UNSUPPORTED;
+        s->gs = force_gs;
+        s->sub_groups = s->group / force_gs;
+    } else if (!split_group(s->group, max_gs, &s->sub_groups, &s->gs)) {
+        return PKV_ERR_UNSUPPORTED;
+    }
     s->units_per_b = n_kv_heads * s->sub_groups;
     s->units = (long long)batch * s->units_per_b;
     s->kernel = pick_kernel(dtype, head_dim, v, s->gs);
@@ -268,13 +275,22 @@ pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dt
 
 pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch, int page_size,
                    int table_stride, int num_workers, void* workspace, const DecodeSetup& s,
-                   const pkv::AppendArgs* append, cudaStream_t stream) {
+                   const pkv::AppendArgs* append, cudaStream_t stream, int skip_cols = 0,
+                   int uniform_len = -1, const int32_t* share_table = nullptr,
+                   int share_rows = 0, int share_cols = 0) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     pkv::PlanArgs pa;
     pa.lens = context_lens;
+    // skip_cols: the decoded range starts skip_cols table columns into each row
+    // (table points at that column); lengths count from the row's start
+    pa.len_offset = skip_cols * page_size;
+    pa.uniform_len = uniform_len;      // >= 0: every sequence has this length (lens unused)
+    pa.share_table = share_table;      // rows 1.. must start with row 0's first share_cols ids
+    pa.share_rows = share_rows;
+    pa.share_cols = share_cols;
     pa.batch = batch;
     pa.units_per_b = s.units_per_b;
-    pa.cap = (long long)table_stride * page_size;
+    pa.cap = (long long)(table_stride - skip_cols) * page_size;
     pa.workers_req = num_workers > 0 ? s.workers : 0;
     pa.workers_auto = s.workers_auto;
     pa.min_chunks = kMinChunksPerWorker;
@@ -293,7 +309,8 @@ pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch,
 pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
                   int table_stride, int batch, int n_q_heads, int n_kv_heads, int head_dim,
                   int page_size, int num_pages, pkv_dtype dtype, float scale, void* out,
-                  void* workspace, const DecodeSetup& s, bool merge, cudaStream_t stream) {
+                  void* workspace, const DecodeSetup& s, bool merge, cudaStream_t stream,
+                  bool all_partials = false, uint32_t* status = nullptr) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     pkv::DecodeParams p;
     p.q = q;
@@ -305,10 +322,11 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.wstart = reinterpret_cast<const int32_t*>(ws + s.ws.wstart);
     p.units = (int)s.units;
     p.hdr = reinterpret_cast<const WsHeader*>(ws);
-    p.status = &reinterpret_cast<WsHeader*>(ws)->status;
+    p.status = status ? status : &reinterpret_cast<WsHeader*>(ws)->status;
     p.partials = reinterpret_cast<float*>(ws + s.ws.partials);
     p.unit_done = merge ? reinterpret_cast<int32_t*>(ws + s.ws.unit_done) : nullptr;
     p.merge_batch = s.merge_batch;
+    p.all_partials = all_partials ? 1 : 0;
     p.out = out;
     p.table_stride = table_stride;
     p.batch = batch;
@@ -781,6 +799,138 @@ pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
     for (int i = 0; i < n; ++i) v |= h.append_status[i];
     *status_out = v;
     return v ? PKV_ERR_DEVICE_CHECK : PKV_OK;
+}
+
+}  // extern "C"
+
+// --- shared-prefix decode (cascade) ----------------------------------------
+namespace {
+struct PrefixSetup {
+    DecodeSetup real, virt;  // suffix pass (real units), prefix pass (virtual units)
+    size_t qv_off, v_off, s_off, total;
+};
+
+// The prefix pass: one sequence (the shared prefix) whose every KV head serves
+// all B*G query rows of that head, in sub-groups of gs_v rows, gs_v a multiple
+// of the real sub-group size so that every real unit lies in one virtual unit.
+pkv_status setup_prefix(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                        pkv_dtype dtype, int num_workers, int variant, PrefixSetup* ps) {
+    pkv_status st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype,
+                                 num_workers, variant, &ps->real);
+    if (st != PKV_OK) return st;
+    const int max_gs = resolve_variant(variant) == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
+    const long long group_v = (long long)batch * ps->real.group;
+    if (group_v * n_kv_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    int gs_v = ps->real.gs;
+    for (int k = max_gs / ps->real.gs; k >= 1; --k)
+        if (group_v % (k * ps->real.gs) == 0) {
+            gs_v = k * ps->real.gs;
+            break;
+        }
+    if ((st = setup_decode(1, (int)(group_v * n_kv_heads), n_kv_heads, head_dim, page_size, dtype,
+                           num_workers, variant, &ps->virt, gs_v)) != PKV_OK)
+        return st;
+    // the suffix pass's workspace first: its header is the call's status word
+    const size_t qv_bytes = align256((size_t)batch * n_q_heads * head_dim * 2);
+    ps->s_off = 0;
+    ps->v_off = align256(ps->real.ws.total);
+    ps->qv_off = ps->v_off + align256(ps->virt.ws.total);
+    ps->total = ps->qv_off + qv_bytes;
+    return PKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_decode_prefix_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                              int head_dim, int num_workers,
+                                              pkv_decode_variant variant, size_t* bytes) {
+    if (!bytes) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) {
+        *bytes = 0;
+        return PKV_OK;
+    }
+    PrefixSetup ps;
+    pkv_status st = setup_prefix(batch, n_q_heads, n_kv_heads, head_dim, 16, PKV_BF16,
+                                 num_workers, variant, &ps);
+    if (st != PKV_OK) return st;
+    *bytes = ps.total;
+    return PKV_OK;
+}
+
+pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* page_table, int table_stride,
+                                         const int32_t* context_lens, int batch, int n_q_heads,
+                                         int n_kv_heads, int head_dim, int page_size,
+                                         int num_pages, pkv_dtype dtype, float scale,
+                                         int prefix_tokens, void* out, void* workspace,
+                                         size_t ws_bytes, int num_workers,
+                                         pkv_decode_variant variant, pkv_stream stream) {
+    pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
+                                         context_lens, true, batch, n_q_heads, n_kv_heads,
+                                         head_dim, page_size, num_pages, dtype, scale, out,
+                                         workspace, ws_bytes, num_workers, variant);
+    if (st != PKV_OK || batch == 0) return st;
+    if (prefix_tokens <= 0 || prefix_tokens % page_size ||
+        prefix_tokens / page_size > table_stride)
+        return PKV_ERR_INVALID_ARG;
+    PrefixSetup ps;
+    if ((st = setup_prefix(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           variant, &ps)) != PKV_OK)
+        return st;
+    if (ws_bytes < ps.total) return PKV_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* qv = ws + ps.qv_off;
+    void* ws_v = ws + ps.v_off;
+    void* ws_s = ws + ps.s_off;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const int skip = prefix_tokens / page_size;
+    const int hq_v = (int)((long long)batch * ps.real.group * n_kv_heads);
+    // plans: the prefix (one sequence of prefix_tokens, read through row 0, with
+    // the check that every row starts with row 0's prefix pages) and the
+    // suffixes (each row from column skip on, lengths minus prefix_tokens)
+    if ((st = do_plan(nullptr, page_table, 1, page_size, table_stride, num_workers, ws_v, ps.virt,
+                      nullptr, cs, 0, prefix_tokens)) != PKV_OK)
+        return st;
+    if ((st = do_plan(context_lens, page_table + skip, batch, page_size, table_stride, num_workers,
+                      ws_s, ps.real, nullptr, cs, skip, -1, page_table, batch, skip)) != PKV_OK)
+        return st;
+    uint32_t* call_status = &reinterpret_cast<WsHeader*>(ws_s)->status;
+    if ((st = cuda_status(pkv::launch_gather_q(q, qv, batch, n_kv_heads, ps.real.group, head_dim,
+                                               cs))) != PKV_OK)
+        return st;
+    if ((st = do_run(qv, k_pool, v_pool, page_table, table_stride, 1, hq_v, n_kv_heads, head_dim,
+                     page_size, num_pages, dtype, scale, out, ws_v, ps.virt, false, cs, true,
+                     call_status)) != PKV_OK)
+        return st;
+    if ((st = do_run(q, k_pool, v_pool, page_table + skip, table_stride, batch, n_q_heads,
+                     n_kv_heads, head_dim, page_size, num_pages, dtype, scale, out, ws_s, ps.real,
+                     false, cs, true)) != PKV_OK)
+        return st;
+    uint8_t* wv = static_cast<uint8_t*>(ws_v);
+    uint8_t* wsu = static_cast<uint8_t*>(ws_s);
+    pkv::CascadeArgs c;
+    c.s_partials = reinterpret_cast<const float*>(wsu + ps.real.ws.partials);
+    c.s_prefix = reinterpret_cast<const int32_t*>(wsu + ps.real.ws.prefix);
+    c.s_lens = reinterpret_cast<const int32_t*>(wsu + ps.real.ws.lens_eff);
+    c.s_hdr = reinterpret_cast<const WsHeader*>(wsu);
+    c.v_partials = reinterpret_cast<const float*>(wv + ps.virt.ws.partials);
+    c.v_hdr = reinterpret_cast<const WsHeader*>(wv);
+    c.out = out;
+    c.units_per_b = ps.real.units_per_b;
+    c.sub_groups = ps.real.sub_groups;
+    c.gs = ps.real.gs;
+    c.group = ps.real.group;
+    c.n_q_heads = n_q_heads;
+    c.v_gs = ps.virt.gs;
+    c.v_sub = ps.virt.sub_groups;
+    c.v_nch = (prefix_tokens + 15) / 16;
+    // slots staged per batch: about 48 KiB of shared memory
+    const int slot_bytes = pkv::partial_slot_floats(ps.real.gs, head_dim) * 4;
+    c.merge_batch = (48 * 1024 - pkv::merge_smem_bytes(0, ps.real.gs, head_dim)) / slot_bytes;
+    if (c.merge_batch > 32) c.merge_batch = 32;
+    if (c.merge_batch < 1) c.merge_batch = 1;
+    return cuda_status(pkv::launch_cascade_combine(dtype, head_dim, c, (int)ps.real.units, cs));
 }
 
 }  // extern "C"

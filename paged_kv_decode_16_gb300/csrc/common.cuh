@@ -200,6 +200,8 @@ struct DecodeParams {
     int32_t* unit_done;       // [U] chunks finished per unit (zeroed by the plan); null: split
                               // units are left to the combine kernel
     int merge_batch;          // partial slots merged per batch (fit the warp's stage buffers)
+    int all_partials;         // nonzero: every segment leaves a partial state, out is not written
+                              // (a later merge completes it)
     void* out;                // [B][Hq][D]
     int table_stride;
     int batch, n_q_heads, n_kv_heads, page_size, num_pages;

@@ -310,7 +310,7 @@ decode_kernel(const DecodeParams p) {
 
         const bool seg_end = ws.seg_end(i, d);
         if (seg_end) {
-            const bool whole = seg_whole_start && (d.k == d.nch - 1);
+            const bool whole = seg_whole_start && (d.k == d.nch - 1) && !p.all_partials;
             // tokens were split over the r lanes: sum their o
 #pragma unroll
             for (int g = 0; g < GS; ++g) {

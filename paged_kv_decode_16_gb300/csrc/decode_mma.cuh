@@ -380,7 +380,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
 
         const bool seg_end = ws.seg_end(i, d);
         if (seg_end) {
-            const bool whole = seg_whole_start && (d.k == d.nch - 1);
+            const bool whole = seg_whole_start && (d.k == d.nch - 1) && !p.all_partials;
             const int b = d.u / units_per_b;
             const int uidx = d.u - b * units_per_b;
             const int h = uidx / p.sub_groups;

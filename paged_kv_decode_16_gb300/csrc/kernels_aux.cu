@@ -219,11 +219,21 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
     }
     if (pa.unit_done)
         for (long long x = tid; x < pa.units; x += blockDim.x) pa.unit_done[x] = 0;
+    if (pa.share_table) {  // every row must start with row 0's prefix pages
+        bool differs = false;
+#pragma unroll 4
+        for (long long x = tid; x < (long long)pa.share_rows * pa.share_cols; x += blockDim.x) {
+            const long long r = x / pa.share_cols, c = x - r * pa.share_cols;
+            differs |= __ldg(pa.share_table + r * pa.table_stride + c) != __ldg(pa.share_table + c);
+        }
+        if (differs) atomicOr(&flags, PKV_DEV_BAD_PREFIX);
+    }
     for (int base = 0; base < pa.batch; base += blockDim.x) {
         const int b = base + tid;
         int cnt = 0;
         if (b < pa.batch) {
-            long long L = pa.lens[b];
+            long long L = (long long)(pa.uniform_len >= 0 ? pa.uniform_len : pa.lens[b]) -
+                          pa.len_offset;
             if (L < 0) { L = 0; atomicOr(&flags, PKV_DEV_BAD_LEN); }
             if (L > pa.cap) { L = pa.cap; atomicOr(&flags, PKV_DEV_BAD_LEN); }
             pa.lens_eff[b] = (int32_t)L;
@@ -381,6 +391,136 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
         const int it = k * blockDim.x + tid;
         if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Cascade combine (shared-prefix decode).  The prefix pass ran the shared
+// prefix once per KV head for all B*G query rows (virtual units of gs_v rows,
+// rows in b-major, head-minor order); the suffix pass ran each sequence's own
+// tokens.  Both left only partial states.  One CTA per real unit (sequence,
+// KV head, sub-group of gs rows): its rows sit at rows ro .. ro+gs-1 of one
+// virtual unit (gs divides gs_v).  The prefix segments, then the suffix
+// segments, are staged merge_batch at a time in the real slot layout and
+// folded with merge_weights / merge_accumulate.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+cascade_combine_kernel(CascadeArgs c) {
+    extern __shared__ float4 sbuf4[];
+    const int u = blockIdx.x;
+    const int b = u / c.units_per_b;
+    const int uidx = u - b * c.units_per_b;
+    const int h = uidx / c.sub_groups;
+    const int sgi = uidx - h * c.sub_groups;
+    const int gs = c.gs, tid = threadIdx.x;
+    T* o = static_cast<T*>(c.out) + ((long long)b * c.n_q_heads + h * c.group + sgi * gs) * D;
+    // the prefix side: the virtual unit holding this unit's rows
+    const int r0 = b * c.group + sgi * gs;             // row among head h's B*G rows
+    const int vu = h * c.v_sub + r0 / c.v_gs, ro = r0 % c.v_gs;
+    const UnitSegments pv = unit_segments(c.v_hdr->chunks_per_worker, c.v_hdr->extra_chunks, vu,
+                                          vu * c.v_nch, c.v_nch);
+    const int np = c.v_nch > 0 && c.v_hdr->num_workers > 0 ? pv.count() : 0;
+    // the suffix side: this unit's own segments
+    const int L = c.s_lens[b];
+    const int nch = (L + kChunk - 1) / kChunk;
+    UnitSegments sv{0, 0};
+    if (nch > 0 && c.s_hdr->num_workers > 0)
+        sv = unit_segments(c.s_hdr->chunks_per_worker, c.s_hdr->extra_chunks, u,
+                           c.s_prefix[b] + uidx * nch, nch);
+    const int ns = sv.count();
+    pdl_wait();  // the partial states of both passes are complete from here on
+    pdl_trigger();
+    const int stride = partial_slot_floats(gs, D);
+    const int vstride = partial_slot_floats(c.v_gs, D);
+    const int n = gs * D;
+    constexpr int Q = D / 4;
+    constexpr int KPT = (16 * Q + kCombineWarps * 32 - 1) / (kCombineWarps * 32);
+    float* slots = reinterpret_cast<float*>(sbuf4);
+    MergeHead* heads = reinterpret_cast<MergeHead*>(slots + c.merge_batch * stride);
+    if (tid < gs) heads[tid] = MergeHead{-INFINITY, 0.f, 0.f, 0.f};
+    float4 acc[KPT];
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < np + ns; s0 += c.merge_batch) {
+        const int cnt = min(c.merge_batch, np + ns - s0);
+        __syncthreads();
+        // o rows as 16-byte vectors, then m and l as scalars
+        const int vrow = n / 4;
+        for (int v = tid; v < cnt * vrow; v += blockDim.x) {
+            const int s = v / vrow, e = v - s * vrow;
+            const int g = s0 + s;
+            const float* src = g < np ? c.v_partials + pv.slot(g) * vstride + (long long)ro * D
+                                      : c.s_partials + sv.slot(g - np) * stride;
+            sbuf4[(s * stride) / 4 + e] = __ldcg(reinterpret_cast<const float4*>(src) + e);
+        }
+        for (int v = tid; v < cnt * 2 * gs; v += blockDim.x) {
+            const int s = v / (2 * gs), e = v - s * 2 * gs;  // e < gs: m, else l
+            const int g = s0 + s;
+            float x;
+            if (g < np) {
+                const float* base = c.v_partials + pv.slot(g) * vstride + (long long)c.v_gs * D;
+                x = __ldcg(e < gs ? base + ro + e : base + c.v_gs + ro + (e - gs));
+            } else {
+                x = __ldcg(c.s_partials + sv.slot(g - np) * stride + n + e);
+            }
+            slots[s * stride + n + e] = x;
+        }
+        __syncthreads();
+        if (tid < 32) merge_weights(slots, stride, cnt, gs, D, heads, tid);
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < KPT; ++k) {
+            const int it = k * blockDim.x + tid;
+            if (it < gs * Q) merge_accumulate<D>(slots, stride, cnt, gs, heads, it / Q, it % Q, acc[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+        const int it = k * blockDim.x + tid;
+        if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o);
+    }
+}
+
+__global__ void __launch_bounds__(256)
+gather_q_kernel(const uint4* __restrict__ q, uint4* __restrict__ qv, int batch, int n_kv_heads,
+                int group, int vecs) {
+    pdl_wait();
+    pdl_trigger();
+    const long long total = (long long)batch * n_kv_heads * group * vecs;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int vec = (int)(idx % vecs);
+    const long long row = idx / vecs;  // (h * B + b) * G + g in qv
+    const int g = (int)(row % group);
+    const long long hb = row / group;
+    const int b = (int)(hb % batch), h = (int)(hb / batch);
+    qv[idx] = q[(((long long)b * n_kv_heads + h) * group + g) * vecs + vec];
+}
+
+cudaError_t launch_gather_q(const void* q, void* qv, int batch, int n_kv_heads, int group,
+                            int head_dim, cudaStream_t stream) {
+    const int vecs = head_dim / 8;
+    const long long total = (long long)batch * n_kv_heads * group * vecs;
+    if (total == 0) return cudaSuccess;
+    return launch_pdl(gather_q_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0,
+                      stream, static_cast<const uint4*>(q), static_cast<uint4*>(qv), batch,
+                      n_kv_heads, group, vecs);
+}
+
+cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeArgs& c,
+                                   int units, cudaStream_t stream) {
+    if (units <= 0) return cudaSuccess;
+    const size_t smem = (size_t)merge_smem_bytes(c.merge_batch, c.gs, head_dim);
+#define PKV_CASCADE(T, D) \
+    return launch_pdl(cascade_combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32), smem, \
+                      stream, c)
+    if (dtype == PKV_BF16) {
+        if (head_dim == 128) PKV_CASCADE(__nv_bfloat16, 128);
+        PKV_CASCADE(__nv_bfloat16, 64);
+    }
+    if (head_dim == 128) PKV_CASCADE(__half, 128);
+    PKV_CASCADE(__half, 64);
+#undef PKV_CASCADE
 }
 
 // ---------------------------------------------------------------------------

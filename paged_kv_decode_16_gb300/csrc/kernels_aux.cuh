@@ -11,6 +11,10 @@ namespace pkv {
 
 struct PlanArgs {
     const int32_t* lens;   // [B] context lengths (caller)
+    int len_offset;        // tokens before the decoded range (lengths below it are flagged)
+    int uniform_len;       // >= 0: every sequence has this length and lens is not read
+    const int32_t* share_table;  // nullable: check rows 1 .. share_rows-1 of this table start
+    int share_rows, share_cols;  // with row 0's first share_cols page ids (PKV_DEV_BAD_PREFIX)
     int batch;
     int units_per_b;       // Hkv * sub_groups
     long long cap;         // table_stride * page_size
@@ -59,6 +63,30 @@ cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
 
 // batches up to this size keep their chunk prefix sums in the plan's shared memory
 constexpr int kPlanSmemSeqs = 4096;
+
+// Shared-prefix decode: the partial states of the prefix pass (virtual units
+// of v_gs rows over the shared prefix, v_nch chunks each) and of the suffix
+// pass (the usual units over each sequence's own tokens), merged into out.
+struct CascadeArgs {
+    const float* s_partials;  // suffix pass
+    const int32_t* s_prefix;
+    const int32_t* s_lens;
+    const WsHeader* s_hdr;
+    const float* v_partials;  // prefix pass
+    const WsHeader* v_hdr;
+    void* out;
+    int units_per_b, sub_groups, gs, group, n_q_heads;  // real units
+    int v_gs, v_sub, v_nch;                              // virtual units per KV head, chunks
+    int merge_batch;
+};
+
+// qv[h][b * G + g][:] = q[b][h * G + g][:]: the query rows of each KV head
+// gathered in sequence-major order (the prefix pass's virtual heads).
+cudaError_t launch_gather_q(const void* q, void* qv, int batch, int n_kv_heads, int group,
+                            int head_dim, cudaStream_t stream);
+
+cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeArgs& c,
+                                   int units, cudaStream_t stream);
 
 cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status, cudaStream_t stream);
 
