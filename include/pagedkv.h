@@ -149,6 +149,49 @@ pkv_status kv_pool_info(const pkv_pool* pool, int* num_pages, int* page_size,
                         int* n_kv_heads, int* head_dim, pkv_dtype* dtype);
 
 /* ------------------------------------------------------------------------
+ * Prefix cache: a host radix tree of cached prompt prefixes over the pool
+ * (TorchInferno, "Runtime Scaffolds": runtime.prefix, a radix prefix tree with
+ * prefix-aware lookup, and runtime.prefix_cache; CacheIR, "Current
+ * Capabilities": shared KV page allocator accounting across forked request
+ * sessions).  Page-granular: only whole pages of tokens are cached and
+ * shared, so a sequence's partly filled last page is always its own.  The
+ * cache holds one pool reference per cached page; a match hands the caller
+ * one more reference per matched page (release them with
+ * kv_pool_release_pages when the sequence ends).  Thread-safe; takes the
+ * cache's lock, then the pool's.  Not on the GPU path.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_prefix_cache pkv_prefix_cache; /* opaque */
+
+/* A cache over `pool` (which must outlive it).  *out receives the handle. */
+pkv_status pkv_prefix_cache_create(pkv_pool* pool, pkv_prefix_cache** out);
+
+/* Release every cached page reference and free the cache (NULL: no-op). */
+pkv_status pkv_prefix_cache_destroy(pkv_prefix_cache* cache);
+
+/* Record that the first n_tokens/page_size full pages of `tokens` (host int32
+ * token ids) are stored in pages[0 ..] (host int32 page ids, the sequence's
+ * table row, each held by the caller).  Pages of a prefix already cached are
+ * left as they are (the first insertion wins); new ones gain the cache's
+ * reference.  *n_new (nullable): pages newly cached.  Errors: INVALID_ARG
+ * (page id outside the pool), REFCOUNT (a page that is not allocated). */
+pkv_status pkv_prefix_cache_insert(pkv_prefix_cache* cache, const int32_t* tokens, int n_tokens,
+                                   const int32_t* pages, int* n_new);
+
+/* Longest cached prefix of `tokens` in whole pages, at most max_pages: writes
+ * its page ids to pages_out (host) and their count to *n_pages, and retains
+ * each for the caller.  A new sequence's table row can start with them. */
+pkv_status pkv_prefix_cache_match(pkv_prefix_cache* cache, const int32_t* tokens, int n_tokens,
+                                  int32_t* pages_out, int max_pages, int* n_pages);
+
+/* Free up to n_pages cached pages: least recently used leaves whose page only
+ * the cache still references (a leaf's parent becomes a leaf in turn).
+ * *n_freed (nullable): pages returned to the pool. */
+pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_freed);
+
+/* Pages currently cached (-1 for NULL). */
+int pkv_prefix_cache_pages(const pkv_prefix_cache* cache);
+
+/* ------------------------------------------------------------------------
  * Per-step KV append
  * (TorchInferno, "OpenAI-Compatible Serving" knob list: KV-append kernel;
  *  CacheIR, "Compiler Example": the new K/V are written before the paged

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "PagedKVError", "load_library", "library_path", "pkv_status_string", "pkv_version",
-    "Pool", "kv_pool_create", "kv_append", "kv_append_rope", "kv_gather",
+    "Pool", "kv_pool_create", "PrefixCache", "kv_append", "kv_append_rope", "kv_gather",
     "paged_decode_workspace_size", "paged_decode_step_rope", "paged_decode_attention_prefix",
     "paged_decode_prefix_workspace_size", "alloc_prefix_workspace", "DEV_BAD_PREFIX",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
@@ -80,6 +80,12 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "kv_pool_refcount": ([V, ctypes.c_int32], I),
         "kv_pool_info": ([V, V, V, V, V, V], I),
         "kv_append": ([V, V, V, V, I, V, I, V, V], I),
+        "pkv_prefix_cache_create": ([V, ctypes.POINTER(V)], I),
+        "pkv_prefix_cache_destroy": ([V], I),
+        "pkv_prefix_cache_insert": ([V, V, I, V, ctypes.POINTER(I)], I),
+        "pkv_prefix_cache_match": ([V, V, I, V, I, ctypes.POINTER(I)], I),
+        "pkv_prefix_cache_evict": ([V, I, ctypes.POINTER(I)], I),
+        "pkv_prefix_cache_pages": ([V], I),
         "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, V], I),
         "paged_decode_prefix_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_attention_prefix": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, I, V, V, Z,
@@ -241,6 +247,66 @@ def kv_pool_create(num_pages: int, page_size: int, n_kv_heads: int, head_dim: in
                                          _ptr(k_pool), _ptr(v_pool), ctypes.byref(h)),
            "kv_pool_create")
     return Pool(h.value, k_pool, v_pool, num_pages, page_size, n_kv_heads, head_dim, dtype)
+
+
+class PrefixCache:
+    """Host radix tree of cached prompt prefixes over a pool (whole pages of
+    token ids -> pool pages).  `pool` is a Pool or a raw pool handle; it must
+    outlive the cache.  match() hands the caller one reference per returned
+    page (release them through the pool when the sequence ends)."""
+
+    def __init__(self, pool):
+        self._pool = pool
+        h = pool.handle if isinstance(pool, Pool) else pool
+        self._h = ctypes.c_void_p()
+        _check(load_library().pkv_prefix_cache_create(h, ctypes.byref(self._h)),
+               "pkv_prefix_cache_create")
+
+    @staticmethod
+    def _i32(xs):
+        a = (ctypes.c_int32 * max(len(xs), 1))(*[int(x) for x in xs])
+        return a
+
+    def insert(self, tokens, pages) -> int:
+        """Cache the full pages of `tokens` stored in `pages`; returns how many
+        pages were new to the cache."""
+        n = ctypes.c_int()
+        _check(load_library().pkv_prefix_cache_insert(self._h, self._i32(tokens), len(tokens),
+                                                      self._i32(pages), ctypes.byref(n)),
+               "pkv_prefix_cache_insert")
+        return n.value
+
+    def match(self, tokens, max_pages: int | None = None) -> list[int]:
+        """Pages of the longest cached whole-page prefix of `tokens` (retained
+        for the caller)."""
+        cap = len(tokens) if max_pages is None else int(max_pages)
+        out = (ctypes.c_int32 * max(cap, 1))()
+        n = ctypes.c_int()
+        _check(load_library().pkv_prefix_cache_match(self._h, self._i32(tokens), len(tokens), out,
+                                                     cap, ctypes.byref(n)),
+               "pkv_prefix_cache_match")
+        return list(out[:n.value])
+
+    def evict(self, n_pages: int) -> int:
+        n = ctypes.c_int()
+        _check(load_library().pkv_prefix_cache_evict(self._h, int(n_pages), ctypes.byref(n)),
+               "pkv_prefix_cache_evict")
+        return n.value
+
+    def pages(self) -> int:
+        return load_library().pkv_prefix_cache_pages(self._h)
+
+    def destroy(self) -> None:
+        if self._h:
+            h, self._h = self._h, ctypes.c_void_p(None)
+            _check(load_library().pkv_prefix_cache_destroy(h), "pkv_prefix_cache_destroy")
+
+    def __del__(self):
+        try:
+            if self._h:
+                load_library().pkv_prefix_cache_destroy(self._h)
+        except Exception:
+            pass
 
 
 def kv_append(pool: Pool, k_new: torch.Tensor, v_new: torch.Tensor, page_table: torch.Tensor,

@@ -1,0 +1,218 @@
+// prefix_cache.cpp -- host radix tree of cached prompt prefixes over the page
+// pool (TorchInferno, "Runtime Scaffolds": runtime.prefix, a radix prefix tree
+// with prefix-aware lookup, and runtime.prefix_cache, prefix-cache lookup for
+// reusable entries; CacheIR, "Current Capabilities": shared KV page allocator
+// accounting across forked request sessions).
+//
+// The tree is page-granular: below the root, a node stands for one full page
+// of token ids (page_size of them) following its parent's tokens, and names the
+// pool page that holds their K/V.  A node's children are kept in a hash map by
+// a hash of their tokens, with the tokens compared in full on lookup, so a
+// collision never merges two prefixes.  The cache owns one pool reference per
+// node; a match hands the caller one more reference per matched page, so a
+// page stays allocated while any sequence or the cache uses it.  Eviction
+// removes least-recently-used leaves whose page only the cache still holds.
+#include <stdint.h>
+
+#include <algorithm>
+#include <memory>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "pagedkv.h"
+#include "pool_impl.hpp"
+
+namespace {
+
+struct Node {
+    std::vector<int32_t> tokens;  // the page's token ids (empty at the root)
+    int32_t page = -1;
+    Node* parent = nullptr;
+    uint64_t last_use = 0;
+    std::unordered_map<uint64_t, std::vector<std::unique_ptr<Node>>> children;
+};
+
+// FNV-1a over the bytes of the token ids.
+uint64_t hash_tokens(const int32_t* t, int n) {
+    uint64_t h = 1469598103934665603ull;
+    for (int i = 0; i < n; ++i) {
+        uint32_t v = (uint32_t)t[i];
+        for (int b = 0; b < 4; ++b) {
+            h ^= (v >> (8 * b)) & 0xffu;
+            h *= 1099511628211ull;
+        }
+    }
+    return h;
+}
+
+Node* find_child(Node* n, const int32_t* t, int len, uint64_t h) {
+    auto it = n->children.find(h);
+    if (it == n->children.end()) return nullptr;
+    for (auto& c : it->second)
+        if ((int)c->tokens.size() == len && std::equal(c->tokens.begin(), c->tokens.end(), t))
+            return c.get();
+    return nullptr;
+}
+
+}  // namespace
+
+struct pkv_prefix_cache {
+    pkv_pool* pool = nullptr;
+    int page_size = 0;
+    std::mutex mu;  // guards the tree; taken before the pool's own lock
+    Node root;
+    uint64_t clock = 0;
+    int pages = 0;  // nodes below the root
+};
+
+namespace {
+
+// Release every page below n (children first) and drop the nodes.
+void release_subtree(pkv_prefix_cache* c, Node* n) {
+    for (auto& kv : n->children)
+        for (auto& ch : kv.second) {
+            release_subtree(c, ch.get());
+            kv_pool_release_pages(c->pool, &ch->page, 1);
+            --c->pages;
+        }
+    n->children.clear();
+}
+
+// The least recently used leaf whose page only the cache references.
+Node* lru_evictable_leaf(pkv_prefix_cache* c, Node* n, Node* best) {
+    for (auto& kv : n->children)
+        for (auto& ch : kv.second) {
+            Node* x = ch.get();
+            if (x->children.empty()) {
+                if (kv_pool_refcount(c->pool, x->page) == 1 &&
+                    (!best || x->last_use < best->last_use))
+                    best = x;
+            } else {
+                best = lru_evictable_leaf(c, x, best);
+            }
+        }
+    return best;
+}
+
+void remove_leaf(Node* leaf) {
+    Node* p = leaf->parent;
+    const uint64_t h = hash_tokens(leaf->tokens.data(), (int)leaf->tokens.size());
+    auto it = p->children.find(h);
+    auto& v = it->second;
+    for (size_t i = 0; i < v.size(); ++i)
+        if (v[i].get() == leaf) {
+            v.erase(v.begin() + (long)i);
+            break;
+        }
+    if (v.empty()) p->children.erase(it);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_prefix_cache_create(pkv_pool* pool, pkv_prefix_cache** out) {
+    if (!pool || !out) return PKV_ERR_INVALID_ARG;
+    auto* c = new pkv_prefix_cache;
+    c->pool = pool;
+    c->page_size = pool->page_size;
+    *out = c;
+    return PKV_OK;
+}
+
+pkv_status pkv_prefix_cache_destroy(pkv_prefix_cache* cache) {
+    if (!cache) return PKV_OK;
+    {
+        std::lock_guard<std::mutex> lk(cache->mu);
+        release_subtree(cache, &cache->root);
+    }
+    delete cache;
+    return PKV_OK;
+}
+
+pkv_status pkv_prefix_cache_insert(pkv_prefix_cache* cache, const int32_t* tokens, int n_tokens,
+                                   const int32_t* pages, int* n_new) {
+    if (!cache || n_tokens < 0 || (n_tokens > 0 && (!tokens || !pages)))
+        return PKV_ERR_INVALID_ARG;
+    const int P = cache->page_size;
+    const int full = n_tokens / P;
+    for (int i = 0; i < full; ++i)
+        if (pages[i] < 0 || pages[i] >= cache->pool->num_pages) return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(cache->mu);
+    Node* n = &cache->root;
+    const uint64_t now = ++cache->clock;
+    int added = 0;
+    for (int i = 0; i < full; ++i) {
+        const int32_t* t = tokens + (long long)i * P;
+        const uint64_t h = hash_tokens(t, P);
+        Node* c = find_child(n, t, P, h);
+        if (!c) {
+            // the cache's own reference; the caller must hold the page
+            const pkv_status st = kv_pool_retain_pages(cache->pool, &pages[i], 1);
+            if (st != PKV_OK) return st;
+            auto node = std::make_unique<Node>();
+            node->tokens.assign(t, t + P);
+            node->page = pages[i];
+            node->parent = n;
+            c = node.get();
+            n->children[h].push_back(std::move(node));
+            ++cache->pages;
+            ++added;
+        }
+        c->last_use = now;
+        n = c;
+    }
+    if (n_new) *n_new = added;
+    return PKV_OK;
+}
+
+pkv_status pkv_prefix_cache_match(pkv_prefix_cache* cache, const int32_t* tokens, int n_tokens,
+                                  int32_t* pages_out, int max_pages, int* n_pages) {
+    if (!cache || !n_pages || n_tokens < 0 || max_pages < 0 ||
+        (n_tokens > 0 && !tokens) || (max_pages > 0 && !pages_out))
+        return PKV_ERR_INVALID_ARG;
+    const int P = cache->page_size;
+    std::lock_guard<std::mutex> lk(cache->mu);
+    Node* n = &cache->root;
+    const uint64_t now = ++cache->clock;
+    int k = 0;
+    while (k < max_pages && (long long)(k + 1) * P <= n_tokens) {
+        const int32_t* t = tokens + (long long)k * P;
+        Node* c = find_child(n, t, P, hash_tokens(t, P));
+        if (!c) break;
+        c->last_use = now;
+        pages_out[k++] = c->page;
+        n = c;
+    }
+    // the caller's references to the matched pages
+    const pkv_status st = kv_pool_retain_pages(cache->pool, pages_out, k);
+    if (st != PKV_OK) return st;
+    *n_pages = k;
+    return PKV_OK;
+}
+
+pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_freed) {
+    if (!cache || n_pages < 0) return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(cache->mu);
+    int freed = 0;
+    while (freed < n_pages) {
+        Node* leaf = lru_evictable_leaf(cache, &cache->root, nullptr);
+        if (!leaf) break;
+        const pkv_status st = kv_pool_release_pages(cache->pool, &leaf->page, 1);
+        if (st != PKV_OK) return st;
+        remove_leaf(leaf);
+        --cache->pages;
+        ++freed;
+    }
+    if (n_freed) *n_freed = freed;
+    return PKV_OK;
+}
+
+int pkv_prefix_cache_pages(const pkv_prefix_cache* cache) {
+    if (!cache) return -1;
+    std::lock_guard<std::mutex> lk(const_cast<pkv_prefix_cache*>(cache)->mu);
+    return cache->pages;
+}
+
+}  // extern "C"
