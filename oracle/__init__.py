@@ -78,6 +78,9 @@ class Oracle:
         lib.pkv_oracle_gather.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, i32, P]
         lib.pkv_oracle_set_threads.argtypes = [i32]
         lib.pkv_oracle_encode_array.argtypes = [P, ctypes.c_int64, i32, P]
+        lib.pkv_oracle_paged_decode_multi.argtypes = [P, P, P, i32, P, i32, P, i32, i32, i32, i32,
+                                                      i32, i32, i32, ctypes.c_double, P]
+        lib.pkv_oracle_paged_decode_multi.restype = ctypes.c_int
         lib.pkv_oracle_rope.argtypes = [P, P, i32, i32, i32, ctypes.c_double, i32, P, P]
         for name in ("pkv_oracle_encode_array", "pkv_oracle_rope"):
             getattr(lib, name).restype = ctypes.c_int
@@ -122,6 +125,25 @@ class Oracle:
                                               _ptr(table), table.shape[1], _ptr(lens), B, Hq, Hkv,
                                               D, P, NP, float(scale), _ptr(out))
         _check(rc, "paged_decode")
+        return out
+
+    def paged_decode_multi(self, q, k_pool, v_pool, page_table, context_lens, scale: float,
+                           dtype: str) -> np.ndarray:
+        """Several query tokens per sequence: q [B, Qn, Hq, D]; query j of sequence
+        b stands at position L_b - Qn + j and attends causally to tokens
+        0 .. L_b - Qn + j.  Returns float64 [B, Qn, Hq, D]."""
+        q, k_pool, v_pool = _u16(q), _u16(k_pool), _u16(v_pool)
+        table, lens = _i32(page_table), _i32(context_lens)
+        B, Qn, Hq, D = q.shape
+        NP, Hkv, P, D2 = k_pool.shape
+        if D2 != D or v_pool.shape != k_pool.shape or table.ndim != 2 or table.shape[0] != B:
+            raise ValueError("shape mismatch")
+        out = np.zeros((B, Qn, Hq, D), dtype=np.float64)
+        rc = self.lib.pkv_oracle_paged_decode_multi(_ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                                    DTYPES[dtype], _ptr(table), table.shape[1],
+                                                    _ptr(lens), B, Qn, Hq, Hkv, D, P, NP,
+                                                    float(scale), _ptr(out))
+        _check(rc, "paged_decode_multi")
         return out
 
     def paged_decode_rows(self, q, k_pool, v_pool, page_table, context_lens, scale: float,
@@ -224,6 +246,10 @@ def paged_decode_rows(*a, **k) -> np.ndarray:
 
 def kv_append(*a, **k):
     return get().kv_append(*a, **k)
+
+
+def paged_decode_multi(*a, **k) -> np.ndarray:
+    return get().paged_decode_multi(*a, **k)
 
 
 def encode(*a, **k) -> np.ndarray:

@@ -213,20 +213,24 @@ static int check_decode_args(const decode_args* a) {
 }
 
 /* One output row: sequence b, query head hq.  out_row has head_dim doubles. */
-static int decode_row(const decode_args* a, int b, int hq, double* out_row) {
+/* One output row: query row qsel (NULL: row (b, hq) of a->q) of sequence b
+ * over the first n_att of its tokens (n_att < 0: all of them). */
+static int decode_row_at(const decode_args* a, int b, int hq, const uint16_t* qsel, int n_att,
+                         double* out_row) {
     const int D = a->head_dim, P = a->page_size;
     const int group = a->n_q_heads / a->n_kv_heads;
     const int hkv = hq / group; /* consecutive query heads share a KV head */
-    const int L = a->lens[b];
+    const int Lseq = a->lens[b];
     for (int d = 0; d < D; ++d) out_row[d] = 0.0;
-    if (L < 0) return ORC_BAD_LEN;
-    if (L == 0) return ORC_OK;
-    if ((int64_t)L > (int64_t)a->table_stride * P) return ORC_BAD_LEN;
+    if (Lseq < 0) return ORC_BAD_LEN;
+    if ((int64_t)Lseq > (int64_t)a->table_stride * P) return ORC_BAD_LEN;
+    const int L = n_att < 0 ? Lseq : (n_att < Lseq ? n_att : Lseq);  /* tokens attended */
+    if (L <= 0) return ORC_OK;
 
     double* qd = (double*)malloc(sizeof(double) * (size_t)D);
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
     if (!qd || !s) { free(qd); free(s); return ORC_INVALID; }
-    const uint16_t* qrow = a->q + ((int64_t)b * a->n_q_heads + hq) * D;
+    const uint16_t* qrow = qsel ? qsel : a->q + ((int64_t)b * a->n_q_heads + hq) * D;
     for (int d = 0; d < D; ++d) qd[d] = pkv_oracle_decode_bits(qrow[d], a->dtype);
 
     int rc = ORC_OK;
@@ -259,6 +263,45 @@ static int decode_row(const decode_args* a, int b, int hq, double* out_row) {
     free(qd);
     free(s);
     return rc;
+}
+
+static int decode_row(const decode_args* a, int b, int hq, double* out_row) {
+    return decode_row_at(a, b, hq, NULL, -1, out_row);
+}
+
+/*
+ * Several query tokens per sequence (speculative or suffix decoding).  The
+ * n_queries new tokens of sequence b are its last ones, so query j stands at
+ * position L - n_queries + j and, causally, attends to tokens
+ * t = 0 .. L - n_queries + j (its own and every earlier one).
+ * q and out [batch][n_queries][n_q_heads][head_dim].  A query with no token
+ * to attend to (L < n_queries - j) gives zeros.
+ */
+int pkv_oracle_paged_decode_multi(const uint16_t* q, const uint16_t* k_pool,
+                                  const uint16_t* v_pool, int dtype, const int32_t* table,
+                                  int table_stride, const int32_t* lens, int batch, int n_queries,
+                                  int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                                  int num_pages, double scale, double* out) {
+    decode_args a = {q, k_pool, v_pool, dtype, table, table_stride, lens, batch, n_q_heads,
+                     n_kv_heads, head_dim, page_size, num_pages, scale};
+    int rc = check_decode_args(&a);
+    if (rc != ORC_OK || !out || n_queries <= 0) return rc != ORC_OK ? rc : ORC_INVALID;
+    const int64_t rows = (int64_t)batch * n_queries * n_q_heads;
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < rows; ++r) {
+        const int hq = (int)(r % n_q_heads);
+        const int j = (int)((r / n_q_heads) % n_queries);
+        const int b = (int)(r / ((int64_t)n_q_heads * n_queries));
+        const uint16_t* qsel = q + r * head_dim;  /* row (b, j, hq) */
+        const int n_att = lens[b] - n_queries + j + 1;
+        const int e = decode_row_at(&a, b, hq, qsel, n_att, out + r * head_dim);
+        if (e != ORC_OK) {
+#pragma omp critical
+            err = e;
+        }
+    }
+    return err;
 }
 
 /*

@@ -437,6 +437,71 @@ def check_rope_rounds_its_float64_result(orc):
             assert np.array_equal(out, y.astype(np.float16).view(np.uint16))
 
 
+
+
+# ---- several query tokens per sequence (speculative / suffix decoding) ----
+
+def _dense_kv(orc, w):
+    """Dense float64 K/V [B][Hkv][Lmax][D] through the library-independent gather."""
+    kb, vb = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
+    Lmax = int(max(w.context_lens))
+    kd = orc.decode_bits(orc.gather(kb, w.page_table, w.context_lens, Lmax), w.dtype_name)
+    vd = orc.decode_bits(orc.gather(vb, w.page_table, w.context_lens, Lmax), w.dtype_name)
+    return kd, vd
+
+
+def check_multi_query_vs_causal_sdpa(orc):
+    """Each query token j attends to tokens 0 .. L - Qn + j: torch
+    scaled_dot_product_attention in float64 with that causal mask on the dense
+    cache, GQA by repeating KV heads."""
+    rng = np.random.default_rng(21)
+    for dt, Qn in (("bf16", 4), ("f16", 3)):
+        w = wl.make_random(21, batch=3, n_q_heads=8, n_kv_heads=2, head_dim=64, page_size=16,
+                           dtype=TORCH_DT[dt], lens=[5, 40, 70])
+        q = _rand_bits(rng, (3, Qn, 8, 64), dt)
+        got = orc.paged_decode_multi(q, wl.to_bits(w.k_pool), wl.to_bits(w.v_pool), w.page_table,
+                                     w.context_lens, w.scale, dt)
+        kd, vd = _dense_kv(orc, w)
+        qv = orc.decode_bits(q, dt)
+        for b in range(3):
+            L = int(w.context_lens[b])
+            k = torch.from_numpy(np.repeat(kd[b, :, :L], 4, axis=0))    # [Hq][L][D]
+            v = torch.from_numpy(np.repeat(vd[b, :, :L], 4, axis=0))
+            qq = torch.from_numpy(qv[b].transpose(1, 0, 2).copy())     # [Hq][Qn][D]
+            pos = torch.arange(L)
+            mask = pos[None, :] <= (L - Qn + torch.arange(Qn))[:, None]  # [Qn][L]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qq, k, v, attn_mask=mask, scale=w.scale).numpy()        # [Hq][Qn][D]
+            ref = np.nan_to_num(ref.transpose(1, 0, 2))                 # rows with no token: 0
+            assert np.allclose(got[b], ref, rtol=1e-10, atol=1e-12), (dt, b)
+
+
+def check_multi_query_single_token_and_causality(orc):
+    """Qn = 1 is the plain decode; tokens after query j's position do not change
+    row j but do change the last row."""
+    rng = np.random.default_rng(22)
+    dt = "bf16"
+    w = wl.make_random(22, batch=2, n_q_heads=4, n_kv_heads=2, head_dim=64, page_size=16,
+                       dtype=torch.bfloat16, lens=[33, 50])
+    kb, vb = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
+    q1 = wl.to_bits(w.q)
+    one = orc.paged_decode_multi(q1[:, None], kb, vb, w.page_table, w.context_lens, w.scale, dt)
+    assert np.array_equal(one[:, 0], orc.paged_decode(q1, kb, vb, w.page_table, w.context_lens,
+                                                      w.scale, dt))
+    Qn = 5
+    q = _rand_bits(rng, (2, Qn, 4, 64), dt)
+    base = orc.paged_decode_multi(q, kb, vb, w.page_table, w.context_lens, w.scale, dt)
+    L = int(w.context_lens[1])
+    t = L - 2                                   # seen by queries 3 and 4 only
+    page, slot = w.page_table[1, t // 16], t % 16
+    kb2 = kb.copy()
+    kb2[page, :, slot, :] = _rand_bits(rng, (2, 64), dt)
+    moved = orc.paged_decode_multi(q, kb2, vb, w.page_table, w.context_lens, w.scale, dt)
+    assert np.array_equal(moved[1, :3], base[1, :3])
+    assert not np.allclose(moved[1, 3:], base[1, 3:])
+    assert np.array_equal(moved[0], base[0])
+
+
 ALL_CHECKS = [
     check_decode_f16_all_patterns,
     check_decode_bf16_all_patterns,
@@ -456,4 +521,6 @@ ALL_CHECKS = [
     check_rope_one_hot_closed_form,
     check_rope_is_a_rotation,
     check_rope_rounds_its_float64_result,
+    check_multi_query_vs_causal_sdpa,
+    check_multi_query_single_token_and_causality,
 ]

@@ -51,6 +51,10 @@ MUTATIONS = [
     ("encode_no_carry", "if (r == ldexp(1.0, mbits + 1)) {", "if (r == ldexp(1.0, mbits + 2)) {"),
     ("encode_subnormal_spacing", "nearbyint(ldexp(a, mbits - emin))",
      "nearbyint(ldexp(a, mbits - emin + 1))"),
+    ("multi_query_causal_off_by_one", "const int n_att = lens[b] - n_queries + j + 1;",
+     "const int n_att = lens[b] - n_queries + j;"),
+    ("multi_query_sees_all_tokens", "const int n_att = lens[b] - n_queries + j + 1;",
+     "const int n_att = lens[b];"),
 ]
 
 RUNNER = textwrap.dedent("""
