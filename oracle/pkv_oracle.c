@@ -295,7 +295,8 @@ int pkv_oracle_paged_decode_multi(const uint16_t* q, const uint16_t* k_pool,
         const int b = (int)(r / ((int64_t)n_q_heads * n_queries));
         const uint16_t* qsel = q + r * head_dim;  /* row (b, j, hq) */
         const int n_att = lens[b] - n_queries + j + 1;
-        const int e = decode_row_at(&a, b, hq, qsel, n_att, out + r * head_dim);
+        /* before the first token (n_att <= 0) the query sees nothing: zeros */
+        const int e = decode_row_at(&a, b, hq, qsel, n_att > 0 ? n_att : 0, out + r * head_dim);
         if (e != ORC_OK) {
 #pragma omp critical
             err = e;

@@ -55,6 +55,8 @@ MUTATIONS = [
      "const int n_att = lens[b] - n_queries + j;"),
     ("multi_query_sees_all_tokens", "const int n_att = lens[b] - n_queries + j + 1;",
      "const int n_att = lens[b];"),
+    ("multi_query_early_row_sees_all", "n_att > 0 ? n_att : 0, out + r * head_dim",
+     "n_att, out + r * head_dim"),
 ]
 
 RUNNER = textwrap.dedent("""
