@@ -457,6 +457,31 @@ def run_ours(args):
     pby = step_bytes(wp)
     del wp, tp, lp, op, wsp, wsp_plain
 
+    # ---- several query tokens per sequence (four draft tokens, causal) on the
+    # step's own cache, against the one-query decode of the same batch ----
+    QN = 4
+    multi = None
+    if var != pkv.VARIANT_CUDA_CORES:
+        gq = torch.Generator(device=dev).manual_seed(args.seed + 1)
+        qm = torch.randn(B, QN, w.n_q_heads, w.head_dim, generator=gq, device=dev,
+                         dtype=torch.float32).to(w.dtype)
+        om = torch.empty_like(qm)
+        wsm = pkv.alloc_multi_workspace(B, QN, w.n_q_heads, w.n_kv_heads, w.head_dim, nw,
+                                        device=dev, variant=var)
+        multi_ms = timed_loop(lambda: pkv.paged_decode_attention_multi(
+            qm, w.k_pool, w.v_pool, table, lens, w.scale, om, wsm, nw, variant=var), KP)
+        one_ms = timed_loop(lambda: pkv.paged_decode_attention(
+            w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws, nw, variant=var), KP)
+        mbytes = by["kv_unique"] + QN * by["qo"]
+        multi = {"what": f"paged_decode_attention_multi with {QN} causal query tokens per "
+                         "sequence (each K/V chunk read once for all of them) vs "
+                         "paged_decode_attention with one, same cache",
+                 "n_queries": QN, "ms_multi": multi_ms, "ms_one_query": one_ms, "steps": KP,
+                 "gbs_multi": mbytes / (multi_ms * 1e-3) / 1e9,
+                 "tokens_per_s_multi": B * QN / (multi_ms * 1e-3),
+                 "tokens_per_s_one_query": B / (one_ms * 1e-3)}
+        del qm, om, wsm
+
     # ---- the decode kernel alone: events around its launch on its stream ----
     KD = max(1, min(K, 2000))
     dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
@@ -576,6 +601,7 @@ def run_ours(args):
             "gbs_unique_prefix": (pby["kv_unique"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
             "gbs_logical_prefix": (pby["kv_logical"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
             "gbs_logical_plain": (pby["kv_logical"] + pby["qo"]) / (plain_ms * 1e-3) / 1e9},
+        "multi_query": multi,
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "device_status": status,

@@ -404,6 +404,37 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
                                          pkv_decode_variant variant, pkv_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Several query tokens per sequence (speculative or suffix decoding).
+ * (Experimental LibTorch prefix cache, "Current execution limits": causal
+ * suffix queries of a request, from one up to 64, attended in tiles of 16
+ * queries per warp.)
+ *
+ * q and out [batch][n_queries][n_q_heads][head_dim]; the n_queries new tokens
+ * of sequence b are its last ones (already in the cache), so query j stands at
+ * position context_lens[b] - n_queries + j and attends causally to tokens
+ * 0 .. context_lens[b] - n_queries + j; a query with no such token (when
+ * context_lens[b] < n_queries - j) gives zeros.  A unit of work is one m16
+ * tile of query rows: the queries are cut into the fewest tiles of at most 16
+ * tokens (equal sizes but the last), and a tile of t tokens takes the most
+ * heads h of the GQA group with t * h <= 16; every K/V chunk of a KV head is
+ * read once per (tile, head block).  1 <= n_queries <= 64 (else UNSUPPORTED);
+ * tensor-core variant only (CUDA_CORES: UNSUPPORTED).  n_queries = 1 is
+ * paged_decode_attention.  Three launches.
+ * ------------------------------------------------------------------------ */
+pkv_status paged_decode_multi_workspace_size(int batch, int n_queries, int n_q_heads,
+                                             int n_kv_heads, int head_dim, int num_workers,
+                                             pkv_decode_variant variant, size_t* bytes);
+
+pkv_status paged_decode_attention_multi(const void* q, const void* k_pool, const void* v_pool,
+                                        const int32_t* page_table, int table_stride,
+                                        const int32_t* context_lens, int batch, int n_queries,
+                                        int n_q_heads, int n_kv_heads, int head_dim,
+                                        int page_size, int num_pages, pkv_dtype dtype,
+                                        float scale, void* out, void* workspace, size_t ws_bytes,
+                                        int num_workers, pkv_decode_variant variant,
+                                        pkv_stream stream);
+
+/* ------------------------------------------------------------------------
  * Decode without a caller-provided workspace.
  * (No counterpart on the source pages: an addition of this library.)
  *

@@ -23,6 +23,7 @@ __all__ = [
     "Pool", "kv_pool_create", "PrefixCache", "kv_append", "kv_append_rope", "kv_gather",
     "paged_decode_workspace_size", "paged_decode_step_rope", "paged_decode_attention_prefix",
     "paged_decode_prefix_workspace_size", "alloc_prefix_workspace", "DEV_BAD_PREFIX",
+    "paged_decode_attention_multi", "paged_decode_multi_workspace_size", "alloc_multi_workspace",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
@@ -88,6 +89,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "pkv_prefix_cache_pages": ([V], I),
         "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, V], I),
         "paged_decode_prefix_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
+        "paged_decode_multi_workspace_size": ([I, I, I, I, I, I, I, ctypes.POINTER(Z)], I),
+        "paged_decode_attention_multi": ([V, V, V, V, I, V, I, I, I, I, I, I, I, I, F, V, V, Z, I,
+                                          I, V], I),
         "paged_decode_attention_prefix": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, I, V, V, Z,
                                            I, I, V], I),
         "paged_decode_step_rope": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F,
@@ -440,6 +444,51 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
         _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out), int(num_workers),
         int(variant), _stream(stream)),
         "paged_decode_attention_no_alloc")
+    return out
+
+
+def paged_decode_multi_workspace_size(batch: int, n_queries: int, n_q_heads: int,
+                                      n_kv_heads: int, head_dim: int, num_workers: int = 0,
+                                      variant: int = VARIANT_AUTO) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().paged_decode_multi_workspace_size(
+        batch, n_queries, n_q_heads, n_kv_heads, head_dim, int(num_workers), int(variant),
+        ctypes.byref(n)), "paged_decode_multi_workspace_size")
+    return n.value
+
+
+def alloc_multi_workspace(batch: int, n_queries: int, n_q_heads: int, n_kv_heads: int,
+                          head_dim: int, num_workers: int = 0, device=None,
+                          variant: int = VARIANT_AUTO) -> torch.Tensor:
+    n = paged_decode_multi_workspace_size(batch, n_queries, n_q_heads, n_kv_heads, head_dim,
+                                          num_workers, variant)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_attention_multi(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                 page_table: torch.Tensor, context_lens: torch.Tensor,
+                                 scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                                 num_workers: int = 0, stream=None,
+                                 variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """q, out [B, Qn, Hq, D]: query j of sequence b attends causally to tokens
+    0 .. context_lens[b] - Qn + j."""
+    _dev(q, "q", None, 4)
+    dt = _dtype_code(q)
+    _dev(out, "out", q.dtype, 4)
+    _dev(k_pool, "k_pool", q.dtype, 4)
+    _dev(v_pool, "v_pool", q.dtype, 4)
+    _dev(page_table, "page_table", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8)
+    B, Qn, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or out.shape != q.shape or page_table.shape[0] != B:
+        raise ValueError("q/out [B, Qn, Hq, D], pools [NP, Hkv, P, D] and table disagree")
+    _check(load_library().paged_decode_attention_multi(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), page_table.shape[1],
+        _ptr(context_lens), B, Qn, Hq, Hkv, D, P, NP, dt, float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), int(num_workers), int(variant), _stream(stream)),
+        "paged_decode_attention_multi")
     return out
 
 

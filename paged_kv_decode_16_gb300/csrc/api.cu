@@ -166,7 +166,11 @@ struct DecodeSetup {
     KernelPick kernel;
     WsLayout ws;
     int merge_batch;   // partial slots per merge batch: as many as a warp's stage buffers hold
+    pkv::RowShape rs{};  // the query rows of each unit
 };
+
+// Query tokens per sequence that paged_decode_attention_multi takes.
+constexpr int kMaxQueries = 64;
 
 // AUTO picks the tensor-core kernel; CUDA cores on request.
 int resolve_variant(int variant) {
@@ -175,7 +179,7 @@ int resolve_variant(int variant) {
 
 pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                         pkv_dtype dtype, int num_workers, int variant, DecodeSetup* s,
-                        int force_gs = 0) {
+                        int force_gs = 0, int n_queries = 1) {
     pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, page_size);
     if (st != PKV_OK) return st;
     if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
@@ -183,13 +187,27 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     const int v = resolve_variant(variant);
     s->group = n_q_heads / n_kv_heads;
     const int max_gs = v == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
-    if (force_gs > 0) {  // a sub-group size chosen by the caller (divides the group)
+    if (n_queries > 1) {
+        // rows of a unit (one m16 tile): the queries split into the fewest
+        // tiles of at most 16 tokens, of equal size but the last, times the
+        // most heads of the group that still fit 16 rows
+        if (v != PKV_VARIANT_TENSOR_CORES || n_queries > kMaxQueries) return PKV_ERR_UNSUPPORTED;
+        const int qpu = (n_queries + (n_queries + 15) / 16 - 1) / ((n_queries + 15) / 16);
+        const int tiles = (n_queries + qpu - 1) / qpu;
+        int hpu = 1;
+        for (int d = 1; d <= s->group; ++d)
+            if (s->group % d == 0 && qpu * d <= 16) hpu = d;
+        s->gs = qpu * hpu;
+        s->sub_groups = (s->group / hpu) * tiles;
+        s->rs = pkv::RowShape{n_queries, qpu, hpu, s->group / hpu, s->group, n_q_heads};
+    } else if (force_gs > 0) {  // a sub-group size chosen by the caller (divides the group)
         if (force_gs > max_gs || s->group % force_gs) return PKV_ERR_UNSUPPORTED;
         s->gs = force_gs;
         s->sub_groups = s->group / force_gs;
     } else if (!split_group(s->group, max_gs, &s->sub_groups, &s->gs)) {
         return PKV_ERR_UNSUPPORTED;
     }
+    if (n_queries <= 1) s->rs = pkv::RowShape{1, 1, s->gs, s->sub_groups, s->group, n_q_heads};
     s->units_per_b = n_kv_heads * s->sub_groups;
     s->units = (long long)batch * s->units_per_b;
     s->kernel = pick_kernel(dtype, head_dim, v, s->gs);
@@ -327,6 +345,7 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.unit_done = merge ? reinterpret_cast<int32_t*>(ws + s.ws.unit_done) : nullptr;
     p.merge_batch = s.merge_batch;
     p.all_partials = all_partials ? 1 : 0;
+    p.rows = s.rs;
     p.out = out;
     p.table_stride = table_stride;
     p.batch = batch;
@@ -361,8 +380,7 @@ pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, v
         dtype, head_dim, reinterpret_cast<const float*>(ws + s.ws.partials),
         reinterpret_cast<const int32_t*>(ws + s.ws.prefix),
         reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<const WsHeader*>(ws),
-        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.group, n_q_heads, s.merge_batch,
-        stream));
+        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.merge_batch, s.rs, stream));
 }
 
 // --- fixed device scratch for paged_decode_attention_no_alloc -------------
@@ -931,6 +949,63 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
     if (c.merge_batch > 32) c.merge_batch = 32;
     if (c.merge_batch < 1) c.merge_batch = 1;
     return cuda_status(pkv::launch_cascade_combine(dtype, head_dim, c, (int)ps.real.units, cs));
+}
+
+}  // extern "C"
+
+// --- several query tokens per sequence --------------------------------------
+extern "C" {
+
+pkv_status paged_decode_multi_workspace_size(int batch, int n_queries, int n_q_heads,
+                                             int n_kv_heads, int head_dim, int num_workers,
+                                             pkv_decode_variant variant, size_t* bytes) {
+    if (!bytes) return PKV_ERR_INVALID_ARG;
+    *bytes = 0;
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, 16);
+    if (st != PKV_OK) return st;
+    if (num_workers < 0 || !valid_variant(variant) || n_queries < 1) return PKV_ERR_INVALID_ARG;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, PKV_BF16, num_workers,
+                           variant, &s, 0, n_queries)) != PKV_OK)
+        return st;
+    *bytes = s.ws.total;
+    return PKV_OK;
+}
+
+pkv_status paged_decode_attention_multi(const void* q, const void* k_pool, const void* v_pool,
+                                        const int32_t* page_table, int table_stride,
+                                        const int32_t* context_lens, int batch, int n_queries,
+                                        int n_q_heads, int n_kv_heads, int head_dim,
+                                        int page_size, int num_pages, pkv_dtype dtype,
+                                        float scale, void* out, void* workspace, size_t ws_bytes,
+                                        int num_workers, pkv_decode_variant variant,
+                                        pkv_stream stream) {
+    if (n_queries < 1) return PKV_ERR_INVALID_ARG;
+    pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
+                                         context_lens, true, batch, n_q_heads, n_kv_heads,
+                                         head_dim, page_size, num_pages, dtype, scale, out,
+                                         workspace, ws_bytes, num_workers, variant);
+    if (st != PKV_OK || batch == 0) return st;
+    // q and out hold n_queries rows per sequence: check the full extents
+    const size_t qo = (size_t)batch * n_queries * n_q_heads * head_dim * 2;
+    const size_t pool_bytes = (size_t)num_pages * n_kv_heads * page_size * head_dim * 2;
+    if (overlaps(out, qo, q, qo) || overlaps(out, qo, k_pool, pool_bytes) ||
+        overlaps(out, qo, v_pool, pool_bytes) || overlaps(out, qo, workspace, ws_bytes))
+        return PKV_ERR_ALIAS;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           variant, &s, 0, n_queries)) != PKV_OK)
+        return st;
+    if ((st = check_workspace(workspace, ws_bytes, s)) != PKV_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = do_plan(context_lens, page_table, batch, page_size, table_stride, num_workers,
+                      workspace, s, nullptr, cs)) != PKV_OK)
+        return st;
+    if ((st = do_run(q, k_pool, v_pool, page_table, table_stride, batch, n_q_heads, n_kv_heads,
+                     head_dim, page_size, num_pages, dtype, scale, out, workspace, s, false,
+                     cs)) != PKV_OK)
+        return st;
+    return do_combine(batch, n_q_heads, head_dim, dtype, out, workspace, s, cs);
 }
 
 }  // extern "C"

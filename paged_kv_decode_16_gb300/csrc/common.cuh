@@ -44,6 +44,39 @@ __host__ __device__ __forceinline__ int worker_of(int f, int sw, int r) {
     return f < big ? f / (sw + 1) : r + (f - big) / sw;
 }
 
+// Query rows of the units.  Unit (b, KV head h, sub-group sg) holds rows
+// r = 0 .. rows(sg) - 1; sub-group sg = tile * head_blocks + block picks one
+// tile of queries_per_unit query tokens (the last tile may be shorter) and one
+// block of heads_per_unit query heads of the GQA group; row r is token
+// first_query(sg) + r / heads_per_unit of query head
+// h * group + block * heads_per_unit + r % heads_per_unit.  One query per
+// sequence: a single tile of one token, every row of a unit in use.
+struct RowShape {
+    int n_queries;         // query tokens per sequence: q, out [B][n_queries][Hq][D]
+    int queries_per_unit;  // tokens of a full query tile
+    int heads_per_unit;    // query heads of a head block
+    int head_blocks;       // group / heads_per_unit
+    int group, n_q_heads;
+
+    __host__ __device__ __forceinline__ int first_query(int sg) const {
+        return (sg / head_blocks) * queries_per_unit;
+    }
+    __host__ __device__ __forceinline__ int rows(int sg) const {
+        const int n = n_queries - first_query(sg);
+        return (n < queries_per_unit ? n : queries_per_unit) * heads_per_unit;
+    }
+    __host__ __device__ __forceinline__ int query(int sg, int r) const {
+        return first_query(sg) + r / heads_per_unit;
+    }
+    // row r of unit (b, h, sg) as a row of q / out
+    __host__ __device__ __forceinline__ long long row(int b, int h, int sg, int r) const {
+        const int t = sg / head_blocks, blk = sg - t * head_blocks;
+        const int jl = r / heads_per_unit, g = r - jl * heads_per_unit;
+        return ((long long)b * n_queries + t * queries_per_unit + jl) * n_q_heads + h * group +
+               blk * heads_per_unit + g;
+    }
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -202,11 +235,12 @@ struct DecodeParams {
     int merge_batch;          // partial slots merged per batch (fit the warp's stage buffers)
     int all_partials;         // nonzero: every segment leaves a partial state, out is not written
                               // (a later merge completes it)
-    void* out;                // [B][Hq][D]
+    RowShape rows;            // the query rows of each unit
+    void* out;                // [B][n_queries][Hq][D]
     int table_stride;
     int batch, n_q_heads, n_kv_heads, page_size, num_pages;
     int group;                // G = Hq / Hkv
-    int sub_groups;           // units per KV head (G = sub_groups * GS)
+    int sub_groups;           // units per KV head (query tiles x head blocks)
     float scale_log2;         // scale * log2(e)
 };
 

@@ -177,8 +177,13 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         const bool seg_start = ws.seg_start(j, d);
         if (lane == 0) {
             const int st = j % STAGES;
+            const int b = d.u / units_per_b;
+            const int uidx = d.u - b * units_per_b;
+            const int h = uidx / p.sub_groups;
+            const int sg = uidx - h * p.sub_groups;
+            const int nrows = p.rows.rows(sg);
             const uint32_t kv_bytes = d.off >= 0 ? (uint32_t)Lay::kStageBytes : 0u;
-            const uint32_t q_bytes = seg_start ? (uint32_t)Lay::kQBytes : 0u;
+            const uint32_t q_bytes = seg_start ? (uint32_t)(nrows * D * 2) : 0u;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bar[st], kv_bytes + q_bytes);
             if (kv_bytes) {
@@ -192,12 +197,11 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 }
             }
             if (q_bytes) {
-                const int b = d.u / units_per_b;
-                const int uidx = d.u - b * units_per_b;
-                const int h = uidx / p.sub_groups;
-                const int sg = uidx - h * p.sub_groups;
-                const long long qrow = (long long)b * p.n_q_heads + h * p.group + sg * GS;
-                bulk_g2s(sq + st * GS * D, qg + qrow * D, q_bytes, &bar[st]);
+                // the unit's rows: one block of heads_per_unit contiguous q rows per token
+                const int hpu = p.rows.heads_per_unit;
+                for (int r = 0; r < nrows; r += hpu)
+                    bulk_g2s(sq + st * GS * D + r * D, qg + p.rows.row(b, h, sg, r) * D,
+                             (uint32_t)(hpu * D * 2), &bar[st]);
             }
         }
         return true;
@@ -212,6 +216,8 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
     float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
     bool seg_whole_start = false;
     int seg_slot = 0, seg_first = 0;
+    int seg_rows = GS;              // rows of the segment's unit in use
+    int jq_lo = 0, jq_hi = 0;       // query tokens of rows g_lo and g_lo + 8
     // split segments to report after the loop (at most two: the range's first and last)
     int npend = 0;
     PendingMerge pend0 = {0, 0, 0, 0}, pend1 = {0, 0, 0, 0};
@@ -232,16 +238,22 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         if (seg_start) {
             seg_slot = ws.slot_base + d.u;
             seg_first = i;
+            {
+                const int sg = (d.u % units_per_b) % p.sub_groups;
+                seg_rows = p.rows.rows(sg);
+                jq_lo = p.rows.query(sg, g_lo);
+                jq_hi = p.rows.query(sg, g_lo + 8);
+            }
             // A fragments of Q: a0 (row g, k tq..tq+1), a1 (row g+8), a2 (k+8), a3
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(sq + st * GS * D);
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int c0 = (kk * 16 + tq) / 2, c1 = (kk * 16 + 8 + tq) / 2;
-                qa[kk][0] = g_lo < GS ? q32[g_lo * (D / 2) + c0] : 0u;
-                qa[kk][2] = g_lo < GS ? q32[g_lo * (D / 2) + c1] : 0u;
+                qa[kk][0] = g_lo < seg_rows ? q32[g_lo * (D / 2) + c0] : 0u;
+                qa[kk][2] = g_lo < seg_rows ? q32[g_lo * (D / 2) + c1] : 0u;
                 if constexpr (kTwoHalves) {
-                    qa[kk][1] = g_lo + 8 < GS ? q32[(g_lo + 8) * (D / 2) + c0] : 0u;
-                    qa[kk][3] = g_lo + 8 < GS ? q32[(g_lo + 8) * (D / 2) + c1] : 0u;
+                    qa[kk][1] = g_lo + 8 < seg_rows ? q32[(g_lo + 8) * (D / 2) + c0] : 0u;
+                    qa[kk][3] = g_lo + 8 < seg_rows ? q32[(g_lo + 8) * (D / 2) + c1] : 0u;
                 } else {
                     qa[kk][1] = 0u;
                     qa[kk][3] = 0u;
@@ -293,6 +305,14 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 Mma<T>::run(s[1][kk & 1], qa[kk], kb[2], kb[3]);
             }
             // ---- online softmax (base 2) on rows g_lo (c0,c1) and g_lo+8 (c2,c3) ----
+            // causal limit of several query tokens: query j of a unit row sees
+            // tokens up to len - n_queries + j (no limit inside the chunk when 1)
+            int lim_lo = kChunk, lim_hi = kChunk;
+            if (p.rows.n_queries > 1) {
+                const int base = d.len - p.rows.n_queries - d.k * kChunk;
+                lim_lo = base + jq_lo;
+                lim_hi = base + jq_hi;
+            }
             float sc[2][4];
 #pragma unroll
             for (int a = 0; a < 2; ++a)
@@ -300,7 +320,7 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 for (int e = 0; e < 4; ++e) {
                     const int t = a * 8 + tq + (e & 1);
                     const float v = (s[a][0][e] + s[a][1][e]) * p.scale_log2;
-                    sc[a][e] = t < nvalid ? v : -INFINITY;
+                    sc[a][e] = (t < nvalid && t <= (e < 2 ? lim_lo : lim_hi)) ? v : -INFINITY;
                 }
             uint32_t pa[4];        // A fragments of P (its bf16 high part when split)
             uint32_t pl[4] = {0u, 0u, 0u, 0u};  // bf16 residual p - hi (split only)
@@ -309,9 +329,11 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
                 const float m_new = fmaxf(m_lo, mx);
-                const float alpha = fast_exp2(m_lo - m_new);
-                const float p00 = fast_exp2(sc[0][0] - m_new), p01 = fast_exp2(sc[0][1] - m_new);
-                const float p10 = fast_exp2(sc[1][0] - m_new), p11 = fast_exp2(sc[1][1] - m_new);
+                // a causal row with no token yet (m_new = -inf) takes weights 0
+                const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = fast_exp2(m_lo - m_ref);
+                const float p00 = fast_exp2(sc[0][0] - m_ref), p01 = fast_exp2(sc[0][1] - m_ref);
+                const float p10 = fast_exp2(sc[1][0] - m_ref), p11 = fast_exp2(sc[1][1] - m_ref);
                 float rs = (p00 + p01) + (p10 + p11);
                 rs += __shfl_xor_sync(kFull, rs, 1);
                 rs += __shfl_xor_sync(kFull, rs, 2);
@@ -335,9 +357,11 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
                 const float m_new = fmaxf(m_hi, mx);
-                const float alpha = fast_exp2(m_hi - m_new);
-                const float p00 = fast_exp2(sc[0][2] - m_new), p01 = fast_exp2(sc[0][3] - m_new);
-                const float p10 = fast_exp2(sc[1][2] - m_new), p11 = fast_exp2(sc[1][3] - m_new);
+                // a causal row with no token yet (m_new = -inf) takes weights 0
+                const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = fast_exp2(m_hi - m_ref);
+                const float p00 = fast_exp2(sc[0][2] - m_ref), p01 = fast_exp2(sc[0][3] - m_ref);
+                const float p10 = fast_exp2(sc[1][2] - m_ref), p11 = fast_exp2(sc[1][3] - m_ref);
                 float rs = (p00 + p01) + (p10 + p11);
                 rs += __shfl_xor_sync(kFull, rs, 1);
                 rs += __shfl_xor_sync(kFull, rs, 2);
@@ -385,15 +409,14 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
             const int uidx = d.u - b * units_per_b;
             const int h = uidx / p.sub_groups;
             const int sg = uidx - h * p.sub_groups;
-            const long long hq0 = (long long)b * p.n_q_heads + h * p.group + sg * GS;
 #pragma unroll
             for (int half = 0; half < (kTwoHalves ? 2 : 1); ++half) {
                 const int g = g_lo + half * 8;
                 const float l = half ? l_hi : l_lo;
                 const float m = half ? m_hi : m_lo;
-                if (g < GS) {
+                if (g < seg_rows) {
                     if (whole) {
-                        T* outp = static_cast<T*>(p.out) + (hq0 + g) * D;
+                        T* outp = static_cast<T*>(p.out) + p.rows.row(b, h, sg, g) * D;
                         const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {

@@ -336,8 +336,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ prefix,
                const int32_t* __restrict__ lens_eff, const WsHeader* __restrict__ hdr,
-               T* __restrict__ out, int units_per_b, int sub_groups, int gs, int group,
-               int n_q_heads, int merge_batch) {
+               T* __restrict__ out, int units_per_b, int sub_groups, int gs, int merge_batch,
+               RowShape rs) {
     extern __shared__ float4 sbuf4[];  // merge_batch staged partial slots
     // Everything up to pdl_wait reads only what the plan wrote: the plan grid
     // completed before any decode CTA passed its own wait and let this
@@ -347,7 +347,6 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     const int uidx = u - b * units_per_b;
     const int h = uidx / sub_groups;
     const int sgi = uidx - h * sub_groups;
-    T* o = out + ((long long)b * n_q_heads + h * group + sgi * gs) * D;
     const int L = lens_eff[b];
     const int nch = (L + kChunk - 1) / kChunk;
     const int tid = threadIdx.x;
@@ -389,7 +388,11 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
 #pragma unroll
     for (int k = 0; k < KPT; ++k) {
         const int it = k * blockDim.x + tid;
-        if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o);
+        if (it < gs * Q) {
+            const int g = it / Q;
+            if (g < rs.rows(sgi))
+                merge_store<T, D>(acc[k], heads, g, it % Q, out + rs.row(b, h, sgi, g) * D);
+        }
     }
 }
 
@@ -477,7 +480,7 @@ cascade_combine_kernel(CascadeArgs c) {
 #pragma unroll
     for (int k = 0; k < KPT; ++k) {
         const int it = k * blockDim.x + tid;
-        if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o);
+        if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o + (it / Q) * D);
     }
 }
 
@@ -594,13 +597,13 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           int group, int n_q_heads, int merge_batch, cudaStream_t stream) {
+                           int merge_batch, const RowShape& rs, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
 #define PKV_COMBINE(T, D)                                                                     \
     return launch_pdl(combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32),           \
                       (size_t)merge_smem_bytes(merge_batch, gs, D), stream, partials,         \
                       prefix, lens_eff, hdr, static_cast<T*>(out), units_per_b, sub_groups,   \
-                      gs, group, n_q_heads, merge_batch)
+                      gs, merge_batch, rs)
     if (dtype == PKV_BF16) {
         if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128);
         PKV_COMBINE(__nv_bfloat16, 64);

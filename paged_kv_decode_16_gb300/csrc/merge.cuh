@@ -97,6 +97,7 @@ __device__ __forceinline__ void merge_accumulate(const float* slots, int stride,
     acc = x;
 }
 
+// Outputs 4*d4 .. 4*d4+3 of unit row g, whose output row starts at out_row.
 template <typename T, int D>
 __device__ __forceinline__ void merge_store(const float4& acc, const MergeHead* heads, int g,
                                             int d4, T* out_row) {
@@ -105,7 +106,7 @@ __device__ __forceinline__ void merge_store(const float4& acc, const MergeHead* 
     uint2 w2;
     w2.x = Cvt<T>::pack2(acc.x * inv, acc.y * inv);
     w2.y = Cvt<T>::pack2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out_row + g * D + d4 * 4) = w2;
+    *reinterpret_cast<uint2*>(out_row + d4 * 4) = w2;
 }
 
 // Bytes of shared memory a merge needs: merge_batch staged slots, then the
@@ -174,11 +175,15 @@ __device__ __noinline__ void merge_staged(const DecodeParams& p, const PendingMe
     const int uidx = pm.u - b * units_per_b;
     const int h = uidx / p.sub_groups;
     const int sgi = uidx - h * p.sub_groups;
-    T* out_row = static_cast<T*>(p.out) + ((long long)b * p.n_q_heads + h * p.group + sgi * GS) * D;
 #pragma unroll
     for (int k = 0; k < KPL; ++k) {
         const int it = k * 32 + lane;
-        if (it < GS * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, out_row);
+        if (it < GS * Q) {
+            const int g = it / Q;
+            if (g < p.rows.rows(sgi))
+                merge_store<T, D>(acc[k], heads, g, it % Q,
+                                  static_cast<T*>(p.out) + p.rows.row(b, h, sgi, g) * D);
+        }
     }
 }
 
@@ -216,7 +221,7 @@ __device__ __forceinline__ void finish_pending(const DecodeParams& p, int npend,
 // Warp-collective.
 __device__ __forceinline__ void zero_empty_sequences(const DecodeParams& p, int head_dim, int gw,
                                                      int nwarps, int lane) {
-    const long long vecs = (long long)p.n_q_heads * head_dim * 2 / 16;  // per sequence
+    const long long vecs = (long long)p.rows.n_queries * p.n_q_heads * head_dim * 2 / 16;  // per seq
     for (long long b0 = (long long)gw * 32; b0 < p.batch; b0 += (long long)nwarps * 32) {
         const long long b = b0 + lane;
         const bool empty = b < p.batch && __ldg(p.lens_eff + b) == 0;

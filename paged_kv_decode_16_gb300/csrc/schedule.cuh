@@ -30,6 +30,7 @@ struct ChunkDesc {
     int k;          // chunk index within the unit
     int nch;        // chunks of the unit
     int nvalid;     // valid tokens in the chunk (1..16)
+    int len;        // tokens of the sequence
     long long off;  // first pool row of the chunk ([page][h][slot] rows of D), -1: bad page id
 };
 
@@ -51,6 +52,7 @@ __device__ __forceinline__ ChunkDesc describe_chunk(const DecodeParams& p, int f
     d.nch = nch;
     d.u = b * units_per_b + uidx;
     d.nvalid = min(kChunk, L - d.k * kChunk);
+    d.len = L;
     const int h = uidx / p.sub_groups;
     const int tok = d.k * kChunk;
     const int page = __ldg(p.table + (long long)b * p.table_stride + tok / p.page_size);
@@ -69,6 +71,7 @@ __device__ __forceinline__ ChunkDesc shfl_desc(const ChunkDesc& a, int src) {
     d.k = __shfl_sync(kFull, a.k, src);
     d.nch = __shfl_sync(kFull, a.nch, src);
     d.nvalid = __shfl_sync(kFull, a.nvalid, src);
+    d.len = __shfl_sync(kFull, a.len, src);
     d.off = __shfl_sync(kFull, a.off, src);
     return d;
 }
@@ -80,6 +83,7 @@ __device__ __forceinline__ ChunkDesc sel_desc(bool second, const ChunkDesc& a,
     d.k = second ? b.k : a.k;
     d.nch = second ? b.nch : a.nch;
     d.nvalid = second ? b.nvalid : a.nvalid;
+    d.len = second ? b.len : a.len;
     d.off = second ? b.off : a.off;
     return d;
 }
@@ -113,7 +117,7 @@ struct WorkStream {
         next_f += len;
         b_len = len;
         wb.off = -1;
-        wb.u = wb.k = wb.nvalid = 0;
+        wb.u = wb.k = wb.nvalid = wb.len = 0;
         wb.nch = 1;
         if (lane < len) wb = describe_chunk(p, f + lane, units_per_b, b_lo, b_hi);
     }
