@@ -81,7 +81,6 @@ struct KernelPick {
     int smem() const {
         return variant == PKV_VARIANT_TENSOR_CORES ? mma.smem_bytes : cc.smem_bytes;
     }
-    int stages() const { return variant == PKV_VARIANT_TENSOR_CORES ? mma.stages : cc.stages; }
 };
 
 KernelPick pick_kernel(pkv_dtype dtype, int head_dim, int variant, int gs) {
@@ -165,7 +164,6 @@ struct DecodeSetup {
     int workers_auto;  // automatic count for this kernel on this device
     KernelPick kernel;
     WsLayout ws;
-    int merge_batch;   // partial slots per merge batch: as many as a warp's stage buffers hold
     pkv::RowShape rs{};  // the query rows of each unit
 };
 
@@ -216,12 +214,6 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     if (st != PKV_OK) return st;
     s->workers = num_workers > 0 ? num_workers : s->workers_auto;
     s->ws = ws_layout(batch, s->units, s->gs, head_dim, s->workers);
-    // a warp's stage buffers: stages x (K + V) chunks of 16 rows x head_dim x 2 bytes
-    const int stage_bytes = s->kernel.stages() * 64 * head_dim;
-    s->merge_batch = (stage_bytes - pkv::merge_smem_bytes(0, s->gs, head_dim)) /
-                     (pkv::partial_slot_floats(s->gs, head_dim) * 4);
-    if (s->merge_batch > 32) s->merge_batch = 32;
-    if (s->merge_batch < 1) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
 
@@ -343,7 +335,6 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.status = status ? status : &reinterpret_cast<WsHeader*>(ws)->status;
     p.partials = reinterpret_cast<float*>(ws + s.ws.partials);
     p.unit_done = merge ? reinterpret_cast<int32_t*>(ws + s.ws.unit_done) : nullptr;
-    p.merge_batch = s.merge_batch;
     p.all_partials = all_partials ? 1 : 0;
     p.rows = s.rs;
     p.out = out;
@@ -380,7 +371,7 @@ pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, v
         dtype, head_dim, reinterpret_cast<const float*>(ws + s.ws.partials),
         reinterpret_cast<const int32_t*>(ws + s.ws.prefix),
         reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<const WsHeader*>(ws),
-        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.merge_batch, s.rs, stream));
+        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.rs, stream));
 }
 
 // --- fixed device scratch for paged_decode_attention_no_alloc -------------
@@ -944,10 +935,6 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
     c.v_sub = ps.virt.sub_groups;
     c.v_nch = (prefix_tokens + 15) / 16;
     // slots staged per batch: about 48 KiB of shared memory
-    const int slot_bytes = pkv::partial_slot_floats(ps.real.gs, head_dim) * 4;
-    c.merge_batch = (48 * 1024 - pkv::merge_smem_bytes(0, ps.real.gs, head_dim)) / slot_bytes;
-    if (c.merge_batch > 32) c.merge_batch = 32;
-    if (c.merge_batch < 1) c.merge_batch = 1;
     return cuda_status(pkv::launch_cascade_combine(dtype, head_dim, c, (int)ps.real.units, cs));
 }
 

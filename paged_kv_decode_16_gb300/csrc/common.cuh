@@ -232,7 +232,6 @@ struct DecodeParams {
     float* partials;          // [slots][partial_slot_floats(GS, D)]
     int32_t* unit_done;       // [U] chunks finished per unit (zeroed by the plan); null: split
                               // units are left to the combine kernel
-    int merge_batch;          // partial slots merged per batch (fit the warp's stage buffers)
     int all_partials;         // nonzero: every segment leaves a partial state, out is not written
                               // (a later merge completes it)
     RowShape rows;            // the query rows of each unit

@@ -374,7 +374,7 @@ decode_kernel(const DecodeParams p) {
     }
     // every copy has landed and been consumed: the stage buffers serve the merges
     if (npend > 0)
-        finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, wsm + Lay::kOffK, lane);
+        finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, lane);
 }
 
 template <int D, int GS>

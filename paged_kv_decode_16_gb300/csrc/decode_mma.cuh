@@ -100,8 +100,8 @@ __device__ __forceinline__ uint32_t swz128(int r, int j) {
 }
 
 // Shared memory of one CTA: every warp's ring of K/V stages first (each stage a
-// multiple of 1 KiB, as the 128-byte swizzle needs), then every warp's q slots,
-// then the mbarriers.
+// multiple of 1 KiB, as the 128-byte swizzle needs), then every warp's q slots
+// (one per stage), then the mbarriers.
 template <int D, int GS, int STAGES, int WARPS>
 struct MmaLayout {
     static constexpr int kBoxes = D / 64;                       // [16 x 64] boxes per K or V chunk
@@ -177,11 +177,14 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         const bool seg_start = ws.seg_start(j, d);
         if (lane == 0) {
             const int st = j % STAGES;
-            const int b = d.u / units_per_b;
-            const int uidx = d.u - b * units_per_b;
-            const int h = uidx / p.sub_groups;
-            const int sg = uidx - h * p.sub_groups;
-            const int nrows = p.rows.rows(sg);
+            int b = 0, h = 0, sg = 0, nrows = 0;
+            if (seg_start) {
+                b = d.u / units_per_b;
+                const int uidx = d.u - b * units_per_b;
+                h = uidx / p.sub_groups;
+                sg = uidx - h * p.sub_groups;
+                nrows = p.rows.rows(sg);
+            }
             const uint32_t kv_bytes = d.off >= 0 ? (uint32_t)Lay::kStageBytes : 0u;
             const uint32_t q_bytes = seg_start ? (uint32_t)(nrows * D * 2) : 0u;
             fence_proxy_async_smem();
@@ -226,6 +229,13 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         ws.consumer_at(p, i, STAGES + 1);
         const ChunkDesc d = ws.fetch(i);
         const int st = i % STAGES;
+        const bool seg_start = ws.seg_start(i, d);
+        if (seg_start) {
+            const int sg = (d.u % units_per_b) % p.sub_groups;
+            seg_rows = p.rows.rows(sg);
+            jq_lo = p.rows.query(sg, g_lo);
+            jq_hi = p.rows.query(sg, g_lo + 8);
+        }
         if (!mbar_wait_bounded(&bar[st], (uint32_t)((i / STAGES) & 1))) {
             // A copy never landed.  Report it, wait (bounded) for the copies
             // still in flight into this warp's buffers, and stop.
@@ -234,16 +244,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 mbar_wait_bounded(&bar[j % STAGES], (uint32_t)((j / STAGES) & 1));
             return;
         }
-        const bool seg_start = ws.seg_start(i, d);
         if (seg_start) {
             seg_slot = ws.slot_base + d.u;
             seg_first = i;
-            {
-                const int sg = (d.u % units_per_b) % p.sub_groups;
-                seg_rows = p.rows.rows(sg);
-                jq_lo = p.rows.query(sg, g_lo);
-                jq_hi = p.rows.query(sg, g_lo + 8);
-            }
             // A fragments of Q: a0 (row g, k tq..tq+1), a1 (row g+8), a2 (k+8), a3
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(sq + st * GS * D);
 #pragma unroll
@@ -447,9 +450,8 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         // refill: positions up to i + STAGES (stage i % STAGES is free again)
         while (issued <= i + STAGES && issue(issued)) ++issued;
     }
-    // every copy has landed and been consumed: the stage buffers serve the merges
     if (npend > 0)
-        finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, wsm, lane);
+        finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, lane);
 }
 
 template <int D, int GS>

@@ -325,10 +325,8 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
 
 // ---------------------------------------------------------------------------
 // Combine: one CTA per unit (sequence, KV head, sub-group); units finished by
-// a single worker and empty sequences exit at once.  The unit's partial slots
-// are staged in shared memory merge_batch at a time and folded with
-// merge_weights / merge_accumulate, the same batches and arithmetic the decode
-// kernels' own merge uses.
+// a single worker and empty sequences exit at once.  Each warp merges rows of
+// the unit with merge_rows, the routine the decode kernels' own merge uses.
 // ---------------------------------------------------------------------------
 constexpr int kCombineWarps = 8;
 
@@ -336,9 +334,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ prefix,
                const int32_t* __restrict__ lens_eff, const WsHeader* __restrict__ hdr,
-               T* __restrict__ out, int units_per_b, int sub_groups, int gs, int merge_batch,
-               RowShape rs) {
-    extern __shared__ float4 sbuf4[];  // merge_batch staged partial slots
+               T* __restrict__ out, int units_per_b, int sub_groups, int gs, RowShape rs) {
     // Everything up to pdl_wait reads only what the plan wrote: the plan grid
     // completed before any decode CTA passed its own wait and let this
     // kernel launch.  The partial states are read after the wait.
@@ -349,7 +345,6 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     const int sgi = uidx - h * sub_groups;
     const int L = lens_eff[b];
     const int nch = (L + kChunk - 1) / kChunk;
-    const int tid = threadIdx.x;
     if (nch == 0) return;  // the decode kernel zeroed the rows of empty sequences
     if (hdr->total_chunks <= 0 || hdr->num_workers <= 0) return;
     const UnitSegments segs =
@@ -358,42 +353,9 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     if (ns <= 1) return;  // finished in place by its worker
     pdl_wait();
     pdl_trigger();
-    const int stride = partial_slot_floats(gs, D);
-    constexpr int Q = D / 4;
-    constexpr int KPT = (16 * Q + kCombineWarps * 32 - 1) / (kCombineWarps * 32);
-    float* slots = reinterpret_cast<float*>(sbuf4);
-    MergeHead* heads = reinterpret_cast<MergeHead*>(slots + merge_batch * stride);
-    if (tid < gs) heads[tid] = MergeHead{-INFINITY, 0.f, 0.f, 0.f};
-    float4 acc[KPT];
-#pragma unroll
-    for (int k = 0; k < KPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int vps = stride / 4;  // 16-byte vectors per slot
-    for (int s0 = 0; s0 < ns; s0 += merge_batch) {
-        const int cnt = min(merge_batch, ns - s0);
-        __syncthreads();
-        for (int v = tid; v < cnt * vps; v += blockDim.x) {
-            const int s = v / vps;
-            sbuf4[v] = __ldcg(reinterpret_cast<const float4*>(partials + segs.slot(s0 + s) * stride) +
-                              (v - s * vps));
-        }
-        __syncthreads();
-        if (tid < 32) merge_weights(slots, stride, cnt, gs, D, heads, tid);
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < KPT; ++k) {
-            const int it = k * blockDim.x + tid;
-            if (it < gs * Q) merge_accumulate<D>(slots, stride, cnt, gs, heads, it / Q, it % Q, acc[k]);
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < KPT; ++k) {
-        const int it = k * blockDim.x + tid;
-        if (it < gs * Q) {
-            const int g = it / Q;
-            if (g < rs.rows(sgi))
-                merge_store<T, D>(acc[k], heads, g, it % Q, out + rs.row(b, h, sgi, g) * D);
-        }
-    }
+    const SlotSegs sg{partials, segs.base, partial_slot_floats(gs, D), gs, D};
+    merge_rows<T, D>(sg, ns, rs.rows(sgi), threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+                     [&](int g) { return out + rs.row(b, h, sgi, g) * D; });
 }
 
 // ---------------------------------------------------------------------------
@@ -403,19 +365,32 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
 // tokens.  Both left only partial states.  One CTA per real unit (sequence,
 // KV head, sub-group of gs rows): its rows sit at rows ro .. ro+gs-1 of one
 // virtual unit (gs divides gs_v).  The prefix segments, then the suffix
-// segments, are staged merge_batch at a time in the real slot layout and
-// folded with merge_weights / merge_accumulate.
+// segments, are merged as one list with merge_rows.
 // ---------------------------------------------------------------------------
+struct CascadeSegs {
+    SlotSegs pre;  // the virtual unit's segments (rows offset by ro)
+    int ro, np;
+    SlotSegs suf;  // the unit's own segments
+    __device__ __forceinline__ const float* o(int s, int g) const {
+        return s < np ? pre.o(s, ro + g) : suf.o(s - np, g);
+    }
+    __device__ __forceinline__ const float* m(int s, int g) const {
+        return s < np ? pre.m(s, ro + g) : suf.m(s - np, g);
+    }
+    __device__ __forceinline__ const float* l(int s, int g) const {
+        return s < np ? pre.l(s, ro + g) : suf.l(s - np, g);
+    }
+};
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 cascade_combine_kernel(CascadeArgs c) {
-    extern __shared__ float4 sbuf4[];
     const int u = blockIdx.x;
     const int b = u / c.units_per_b;
     const int uidx = u - b * c.units_per_b;
     const int h = uidx / c.sub_groups;
     const int sgi = uidx - h * c.sub_groups;
-    const int gs = c.gs, tid = threadIdx.x;
+    const int gs = c.gs;
     T* o = static_cast<T*>(c.out) + ((long long)b * c.n_q_heads + h * c.group + sgi * gs) * D;
     // the prefix side: the virtual unit holding this unit's rows
     const int r0 = b * c.group + sgi * gs;             // row among head h's B*G rows
@@ -433,55 +408,11 @@ cascade_combine_kernel(CascadeArgs c) {
     const int ns = sv.count();
     pdl_wait();  // the partial states of both passes are complete from here on
     pdl_trigger();
-    const int stride = partial_slot_floats(gs, D);
-    const int vstride = partial_slot_floats(c.v_gs, D);
-    const int n = gs * D;
-    constexpr int Q = D / 4;
-    constexpr int KPT = (16 * Q + kCombineWarps * 32 - 1) / (kCombineWarps * 32);
-    float* slots = reinterpret_cast<float*>(sbuf4);
-    MergeHead* heads = reinterpret_cast<MergeHead*>(slots + c.merge_batch * stride);
-    if (tid < gs) heads[tid] = MergeHead{-INFINITY, 0.f, 0.f, 0.f};
-    float4 acc[KPT];
-#pragma unroll
-    for (int k = 0; k < KPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < np + ns; s0 += c.merge_batch) {
-        const int cnt = min(c.merge_batch, np + ns - s0);
-        __syncthreads();
-        // o rows as 16-byte vectors, then m and l as scalars
-        const int vrow = n / 4;
-        for (int v = tid; v < cnt * vrow; v += blockDim.x) {
-            const int s = v / vrow, e = v - s * vrow;
-            const int g = s0 + s;
-            const float* src = g < np ? c.v_partials + pv.slot(g) * vstride + (long long)ro * D
-                                      : c.s_partials + sv.slot(g - np) * stride;
-            sbuf4[(s * stride) / 4 + e] = __ldcg(reinterpret_cast<const float4*>(src) + e);
-        }
-        for (int v = tid; v < cnt * 2 * gs; v += blockDim.x) {
-            const int s = v / (2 * gs), e = v - s * 2 * gs;  // e < gs: m, else l
-            const int g = s0 + s;
-            float x;
-            if (g < np) {
-                const float* base = c.v_partials + pv.slot(g) * vstride + (long long)c.v_gs * D;
-                x = __ldcg(e < gs ? base + ro + e : base + c.v_gs + ro + (e - gs));
-            } else {
-                x = __ldcg(c.s_partials + sv.slot(g - np) * stride + n + e);
-            }
-            slots[s * stride + n + e] = x;
-        }
-        __syncthreads();
-        if (tid < 32) merge_weights(slots, stride, cnt, gs, D, heads, tid);
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < KPT; ++k) {
-            const int it = k * blockDim.x + tid;
-            if (it < gs * Q) merge_accumulate<D>(slots, stride, cnt, gs, heads, it / Q, it % Q, acc[k]);
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < KPT; ++k) {
-        const int it = k * blockDim.x + tid;
-        if (it < gs * Q) merge_store<T, D>(acc[k], heads, it / Q, it % Q, o + (it / Q) * D);
-    }
+    const CascadeSegs sg{SlotSegs{c.v_partials, pv.base, partial_slot_floats(c.v_gs, D), c.v_gs, D},
+                         ro, np,
+                         SlotSegs{c.s_partials, sv.base, partial_slot_floats(gs, D), gs, D}};
+    merge_rows<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+                     [&](int g) { return o + (long long)g * D; });
 }
 
 __global__ void __launch_bounds__(256)
@@ -513,9 +444,8 @@ cudaError_t launch_gather_q(const void* q, void* qv, int batch, int n_kv_heads, 
 cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeArgs& c,
                                    int units, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
-    const size_t smem = (size_t)merge_smem_bytes(c.merge_batch, c.gs, head_dim);
 #define PKV_CASCADE(T, D) \
-    return launch_pdl(cascade_combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32), smem, \
+    return launch_pdl(cascade_combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32), 0, \
                       stream, c)
     if (dtype == PKV_BF16) {
         if (head_dim == 128) PKV_CASCADE(__nv_bfloat16, 128);
@@ -597,13 +527,12 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           int merge_batch, const RowShape& rs, cudaStream_t stream) {
+                           const RowShape& rs, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
 #define PKV_COMBINE(T, D)                                                                     \
-    return launch_pdl(combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32),           \
-                      (size_t)merge_smem_bytes(merge_batch, gs, D), stream, partials,         \
-                      prefix, lens_eff, hdr, static_cast<T*>(out), units_per_b, sub_groups,   \
-                      gs, merge_batch, rs)
+    return launch_pdl(combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32), 0, stream, \
+                      partials, prefix, lens_eff, hdr, static_cast<T*>(out), units_per_b,     \
+                      sub_groups, gs, rs)
     if (dtype == PKV_BF16) {
         if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128);
         PKV_COMBINE(__nv_bfloat16, 64);

@@ -59,7 +59,7 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           int merge_batch, const RowShape& rs, cudaStream_t stream);
+                           const RowShape& rs, cudaStream_t stream);
 
 // batches up to this size keep their chunk prefix sums in the plan's shared memory
 constexpr int kPlanSmemSeqs = 4096;
@@ -77,7 +77,6 @@ struct CascadeArgs {
     void* out;
     int units_per_b, sub_groups, gs, group, n_q_heads;  // real units
     int v_gs, v_sub, v_nch;                              // virtual units per KV head, chunks
-    int merge_batch;
 };
 
 // qv[h][b * G + g][:] = q[b][h * G + g][:]: the query rows of each KV head

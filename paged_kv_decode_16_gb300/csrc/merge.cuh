@@ -2,15 +2,18 @@
 // processed (split-K reduction of flash-decoding), and the other writes that
 // complete the output.
 //
-// A segment s of unit u leaves (o_s, m_s, l_s) per query head: o_s the
+// A segment s of unit u leaves (o_s, m_s, l_s) per query row: o_s the
 // unnormalised weighted sum of V rows, m_s the running maximum of the scores
 // in base-2 units, l_s the sum of 2^(score - m_s).  The merged output is
 //     out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
 //
-// The stand-alone combine kernel and the decode kernels (the warp that
-// finishes the last segment of a unit merges it, after its own chunk stream)
-// fold the same batches of segments with merge_weights / merge_accumulate,
-// so the two paths give the same bits.
+// Two passes, in an order that depends on nothing but the segment count:
+// a warp per row finds M and the denominator (lane t takes segments t, t+32,
+// ... in order; the lane sums meet in a fixed butterfly), then each output
+// vector sums its weighted o_s in segment order straight from the slots.  The
+// stand-alone combine kernels and the decode kernels (the warp that finishes
+// the last segment of a unit merges it after its own chunk stream) call the
+// same routines, so the two paths give the same bits.
 #pragma once
 
 #include "common.cuh"
@@ -35,73 +38,61 @@ __device__ __forceinline__ UnitSegments unit_segments(int sw, int r, int u, int 
     return sg;
 }
 
-// Per-head running state of a merge, kept in shared memory next to the
-// staged slots: maximum so far (base 2), denominator so far, and the factor
-// that rescales the numerators of earlier batches in this batch.
-struct MergeHead {
-    float M, den, a, pad;
+// Segment s of a unit in the usual slot layout (stride floats per slot: o at
+// [g*D], m at [gs*D + g], l at [gs*D + gs + g]), slots base, base + 1, ...
+struct SlotSegs {
+    const float* partials;
+    long long base;
+    int stride, gs, d;
+    __device__ __forceinline__ const float* o(int s, int g) const {
+        return partials + (base + s) * stride + (long long)g * d;
+    }
+    __device__ __forceinline__ const float* m(int s, int g) const {
+        return partials + (base + s) * stride + (long long)gs * d + g;
+    }
+    __device__ __forceinline__ const float* l(int s, int g) const { return m(s, g) + gs; }
 };
 
-// Step 1 of folding a batch of cnt <= 32 staged segments (slot stride
-// `stride` floats: o at [g*D], m at [gs*D + g], l at [gs*D + gs + g]) into a
-// unit's merge: per head, lane s owns segment s; the batch maximum joins the
-// running one, lane s turns m_s into its weight 2^(m_s - M) in place, and the
-// weighted l_s are summed into the denominator.  One warp; heads[] holds the
-// running state (M = -inf, den = 0 before the first batch).
-__device__ __forceinline__ void merge_weights(float* slots, int stride, int cnt, int gs, int D,
-                                              MergeHead* heads, int lane) {
-    const int n = gs * D;
-    for (int g = 0; g < gs; ++g) {
-        float* mp = slots + lane * stride + n + g;
-        const float m = lane < cnt ? *mp : -INFINITY;
-        float mb = m;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
-        const float m_old = heads[g].M;
-        const float mn = fmaxf(m_old, mb);
-        // no finite score yet (mn = -inf): every weight and factor is 0
-        const float w = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-        const float a = (m_old == -INFINITY) ? 0.f : exp2f(m_old - mn);
-        float dl = lane < cnt ? w * mp[gs] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(kFull, dl, o);
-        if (lane < cnt) *mp = w;
-        __syncwarp();
-        if (lane == 0) {
-            heads[g].M = mn;
-            heads[g].den = fmaf(heads[g].den, a, dl);
-            heads[g].a = a;
-        }
-        __syncwarp();
-    }
+struct MergeRow {
+    float M, den;
+    float w;  // ns <= 32: the weight of segment `lane` (0 past ns)
+};
+
+__device__ __forceinline__ float merge_weight(float m, float M) {
+    // no finite score in the segment (m = -inf): weight 0
+    return m == -INFINITY ? 0.f : exp2f(m - M);
 }
 
-// Step 2: output vector (g, d4) (4 consecutive outputs of head g) folds the
-// batch in, in segment order: acc = acc * a_g + sum_s w_s o_s.
-template <int D>
-__device__ __forceinline__ void merge_accumulate(const float* slots, int stride, int cnt, int gs,
-                                                 const MergeHead* heads, int g, int d4,
-                                                 float4& acc) {
-    const int n = gs * D;
-    const float a = heads[g].a;
-    float4 x = make_float4(acc.x * a, acc.y * a, acc.z * a, acc.w * a);
-    for (int s = 0; s < cnt; ++s) {
-        const float* pp = slots + s * stride;
-        const float w = pp[n + g];
-        const float4 v = *reinterpret_cast<const float4*>(pp + g * D + d4 * 4);
-        x.x = fmaf(w, v.x, x.x);
-        x.y = fmaf(w, v.y, x.y);
-        x.z = fmaf(w, v.z, x.z);
-        x.w = fmaf(w, v.w, x.w);
+// Pass 1 for row g of ns segments; one warp, every lane gets M and den.  Up
+// to 32 segments lane t holds segment t's m and l (one round of loads) and
+// keeps its weight for pass 2; beyond, lane t walks segments t, t+32, ...
+// twice.  Both give the same sums: lane t adds its segments' w_s l_s in order.
+template <class Segs>
+__device__ __forceinline__ MergeRow merge_row(const Segs& sg, int ns, int g, int lane) {
+    float M = -INFINITY, den = 0.f, wl = 0.f;
+    if (ns <= 32) {
+        const float m = lane < ns ? __ldcg(sg.m(lane, g)) : -INFINITY;
+        const float l = lane < ns ? __ldcg(sg.l(lane, g)) : 0.f;
+        M = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        wl = merge_weight(m, M);
+        den = fmaf(wl, l, 0.f);
+    } else {
+        for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(sg.m(s, g)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        for (int s = lane; s < ns; s += 32)
+            den = fmaf(merge_weight(__ldcg(sg.m(s, g)), M), __ldcg(sg.l(s, g)), den);
     }
-    acc = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+    return MergeRow{M, den, wl};
 }
 
-// Outputs 4*d4 .. 4*d4+3 of unit row g, whose output row starts at out_row.
+// Outputs 4*d4 .. 4*d4+3 of a merged row (out_row: its first output).
 template <typename T, int D>
-__device__ __forceinline__ void merge_store(const float4& acc, const MergeHead* heads, int g,
-                                            int d4, T* out_row) {
-    const float den = heads[g].den;
+__device__ __forceinline__ void merge_store(const float4& acc, float den, int d4, T* out_row) {
     const float inv = den > 0.f ? 1.0f / den : 0.f;
     uint2 w2;
     w2.x = Cvt<T>::pack2(acc.x * inv, acc.y * inv);
@@ -109,10 +100,32 @@ __device__ __forceinline__ void merge_store(const float4& acc, const MergeHead* 
     *reinterpret_cast<uint2*>(out_row + d4 * 4) = w2;
 }
 
-// Bytes of shared memory a merge needs: merge_batch staged slots, then the
-// per-head state (16 heads at most).
-__host__ __device__ constexpr int merge_smem_bytes(int merge_batch, int gs, int d) {
-    return merge_batch * partial_slot_floats(gs, d) * 4 + 16 * (int)sizeof(MergeHead);
+// Merge rows [0, nrows) of a unit with the warps of a CTA (warp w of nwarps
+// takes rows w, w + nwarps, ...); out_rows(g) gives row g's output.  Pass 2:
+// lane t sums output vector t of the row, sum_s w_s o_s in segment order.
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, int warp, int nwarps,
+                                           int lane, const RowOut& out_rows) {
+    constexpr int Q = D / 4;  // output vectors per row
+    static_assert(Q <= 32, "one vector per lane");
+    for (int g = warp; g < nrows; g += nwarps) {
+        const MergeRow mr = merge_row(sg, ns, g, lane);
+        const bool act = lane < Q;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int s = 0; s < ns; ++s) {
+            const float w = ns <= 32 ? __shfl_sync(kFull, mr.w, s)
+                                     : merge_weight(__ldcg(sg.m(s, g)), mr.M);
+            if (act) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(sg.o(s, g)) + lane);
+                x.x = fmaf(w, v.x, x.x);
+                x.y = fmaf(w, v.y, x.y);
+                x.z = fmaf(w, v.z, x.z);
+                x.w = fmaf(w, v.w, x.w);
+            }
+        }
+        if (act) merge_store<T, D>(x, mr.den, lane, out_rows(g));
+    }
 }
 
 // A split segment whose arrival a decode warp reports after its main loop.
@@ -123,68 +136,21 @@ struct PendingMerge {
     int chunks;  // chunks of this warp's segment
 };
 
-// 16-byte asynchronous copy global -> shared through L2 (cp.async.cg), and
-// the wait for every copy this thread issued.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-// Merge split unit `pm` in the decode warp that finished its last segment:
-// copy the segments' partial states, merge_batch slots at a time, into the
-// warp's stage buffers (idle once its chunk stream is done; `stage` holds
-// merge_smem_bytes(merge_batch, GS, D)) and fold them there.  Warp-collective.
+// Merge split unit `pm` in the decode warp that finished its last segment.
+// Warp-collective.
 template <typename T, int D, int GS>
-__device__ __noinline__ void merge_staged(const DecodeParams& p, const PendingMerge& pm, int sw,
-                                          int r, uint8_t* stage, int lane) {
-    constexpr int stride = partial_slot_floats(GS, D);
-    constexpr int vps = stride / 4;  // 16-byte vectors per slot
-    constexpr int Q = D / 4;
-    constexpr int KPL = (GS * Q + 31) / 32;  // output vectors per lane
-    const UnitSegments sg = unit_segments(sw, r, pm.u, pm.a, pm.nch);
-    const int ns = sg.count();
-    float* slots = reinterpret_cast<float*>(stage);
-    MergeHead* heads = reinterpret_cast<MergeHead*>(stage + p.merge_batch * stride * 4);
-    if (lane < GS) heads[lane] = MergeHead{-INFINITY, 0.f, 0.f, 0.f};
-    float4 acc[KPL];
-#pragma unroll
-    for (int k = 0; k < KPL; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += p.merge_batch) {
-        const int cnt = min(p.merge_batch, ns - s0);
-        __syncwarp();  // every lane is done with the previous batch
-        fence_proxy_async_smem();  // after the stage buffers' tensor copies
-        for (int v = lane; v < cnt * vps; v += 32) {
-            const int s = v / vps;
-            cp_async16(slots + v * 4, p.partials + sg.slot(s0 + s) * stride + (v - s * vps) * 4);
-        }
-        cp_async_wait_all();
-        __syncwarp();
-        merge_weights(slots, stride, cnt, GS, D, heads, lane);
-#pragma unroll
-        for (int k = 0; k < KPL; ++k) {
-            const int it = k * 32 + lane;
-            if (it < GS * Q)
-                merge_accumulate<D>(slots, stride, cnt, GS, heads, it / Q, it % Q, acc[k]);
-        }
-    }
+__device__ __noinline__ void merge_unit(const DecodeParams& p, const PendingMerge& pm, int sw,
+                                        int r, int lane) {
+    const UnitSegments us = unit_segments(sw, r, pm.u, pm.a, pm.nch);
+    const SlotSegs sg{p.partials, us.base, partial_slot_floats(GS, D), GS, D};
     const int units_per_b = p.n_kv_heads * p.sub_groups;
     const int b = pm.u / units_per_b;
     const int uidx = pm.u - b * units_per_b;
     const int h = uidx / p.sub_groups;
     const int sgi = uidx - h * p.sub_groups;
-#pragma unroll
-    for (int k = 0; k < KPL; ++k) {
-        const int it = k * 32 + lane;
-        if (it < GS * Q) {
-            const int g = it / Q;
-            if (g < p.rows.rows(sgi))
-                merge_store<T, D>(acc[k], heads, g, it % Q,
-                                  static_cast<T*>(p.out) + p.rows.row(b, h, sgi, g) * D);
-        }
-    }
+    T* out = static_cast<T*>(p.out);
+    merge_rows<T, D>(sg, us.count(), p.rows.rows(sgi), 0, 1, lane,
+                     [&](int g) { return out + p.rows.row(b, h, sgi, g) * D; });
 }
 
 // After a decode warp's main loop: report its split segments (at most two,
@@ -195,7 +161,7 @@ __device__ __noinline__ void merge_staged(const DecodeParams& p, const PendingMe
 template <typename T, int D, int GS>
 __device__ __forceinline__ void finish_pending(const DecodeParams& p, int npend,
                                                const PendingMerge& p0, const PendingMerge& p1,
-                                               int sw, int r, uint8_t* stage, int lane) {
+                                               int sw, int r, int lane) {
     __syncwarp();
     int old0 = 0, old1 = 0;
     if (lane == 0) {
@@ -212,8 +178,8 @@ __device__ __forceinline__ void finish_pending(const DecodeParams& p, int npend,
     old0 = __shfl_sync(kFull, old0, 0);
     old1 = __shfl_sync(kFull, old1, 0);
     __syncwarp();  // lane 0's acquire before the merges below
-    if (old0 + p0.chunks == p0.nch) merge_staged<T, D, GS>(p, p0, sw, r, stage, lane);
-    if (npend > 1 && old1 + p1.chunks == p1.nch) merge_staged<T, D, GS>(p, p1, sw, r, stage, lane);
+    if (old0 + p0.chunks == p0.nch) merge_unit<T, D, GS>(p, p0, sw, r, lane);
+    if (npend > 1 && old1 + p1.chunks == p1.nch) merge_unit<T, D, GS>(p, p1, sw, r, lane);
 }
 
 // Output rows of sequences with no tokens are zeros (no worker visits them).

@@ -274,7 +274,7 @@ def test_split_steps_equal_fused_call(case, variant):
         w = wl.make_random(21, batch=7, n_q_heads=16, n_kv_heads=4, head_dim=128, page_size=16,
                            dtype=torch.bfloat16, lens=[0, 3000, 0, 17, 900, 0, 4500],
                            device="cuda")
-    elif case == "long_split":  # one unit over many workers: several merge batches
+    elif case == "long_split":  # one unit over many workers: more than 32 segments
         w = wl.make_random(22, batch=1, n_q_heads=16, n_kv_heads=1, head_dim=128, page_size=16,
                            dtype=torch.bfloat16, lens=[60000], device="cuda")
     else:
