@@ -231,17 +231,13 @@ def copy_peak_gbs(torch, dev) -> float:
     return 2 * n * 2 / (best * 1e-3) / 1e9
 
 
-def cpu_oracle_sample(w, target_s: float = 12.0):
-    """Time the oracle on host copies of the workload: whole batches while they
-    fit in the budget, otherwise sequences one by one (all query heads)."""
+def _oracle_rate(w, q, kp, vp, target_s: float):
+    """Sequences one by one (all query heads), in a fixed random order, for
+    about target_s seconds: (bytes, sequences, seconds)."""
     import numpy as np
 
     import oracle
-    from paged_kv_decode_16_gb300 import workloads as wl
 
-    q = wl.to_bits(w.q)
-    kp, vp = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
-    cores = oracle.max_threads()
     per_tok = w.n_kv_heads * w.head_dim * 4
     seqs = 0
     nbytes = 0
@@ -256,11 +252,32 @@ def cpu_oracle_sample(w, target_s: float = 12.0):
                                  rows)
         seqs += 1
         nbytes += int(w.context_lens[b]) * per_tok + 2 * w.n_q_heads * w.head_dim * 2
-    dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "seqs_per_s": seqs / dt,
-            "sample": f"{seqs} sequences x all {w.n_q_heads} query heads of the {w.name} "
-                      f"workload, float64 oracle with OpenMP over query heads, {dt:.1f} s"}
+    return nbytes, seqs, time.perf_counter() - t0
+
+
+def cpu_oracle_sample(w, target_s: float = 12.0, one_core_s: float = 4.0):
+    """Time the oracle on host copies of the workload, on all host cores (the
+    reported value) and then on one core."""
+    import oracle
+    from paged_kv_decode_16_gb300 import workloads as wl
+
+    q = wl.to_bits(w.q)
+    kp, vp = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
+    cores = oracle.max_threads()
+    nbytes, seqs, dt = _oracle_rate(w, q, kp, vp, target_s)
+    res = {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "seqs_per_s": seqs / dt,
+           "sample": f"{seqs} sequences x all {w.n_q_heads} query heads of the {w.name} "
+                     f"workload, float64 oracle with OpenMP over query heads, {dt:.1f} s"}
+    if one_core_s > 0:
+        oracle.set_threads(1)
+        try:
+            nb1, s1, dt1 = _oracle_rate(w, q, kp, vp, one_core_s)
+        finally:
+            oracle.set_threads(cores)
+        res["one_core"] = {"value": nb1 / dt1 / 1e9, "unit": UNIT, "seqs_per_s": s1 / dt1,
+                           "sample": f"{s1} sequences, {dt1:.1f} s on 1 thread"}
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -283,11 +300,11 @@ def run_reference(args):
     # about 150 s in all: each step samples at least one sequence (a few ms)
     budget = min(12.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, target_s=budget)
+        cpu_oracle_sample(w, target_s=budget, one_core_s=0)
     vals, seqs = [], []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = cpu_oracle_sample(w, target_s=budget)
+        r = cpu_oracle_sample(w, target_s=budget, one_core_s=0)
         vals.append(r["value"])
         seqs.append(r["seqs_per_s"])
     wall = time.perf_counter() - t0

@@ -934,7 +934,6 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
     c.v_gs = ps.virt.gs;
     c.v_sub = ps.virt.sub_groups;
     c.v_nch = (prefix_tokens + 15) / 16;
-    // slots staged per batch: about 48 KiB of shared memory
     return cuda_status(pkv::launch_cascade_combine(dtype, head_dim, c, (int)ps.real.units, cs));
 }
 

@@ -135,22 +135,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Same, with an L2 eviction-priority policy (from createpolicy).
-__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start while the previous kernel in the
 // stream still runs; pdl_wait() blocks until that kernel has completed and its

@@ -372,7 +372,6 @@ decode_kernel(const DecodeParams p) {
         // refill: positions up to i + STAGES (stage i % STAGES is free again)
         while (issued <= i + STAGES && issue(issued)) ++issued;
     }
-    // every copy has landed and been consumed: the stage buffers serve the merges
     if (npend > 0)
         finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, lane);
 }

@@ -133,3 +133,32 @@ def test_multi_argument_checks():
     with pytest.raises(pkv.PagedKVError) as e:   # out overlapping q
         pkv.paged_decode_attention_multi(q, w.k_pool, w.v_pool, table, lens, w.scale, q, ws)
     assert e.value.name == "PKV_ERR_ALIAS"
+
+
+def test_multi_captured_in_cuda_graph_equals_eager():
+    """paged_decode_attention_multi recorded into a CUDA graph and replayed
+    gives the eager call's bits, and a replay sees new lengths and queries
+    written into the same buffers."""
+    w, q = _case(234, B=6, Qn=5, Hq=16, Hkv=4, D=128, P=16, dtype=torch.bfloat16,
+                 lens=[900, 7, 33, 0, 2048, 160])
+    table, lens, _ = to_dev(w)
+    eager, ws = _run(w, q)
+    out = torch.full_like(q, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pkv.paged_decode_attention_multi(q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    # new lengths within each row's pages (row 3 has none)
+    lens.copy_(torch.tensor([899, 7, 40, 0, 1500, 150], dtype=torch.int32))
+    q.mul_(-0.5)
+    g.replay()
+    torch.cuda.synchronize()
+    w.context_lens[:] = lens.cpu().numpy()
+    assert pkv.pkv_read_device_status(ws) == 0
+    assert_close(out, _oracle(w, q), what="replay with new lengths")

@@ -113,3 +113,26 @@ def test_prefix_argument_checks():
         pkv.paged_decode_attention_prefix(w.q, w.k_pool, w.v_pool, table, lens, w.scale, 64,
                                           torch.empty_like(w.q), ws[:1024])
     assert e.value.name == "PKV_ERR_WORKSPACE"
+
+
+def test_prefix_captured_in_cuda_graph_equals_eager():
+    """paged_decode_attention_prefix (six launches) recorded into a CUDA graph
+    and replayed gives the eager call's bits."""
+    w = _shared(11, B=12, Hq=32, Hkv=8, D=128, P=16, dtype=torch.bfloat16, prefix=512,
+                suffix_max=300)
+    eager, ws = _run(w, 512, pkv.VARIANT_AUTO)
+    table, lens, _ = to_dev(w)
+    out = torch.full_like(w.q, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pkv.paged_decode_attention_prefix(w.q, w.k_pool, w.v_pool, table, lens, w.scale, 512,
+                                              out, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert pkv.pkv_read_device_status(ws) == 0
