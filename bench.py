@@ -72,6 +72,10 @@ def parse_args():
     ap.add_argument("--profile-only", action="store_true",
                     help="only the warm-up and timed steps (for profiler captures): no copy "
                          "peak, clock sampling, end-to-end leg or CPU baseline")
+    ap.add_argument("--profile-path", choices=["step", "prefix"], default="step",
+                    help="with --profile-only: 'prefix' runs, on the prefix_sharing workload, "
+                         "warmup + steps calls of paged_decode_attention_prefix and then one "
+                         "paged_decode_attention (6 launches per call, then 3)")
     return ap.parse_args()
 
 
@@ -374,6 +378,30 @@ def run_ours(args):
         pkv.paged_decode_combine(out, w.n_kv_heads, ws, nw, variant=var)
 
     peak, peak_kind = measured_peak()
+    if args.profile_only and args.profile_path == "prefix":
+        wp = wl.make("prefix_sharing", seed=args.seed, device=dev)
+        tp = torch.from_numpy(wp.page_table).to(dev)
+        lp = torch.from_numpy(wp.context_lens).to(dev)
+        op = torch.empty_like(wp.q)
+        wsc = pkv.alloc_prefix_workspace(wp.batch, wp.n_q_heads, wp.n_kv_heads, wp.head_dim, nw,
+                                         device=dev, variant=var)
+        wsp = pkv.alloc_workspace(wp.batch, wp.n_q_heads, wp.n_kv_heads, wp.head_dim, nw,
+                                  device=dev, variant=var)
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_decode_attention_prefix(wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale,
+                                              wp.prefix_len, op, wsc, nw, variant=var)
+        pkv.paged_decode_attention(wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, op, wsp, nw,
+                                   variant=var)
+        torch.cuda.synchronize()
+        status = pkv.pkv_read_device_status(wsc) | pkv.pkv_read_device_status(wsp)
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "workload": "prefix_sharing",
+                              "path": "prefix", "steps": args.steps, "warmup": args.warmup,
+                              "device_status": status}))
+        pool.destroy()
+        if dist:
+            dist.destroy_process_group()
+        return 0 if status == 0 else 1
     if args.profile_only:
         for _ in range(args.warmup + args.steps):
             step()

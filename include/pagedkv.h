@@ -98,6 +98,18 @@ const char* pkv_status_string(pkv_status s);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pkv_version(void);
 
+/* Check of the failure path every copy wait of the decode kernels takes
+ * (Experimental LibTorch prefix cache, "Model and operation coverage": a
+ * pending producer held by a watchdog rather than waited on forever).  One
+ * warp polls, at most `tries` times, an mbarrier that nothing ever completes;
+ * when the polls run out it ORs PKV_DEV_TIMEOUT into *status (device, 4 bytes)
+ * and writes the wait's duration in ns to *elapsed_ns (device, may be NULL),
+ * then returns: nothing traps and the context stays usable.  The decode
+ * kernels give up the same way after 2^22 polls and report PKV_DEV_TIMEOUT
+ * through pkv_read_device_status.  tries == 0 or status NULL: INVALID_ARG. */
+pkv_status pkv_check_bounded_wait(uint32_t tries, uint32_t* status, unsigned long long* elapsed_ns,
+                                  pkv_stream stream);
+
 /* ------------------------------------------------------------------------
  * Page pool and host page allocator
  * (CacheIR, "Current Capabilities": persistent shared CUDA page-backed KV

@@ -24,6 +24,7 @@ __all__ = [
     "paged_decode_workspace_size", "paged_decode_step_rope", "paged_decode_attention_prefix",
     "paged_decode_prefix_workspace_size", "alloc_prefix_workspace", "DEV_BAD_PREFIX",
     "paged_decode_attention_multi", "paged_decode_multi_workspace_size", "alloc_multi_workspace",
+    "check_bounded_wait",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
     "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
@@ -90,6 +91,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, V], I),
         "paged_decode_prefix_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_multi_workspace_size": ([I, I, I, I, I, I, I, ctypes.POINTER(Z)], I),
+        "pkv_check_bounded_wait": ([ctypes.c_uint32, V, V, V], I),
         "paged_decode_attention_multi": ([V, V, V, V, I, V, I, I, I, I, I, I, I, I, F, V, V, Z, I,
                                           I, V], I),
         "paged_decode_attention_prefix": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, I, V, V, Z,
@@ -445,6 +447,17 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
         int(variant), _stream(stream)),
         "paged_decode_attention_no_alloc")
     return out
+
+
+def check_bounded_wait(tries: int, stream=None) -> tuple[int, int]:
+    """One bounded wait that never succeeds (pkv_check_bounded_wait): returns
+    (device status bits, wait duration in ns) once it has given up."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ns = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(load_library().pkv_check_bounded_wait(int(tries), _ptr(st), _ptr(ns), _stream(stream)),
+           "pkv_check_bounded_wait")
+    torch.cuda.synchronize()
+    return int(st.item()) & 0xFFFFFFFF, int(ns.item())
 
 
 def paged_decode_multi_workspace_size(batch: int, n_queries: int, n_q_heads: int,

@@ -482,6 +482,13 @@ const char* pkv_status_string(pkv_status s) {
 
 int pkv_version(void) { return 200; }
 
+pkv_status pkv_check_bounded_wait(uint32_t tries, uint32_t* status, unsigned long long* elapsed_ns,
+                                  pkv_stream stream) {
+    if (!status || tries == 0) return PKV_ERR_INVALID_ARG;
+    return cuda_status(pkv::launch_wait_check(tries, status, elapsed_ns,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
                      const int32_t* page_table, int table_stride, const int32_t* positions,
                      int batch, uint32_t* dev_status, pkv_stream stream) {

@@ -116,9 +116,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+// Bounded wait for the phase with the given parity to complete: false after
+// `tries` failed polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t tries = kSpinLimit) {
+    for (uint32_t it = 0; it < tries; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
     }
     return false;

@@ -457,6 +457,35 @@ cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeA
 }
 
 // ---------------------------------------------------------------------------
+// Check of the give-up path of the copy waits: one warp waits, bounded, on an
+// mbarrier that nothing ever completes; when the tries run out it records
+// PKV_DEV_TIMEOUT and the elapsed time, and returns.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(32)
+wait_check_kernel(uint32_t tries, uint32_t* status, unsigned long long* elapsed_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    unsigned long long t0, t1;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    const bool done = mbar_wait_bounded(&bar, 0u, tries);  // phase 0 never completes
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+    if (threadIdx.x == 0) {
+        if (!done) set_status(status, PKV_DEV_TIMEOUT);
+        if (elapsed_ns) *elapsed_ns = t1 - t0;
+    }
+}
+
+cudaError_t launch_wait_check(uint32_t tries, uint32_t* status, unsigned long long* elapsed_ns,
+                              cudaStream_t stream) {
+    wait_check_kernel<<<1, 32, 0, stream>>>(tries, status, elapsed_ns);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Stand-alone append: one thread per 16-byte vector of the new rows.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)

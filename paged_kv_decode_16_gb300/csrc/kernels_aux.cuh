@@ -89,6 +89,10 @@ cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeA
 
 cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status, cudaStream_t stream);
 
+// One bounded wait that never succeeds (see pkv_check_bounded_wait).
+cudaError_t launch_wait_check(uint32_t tries, uint32_t* status, unsigned long long* elapsed_ns,
+                              cudaStream_t stream);
+
 // Rotary embedding of q and k_new, then the append (stand-alone launch).
 cudaError_t launch_rope_append(const AppendArgs& a, int batch, int head_dim, uint32_t* status,
                                cudaStream_t stream);

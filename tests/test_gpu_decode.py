@@ -401,3 +401,22 @@ def test_step_captured_in_cuda_graph_equals_eager(variant):
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert pkv.pkv_read_device_status(ws) == 0
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """The give-up path of the copy waits: a wait on an mbarrier that nothing
+    completes ends after its polls with PKV_DEV_TIMEOUT (no trap, no hang),
+    the wait's length grows with the poll count, and decoding right after it
+    on the same context is correct."""
+    st, ns_short = pkv.check_bounded_wait(1000)
+    assert st == pkv.DEV_TIMEOUT
+    st, ns_long = pkv.check_bounded_wait(20000)
+    assert st == pkv.DEV_TIMEOUT
+    assert 0 < ns_short < ns_long < 5_000_000_000
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.check_bounded_wait(0)
+    assert e.value.name == "PKV_ERR_INVALID_ARG"
+    w = wl.make("tiny", seed=9, device="cuda")
+    out, ws, status = run_gpu(w, append=False)
+    assert status == 0
+    assert_close(out, oracle_full(w, append=False), strict=True, what="after the timeout check")
