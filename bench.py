@@ -75,7 +75,7 @@ def parse_args():
     ap.add_argument("--profile-path", choices=["step", "prefix"], default="step",
                     help="with --profile-only: 'prefix' runs, on the prefix_sharing workload, "
                          "warmup + steps calls of paged_decode_attention_prefix and then one "
-                         "paged_decode_attention (6 launches per call, then 3)")
+                         "paged_decode_attention (4 launches per call, then 3)")
     return ap.parse_args()
 
 

@@ -399,8 +399,9 @@ pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const in
  * most table_stride * page_size (INVALID_ARG); every context_lens[b] >=
  * prefix_tokens (else PKV_DEV_BAD_LEN); rows that do not start with row 0's
  * prefix pages set PKV_DEV_BAD_PREFIX (their results are then wrong).  Both
- * read through pkv_read_device_status(workspace).  Six launches (two plans, a
- * query gather, two decodes, the merge).
+ * read through pkv_read_device_status(workspace).  Four launches: one holding
+ * both plans, the query gather and the prefix check; the two decodes; the
+ * merge.
  * ------------------------------------------------------------------------ */
 pkv_status paged_decode_prefix_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                                               int head_dim, int num_workers,

@@ -283,21 +283,18 @@ pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dt
     return PKV_OK;
 }
 
-pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch, int page_size,
-                   int table_stride, int num_workers, void* workspace, const DecodeSetup& s,
-                   const pkv::AppendArgs* append, cudaStream_t stream, int skip_cols = 0,
-                   int uniform_len = -1, const int32_t* share_table = nullptr,
-                   int share_rows = 0, int share_cols = 0) {
+// The plan inputs of one decode.  skip_cols: the decoded range starts
+// skip_cols table columns into each row (table points at that column) and the
+// lengths count from the row's start; uniform_len >= 0: every sequence has
+// this length and context_lens is not read.
+pkv::PlanArgs plan_args(const int32_t* context_lens, const int32_t* table, int batch,
+                        int page_size, int table_stride, int num_workers, void* workspace,
+                        const DecodeSetup& s, int skip_cols = 0, int uniform_len = -1) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     pkv::PlanArgs pa;
     pa.lens = context_lens;
-    // skip_cols: the decoded range starts skip_cols table columns into each row
-    // (table points at that column); lengths count from the row's start
     pa.len_offset = skip_cols * page_size;
-    pa.uniform_len = uniform_len;      // >= 0: every sequence has this length (lens unused)
-    pa.share_table = share_table;      // rows 1.. must start with row 0's first share_cols ids
-    pa.share_rows = share_rows;
-    pa.share_cols = share_cols;
+    pa.uniform_len = uniform_len;
     pa.batch = batch;
     pa.units_per_b = s.units_per_b;
     pa.cap = (long long)(table_stride - skip_cols) * page_size;
@@ -313,7 +310,15 @@ pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch,
     pa.table = table;
     pa.table_stride = table_stride;
     pa.page_size = page_size;
-    return cuda_status(pkv::launch_plan(pa, append, stream));
+    return pa;
+}
+
+pkv_status do_plan(const int32_t* context_lens, const int32_t* table, int batch, int page_size,
+                   int table_stride, int num_workers, void* workspace, const DecodeSetup& s,
+                   const pkv::AppendArgs* append, cudaStream_t stream) {
+    return cuda_status(pkv::launch_plan(plan_args(context_lens, table, batch, page_size,
+                                                  table_stride, num_workers, workspace, s),
+                                        append, stream));
 }
 
 pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
@@ -902,19 +907,26 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int skip = prefix_tokens / page_size;
     const int hq_v = (int)((long long)batch * ps.real.group * n_kv_heads);
-    // plans: the prefix (one sequence of prefix_tokens, read through row 0, with
-    // the check that every row starts with row 0's prefix pages) and the
-    // suffixes (each row from column skip on, lengths minus prefix_tokens)
-    if ((st = do_plan(nullptr, page_table, 1, page_size, table_stride, num_workers, ws_v, ps.virt,
-                      nullptr, cs, 0, prefix_tokens)) != PKV_OK)
-        return st;
-    if ((st = do_plan(context_lens, page_table + skip, batch, page_size, table_stride, num_workers,
-                      ws_s, ps.real, nullptr, cs, skip, -1, page_table, batch, skip)) != PKV_OK)
-        return st;
+    // one launch: the plans of the suffixes (each row from column skip on,
+    // lengths minus prefix_tokens) and of the prefix (one sequence of
+    // prefix_tokens read through row 0), the gather of the query rows per KV
+    // head, and the check that every row starts with row 0's prefix pages
+    const pkv::PlanArgs pv = plan_args(nullptr, page_table, 1, page_size, table_stride,
+                                       num_workers, ws_v, ps.virt, 0, prefix_tokens);
+    const pkv::PlanArgs pss = plan_args(context_lens, page_table + skip, batch, page_size,
+                                        table_stride, num_workers, ws_s, ps.real, skip);
+    pkv::CascadeGather g;
+    g.q = static_cast<const uint4*>(q);
+    g.qv = static_cast<uint4*>(qv);
+    g.batch = batch;
+    g.n_kv_heads = n_kv_heads;
+    g.group = ps.real.group;
+    g.vecs = head_dim / 8;
+    g.table = page_table;
+    g.table_stride = table_stride;
+    g.share_cols = skip;
+    if ((st = cuda_status(pkv::launch_cascade_plan(pss, pv, g, cs))) != PKV_OK) return st;
     uint32_t* call_status = &reinterpret_cast<WsHeader*>(ws_s)->status;
-    if ((st = cuda_status(pkv::launch_gather_q(q, qv, batch, n_kv_heads, ps.real.group, head_dim,
-                                               cs))) != PKV_OK)
-        return st;
     if ((st = do_run(qv, k_pool, v_pool, page_table, table_stride, 1, hq_v, n_kv_heads, head_dim,
                      page_size, num_pages, dtype, scale, out, ws_v, ps.virt, false, cs, true,
                      call_status)) != PKV_OK)

@@ -184,10 +184,9 @@ __device__ uint32_t rope_append_cta(const AppendArgs& a, int batch, int head_dim
 // unit of the sequence), the total, the worker count, and this call's status.
 // Append CTA k writes its own status slot, so no clearing race exists.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024)
-plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
-    pdl_wait();
-    pdl_trigger();
+// The plan of one decode (one CTA of 1024 threads); status_slots: the number
+// of append_status entries other CTAs of the launch write.
+__device__ void plan_cta(const PlanArgs& pa, int status_slots) {
     __shared__ int warp_tot[32];
     __shared__ long long running;
     __shared__ uint32_t flags;
@@ -196,38 +195,14 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
     const bool prefix_smem = pa.batch <= kPlanSmemSeqs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
+    const int append_ctas = status_slots;
     if (tid == 0) {
         running = 0;
         flags = 0;
     }
     __syncthreads();
-    if (blockIdx.x > 0) {
-        uint32_t f = 0;
-        if (aa.q_in) {  // rotary embedding, then the append
-            __shared__ float s_rope[2 * kRopeThreads];
-            f = rope_append_cta(aa, pa.batch, aa.vecs * 8, blockIdx.x - 1, append_ctas, s_rope);
-        } else {
-            const long long total = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
-            for (long long idx = (long long)(blockIdx.x - 1) * blockDim.x + tid; idx < total;
-                 idx += (long long)append_ctas * blockDim.x)
-                f |= append_vec(aa, idx);
-        }
-        if (f) atomicOr(&flags, f);
-        __syncthreads();
-        if (tid == 0) pa.hdr->append_status[blockIdx.x - 1] = flags;
-        return;
-    }
     if (pa.unit_done)
         for (long long x = tid; x < pa.units; x += blockDim.x) pa.unit_done[x] = 0;
-    if (pa.share_table) {  // every row must start with row 0's prefix pages
-        bool differs = false;
-#pragma unroll 4
-        for (long long x = tid; x < (long long)pa.share_rows * pa.share_cols; x += blockDim.x) {
-            const long long r = x / pa.share_cols, c = x - r * pa.share_cols;
-            differs |= __ldg(pa.share_table + r * pa.table_stride + c) != __ldg(pa.share_table + c);
-        }
-        if (differs) atomicOr(&flags, PKV_DEV_BAD_PREFIX);
-    }
     for (int base = 0; base < pa.batch; base += blockDim.x) {
         const int b = base + tid;
         int cnt = 0;
@@ -323,6 +298,74 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
         pa.wstart[w] = seq_of(w < nw ? range_begin(w, sw, r) : T - 1);
 }
 
+__global__ void __launch_bounds__(1024)
+plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0) {
+        plan_cta(pa, append_ctas);
+        return;
+    }
+    __shared__ uint32_t flags;
+    if (threadIdx.x == 0) flags = 0;
+    __syncthreads();
+    uint32_t f = 0;
+    if (aa.q_in) {  // rotary embedding, then the append
+        __shared__ float s_rope[2 * kRopeThreads];
+        f = rope_append_cta(aa, pa.batch, aa.vecs * 8, blockIdx.x - 1, append_ctas, s_rope);
+    } else {
+        const long long total = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
+        for (long long idx = (long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; idx < total;
+             idx += (long long)append_ctas * blockDim.x)
+            f |= append_vec(aa, idx);
+    }
+    if (f) atomicOr(&flags, f);
+    __syncthreads();
+    if (threadIdx.x == 0) pa.hdr->append_status[blockIdx.x - 1] = flags;
+}
+
+// Plan launch of the shared-prefix decode: CTA 0 plans the suffix pass, CTA 1
+// the prefix pass; CTAs 2 .. 2+k-1 gather the query rows of every KV head in
+// sequence-major order (qv[h][b*G + g] = q[b][h*G + g]) and check that every
+// table row starts with row 0's prefix pages (PKV_DEV_BAD_PREFIX into the
+// suffix header's status slot of the CTA).
+__global__ void __launch_bounds__(1024)
+cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0) {
+        plan_cta(ps, k);
+        return;
+    }
+    if (blockIdx.x == 1) {
+        plan_cta(pv, 0);
+        return;
+    }
+    const int c = blockIdx.x - 2;
+    const long long stride = (long long)k * blockDim.x;
+    const long long total = (long long)g.batch * g.n_kv_heads * g.group * g.vecs;
+    for (long long idx = (long long)c * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int vec = (int)(idx % g.vecs);
+        const long long row = idx / g.vecs;  // (h * B + b) * G + gi in qv
+        const int gi = (int)(row % g.group);
+        const long long hb = row / g.group;
+        const int b = (int)(hb % g.batch), h = (int)(hb / g.batch);
+        g.qv[idx] = g.q[(((long long)b * g.n_kv_heads + h) * g.group + gi) * g.vecs + vec];
+    }
+    bool differs = false;
+    const long long cells = (long long)(g.batch - 1) * g.share_cols;
+    for (long long x = (long long)c * blockDim.x + threadIdx.x; x < cells; x += stride) {
+        const long long r = 1 + x / g.share_cols, col = x - (r - 1) * g.share_cols;
+        differs |= __ldg(g.table + r * g.table_stride + col) != __ldg(g.table + col);
+    }
+    __shared__ int any;
+    if (threadIdx.x == 0) any = 0;
+    __syncthreads();
+    if (differs) any = 1;
+    __syncthreads();
+    if (threadIdx.x == 0) ps.hdr->append_status[c] = any ? PKV_DEV_BAD_PREFIX : 0u;
+}
+
 // ---------------------------------------------------------------------------
 // Combine: one CTA per unit (sequence, KV head, sub-group); units finished by
 // a single worker and empty sequences exit at once.  Each warp merges rows of
@@ -413,32 +456,6 @@ cascade_combine_kernel(CascadeArgs c) {
                          SlotSegs{c.s_partials, sv.base, partial_slot_floats(gs, D), gs, D}};
     merge_rows<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
                      [&](int g) { return o + (long long)g * D; });
-}
-
-__global__ void __launch_bounds__(256)
-gather_q_kernel(const uint4* __restrict__ q, uint4* __restrict__ qv, int batch, int n_kv_heads,
-                int group, int vecs) {
-    pdl_wait();
-    pdl_trigger();
-    const long long total = (long long)batch * n_kv_heads * group * vecs;
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= total) return;
-    const int vec = (int)(idx % vecs);
-    const long long row = idx / vecs;  // (h * B + b) * G + g in qv
-    const int g = (int)(row % group);
-    const long long hb = row / group;
-    const int b = (int)(hb % batch), h = (int)(hb / batch);
-    qv[idx] = q[(((long long)b * n_kv_heads + h) * group + g) * vecs + vec];
-}
-
-cudaError_t launch_gather_q(const void* q, void* qv, int batch, int n_kv_heads, int group,
-                            int head_dim, cudaStream_t stream) {
-    const int vecs = head_dim / 8;
-    const long long total = (long long)batch * n_kv_heads * group * vecs;
-    if (total == 0) return cudaSuccess;
-    return launch_pdl(gather_q_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256), 0,
-                      stream, static_cast<const uint4*>(q), static_cast<uint4*>(qv), batch,
-                      n_kv_heads, group, vecs);
 }
 
 cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeArgs& c,
@@ -551,6 +568,15 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
     }
     return launch_pdl(plan_kernel, dim3(1 + append_ctas), dim3(1024), 0, stream, pa, aa,
                       append_ctas);
+}
+
+cudaError_t launch_cascade_plan(const PlanArgs& ps, const PlanArgs& pv, const CascadeGather& g,
+                                cudaStream_t stream) {
+    // gather + check CTAs: about 4 K vectors (64 KiB of q) each, at most kMaxAppendCtas
+    const long long total = (long long)g.batch * g.n_kv_heads * g.group * g.vecs;
+    int k = (int)((total + 4095) / 4096);
+    k = k < 1 ? 1 : (k > kMaxAppendCtas ? kMaxAppendCtas : k);
+    return launch_pdl(cascade_plan_kernel, dim3(2 + k), dim3(1024), 0, stream, ps, pv, g, k);
 }
 
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,

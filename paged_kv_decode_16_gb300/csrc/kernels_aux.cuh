@@ -13,8 +13,6 @@ struct PlanArgs {
     const int32_t* lens;   // [B] context lengths (caller)
     int len_offset;        // tokens before the decoded range (lengths below it are flagged)
     int uniform_len;       // >= 0: every sequence has this length and lens is not read
-    const int32_t* share_table;  // nullable: check rows 1 .. share_rows-1 of this table start
-    int share_rows, share_cols;  // with row 0's first share_cols page ids (PKV_DEV_BAD_PREFIX)
     int batch;
     int units_per_b;       // Hkv * sub_groups
     long long cap;         // table_stride * page_size
@@ -79,10 +77,19 @@ struct CascadeArgs {
     int v_gs, v_sub, v_nch;                              // virtual units per KV head, chunks
 };
 
-// qv[h][b * G + g][:] = q[b][h * G + g][:]: the query rows of each KV head
-// gathered in sequence-major order (the prefix pass's virtual heads).
-cudaError_t launch_gather_q(const void* q, void* qv, int batch, int n_kv_heads, int group,
-                            int head_dim, cudaStream_t stream);
+// The query gather and prefix check of the shared-prefix decode's plan launch.
+struct CascadeGather {
+    const uint4* q;        // [B][Hkv * G][D] as 16-byte vectors
+    uint4* qv;             // [Hkv][B * G][D]: qv[h][b*G + g] = q[b][h*G + g]
+    int batch, n_kv_heads, group, vecs;
+    const int32_t* table;  // rows 1 .. B-1 must start with row 0's first share_cols ids
+    int table_stride, share_cols;
+};
+
+// One launch: the suffix pass's plan (ps, whose header receives the check's
+// status slots), the prefix pass's plan (pv), and the gather + check.
+cudaError_t launch_cascade_plan(const PlanArgs& ps, const PlanArgs& pv, const CascadeGather& g,
+                                cudaStream_t stream);
 
 cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeArgs& c,
                                    int units, cudaStream_t stream);

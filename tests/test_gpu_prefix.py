@@ -116,7 +116,7 @@ def test_prefix_argument_checks():
 
 
 def test_prefix_captured_in_cuda_graph_equals_eager():
-    """paged_decode_attention_prefix (six launches) recorded into a CUDA graph
+    """paged_decode_attention_prefix (four launches) recorded into a CUDA graph
     and replayed gives the eager call's bits."""
     w = _shared(11, B=12, Hq=32, Hkv=8, D=128, P=16, dtype=torch.bfloat16, prefix=512,
                 suffix_max=300)
