@@ -53,6 +53,8 @@ struct SlotSegs {
     __device__ __forceinline__ const float* l(int s, int g) const { return m(s, g) + gs; }
 };
 
+constexpr int kMergeBlock = 8;  // segments whose loads are in flight together
+
 struct MergeRow {
     float M, den;
     float w;  // ns <= 32: the weight of segment `lane` (0 past ns)
@@ -112,16 +114,28 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
         const MergeRow mr = merge_row(sg, ns, g, lane);
         const bool act = lane < Q;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int s = 0; s < ns; ++s) {
-            const float w = ns <= 32 ? __shfl_sync(kFull, mr.w, s)
-                                     : merge_weight(__ldcg(sg.m(s, g)), mr.M);
-            if (act) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(sg.o(s, g)) + lane);
-                x.x = fmaf(w, v.x, x.x);
-                x.y = fmaf(w, v.y, x.y);
-                x.z = fmaf(w, v.z, x.z);
-                x.w = fmaf(w, v.w, x.w);
+        // blocks of kMergeBlock segments: every load of a block is issued
+        // before the first multiply-add waits on one
+        for (int s0 = 0; s0 < ns; s0 += kMergeBlock) {
+            float4 v[kMergeBlock];
+            float w[kMergeBlock];
+#pragma unroll
+            for (int j = 0; j < kMergeBlock; ++j) {
+                const int s = s0 + j;
+                v[j] = act && s < ns
+                           ? __ldcg(reinterpret_cast<const float4*>(sg.o(s, g)) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                w[j] = s >= ns ? 0.f
+                       : ns <= 32 ? __shfl_sync(kFull, mr.w, s & 31)
+                                  : merge_weight(__ldcg(sg.m(s, g)), mr.M);
+            }
+#pragma unroll
+            for (int j = 0; j < kMergeBlock; ++j) {
+                if (s0 + j >= ns) break;
+                x.x = fmaf(w[j], v[j].x, x.x);
+                x.y = fmaf(w[j], v[j].y, x.y);
+                x.z = fmaf(w[j], v[j].z, x.z);
+                x.w = fmaf(w[j], v[j].w, x.w);
             }
         }
         if (act) merge_store<T, D>(x, mr.den, lane, out_rows(g));
