@@ -507,25 +507,31 @@ def run_ours(args):
     QN = 4
     multi = None
     if var != pkv.VARIANT_CUDA_CORES:
-        gq = torch.Generator(device=dev).manual_seed(args.seed + 1)
-        qm = torch.randn(B, QN, w.n_q_heads, w.head_dim, generator=gq, device=dev,
-                         dtype=torch.float32).to(w.dtype)
-        om = torch.empty_like(qm)
-        wsm = pkv.alloc_multi_workspace(B, QN, w.n_q_heads, w.n_kv_heads, w.head_dim, nw,
-                                        device=dev, variant=var)
-        multi_ms = timed_loop(lambda: pkv.paged_decode_attention_multi(
-            qm, w.k_pool, w.v_pool, table, lens, w.scale, om, wsm, nw, variant=var), KP)
+        def multi_ms_for(qn):
+            gq = torch.Generator(device=dev).manual_seed(args.seed + qn)
+            qm = torch.randn(B, qn, w.n_q_heads, w.head_dim, generator=gq, device=dev,
+                             dtype=torch.float32).to(w.dtype)
+            om = torch.empty_like(qm)
+            wsm = pkv.alloc_multi_workspace(B, qn, w.n_q_heads, w.n_kv_heads, w.head_dim, nw,
+                                            device=dev, variant=var)
+            return timed_loop(lambda: pkv.paged_decode_attention_multi(
+                qm, w.k_pool, w.v_pool, table, lens, w.scale, om, wsm, nw, variant=var), KP)
+
+        multi_ms = multi_ms_for(QN)
+        multi8_ms = multi_ms_for(8)
         one_ms = timed_loop(lambda: pkv.paged_decode_attention(
             w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws, nw, variant=var), KP)
         mbytes = by["kv_unique"] + QN * by["qo"]
         multi = {"what": f"paged_decode_attention_multi with {QN} causal query tokens per "
                          "sequence (each K/V chunk read once for all of them) vs "
-                         "paged_decode_attention with one, same cache",
+                         "paged_decode_attention with one, same cache; 8 tokens: units of "
+                         "32 rows, two m16 tiles per warp",
                  "n_queries": QN, "ms_multi": multi_ms, "ms_one_query": one_ms, "steps": KP,
                  "gbs_multi": mbytes / (multi_ms * 1e-3) / 1e9,
                  "tokens_per_s_multi": B * QN / (multi_ms * 1e-3),
-                 "tokens_per_s_one_query": B / (one_ms * 1e-3)}
-        del qm, om, wsm
+                 "tokens_per_s_one_query": B / (one_ms * 1e-3),
+                 "ms_multi_8": multi8_ms,
+                 "tokens_per_s_multi_8": B * 8 / (multi8_ms * 1e-3)}
 
     # ---- the decode kernel alone: events around its launch on its stream ----
     KD = max(1, min(K, 2000))

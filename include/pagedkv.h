@@ -426,11 +426,12 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
  * of sequence b are its last ones (already in the cache), so query j stands at
  * position context_lens[b] - n_queries + j and attends causally to tokens
  * 0 .. context_lens[b] - n_queries + j; a query with no such token (when
- * context_lens[b] < n_queries - j) gives zeros.  A unit of work is one m16
- * tile of query rows: the queries are cut into the fewest tiles of at most 16
- * tokens (equal sizes but the last), and a tile of t tokens takes the most
- * heads h of the GQA group with t * h <= 16; every K/V chunk of a KV head is
- * read once per (tile, head block).  1 <= n_queries <= 64 (else UNSUPPORTED);
+ * context_lens[b] < n_queries - j) gives zeros.  A unit of work is the query
+ * rows one warp serves, up to 32 (two m16 tiles sharing each K/V chunk): the
+ * queries are cut into the fewest tiles of at most 32 tokens (equal sizes but
+ * the last), and a tile of t tokens takes the most heads h of the GQA group
+ * with t * h <= 32; every K/V chunk of a KV head is read once per (tile, head
+ * block).  1 <= n_queries <= 64 (else UNSUPPORTED);
  * tensor-core variant only (CUDA_CORES: UNSUPPORTED).  n_queries = 1 is
  * paged_decode_attention.  Three launches.
  * ------------------------------------------------------------------------ */

@@ -186,16 +186,20 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     s->group = n_q_heads / n_kv_heads;
     const int max_gs = v == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
     if (n_queries > 1) {
-        // rows of a unit (one m16 tile): the queries split into the fewest
-        // tiles of at most 16 tokens, of equal size but the last, times the
-        // most heads of the group that still fit 16 rows
+        // rows of a unit (one warp: one m16 tile, or two): the queries split
+        // into the fewest tiles of at most kUnitRows tokens, of equal size but
+        // the last, times the most heads of the group that still fit kUnitRows
+        // rows; units of more than 16 rows run on the two-tile kernel
         if (v != PKV_VARIANT_TENSOR_CORES || n_queries > kMaxQueries) return PKV_ERR_UNSUPPORTED;
-        const int qpu = (n_queries + (n_queries + 15) / 16 - 1) / ((n_queries + 15) / 16);
+        constexpr int kUnitRows = 32;
+        const int t0 = (n_queries + kUnitRows - 1) / kUnitRows;
+        const int qpu = (n_queries + t0 - 1) / t0;
         const int tiles = (n_queries + qpu - 1) / qpu;
         int hpu = 1;
         for (int d = 1; d <= s->group; ++d)
-            if (s->group % d == 0 && qpu * d <= 16) hpu = d;
-        s->gs = qpu * hpu;
+            if (s->group % d == 0 && qpu * d <= kUnitRows) hpu = d;
+        const int rows = qpu * hpu;
+        s->gs = rows > 16 ? 32 : rows;
         s->sub_groups = (s->group / hpu) * tiles;
         s->rs = pkv::RowShape{n_queries, qpu, hpu, s->group / hpu, s->group, n_q_heads};
     } else if (force_gs > 0) {  // a sub-group size chosen by the caller (divides the group)
@@ -839,6 +843,9 @@ pkv_status setup_prefix(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     pkv_status st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype,
                                  num_workers, variant, &ps->real);
     if (st != PKV_OK) return st;
+    // virtual units of up to one m16 tile (16 rows) on tensor cores, 8 on CUDA
+    // cores (32-row units, two tiles per warp, measured slower here: the pass
+    // is not limited by its L2 re-reads of the prefix)
     const int max_gs = resolve_variant(variant) == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
     const long long group_v = (long long)batch * ps->real.group;
     if (group_v * n_kv_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;

@@ -22,6 +22,7 @@ DecodeMmaInfo decode_mma_info_bf16_d64(int gs) {
         case 14: return make_decode_mma_info<T, 64, 14>();
         case 15: return make_decode_mma_info<T, 64, 15>();
         case 16: return make_decode_mma_info<T, 64, 16>();
+        case 32: return make_decode_mma_info<T, 64, 32>();  // two tiles of 16 rows
     }
     return DecodeMmaInfo{nullptr, 0, 0, 0, 0};
 }

@@ -22,6 +22,7 @@ DecodeMmaInfo decode_mma_info_f16_d128(int gs) {
         case 14: return make_decode_mma_info<T, 128, 14>();
         case 15: return make_decode_mma_info<T, 128, 15>();
         case 16: return make_decode_mma_info<T, 128, 16>();
+        case 32: return make_decode_mma_info<T, 128, 32>();  // two tiles of 16 rows
     }
     return DecodeMmaInfo{nullptr, 0, 0, 0, 0};
 }
