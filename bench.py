@@ -533,6 +533,29 @@ def run_ours(args):
                  "ms_multi_8": multi8_ms,
                  "tokens_per_s_multi_8": B * 8 / (multi8_ms * 1e-3)}
 
+    # ---- the same step on the other full-size workloads: one sequence-long
+    # context per (sequence, KV head) split over many warps, and the mixed
+    # batch whose append writes position L and attends L + 1 tokens ----
+    others = {}
+    for oname in ("long_context", "mixed_append"):
+        w2 = wl.make(oname, seed=args.seed, device=dev)
+        t2 = torch.from_numpy(w2.page_table).to(dev)
+        l2 = torch.from_numpy(w2.context_lens).to(dev)
+        p2 = torch.from_numpy(w2.positions).to(dev)
+        o2 = torch.empty_like(w2.q)
+        ws2 = pkv.alloc_workspace(w2.batch, w2.n_q_heads, w2.n_kv_heads, w2.head_dim, nw,
+                                  device=dev, variant=var)
+        ms2 = timed_loop(lambda: pkv.paged_decode_step(
+            w2.k_new, w2.v_new, p2, w2.q, w2.k_pool, w2.v_pool, t2, l2, w2.scale, o2, ws2, nw,
+            variant=var), KP)
+        b2 = step_bytes(w2)
+        others[oname] = {
+            "ms_per_step": ms2, "value": aggregate_gbs(world, b2["step"], ms2), "unit": UNIT,
+            "pct_of_peak": 100.0 * b2["step"] / (ms2 * 1e-3) / 1e9 / peak, "steps": KP,
+            "batch": w2.batch, "bytes_per_step": b2["step"],
+            "device_status": pkv.pkv_read_device_status(ws2)}
+        del w2, t2, l2, p2, o2, ws2
+
     # ---- the decode kernel alone: events around its launch on its stream ----
     KD = max(1, min(K, 2000))
     dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
@@ -653,6 +676,7 @@ def run_ours(args):
             "gbs_logical_prefix": (pby["kv_logical"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
             "gbs_logical_plain": (pby["kv_logical"] + pby["qo"]) / (plain_ms * 1e-3) / 1e9},
         "multi_query": multi,
+        "other_workloads": others,
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "device_status": status,
