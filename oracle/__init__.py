@@ -82,7 +82,9 @@ class Oracle:
                                                       i32, i32, i32, ctypes.c_double, P]
         lib.pkv_oracle_paged_decode_multi.restype = ctypes.c_int
         lib.pkv_oracle_rope.argtypes = [P, P, i32, i32, i32, ctypes.c_double, i32, P, P]
-        for name in ("pkv_oracle_encode_array", "pkv_oracle_rope"):
+        lib.pkv_oracle_norm_rope.argtypes = [P, P, i32, i32, i32, P, ctypes.c_double,
+                                             ctypes.c_double, i32, P, P]
+        for name in ("pkv_oracle_encode_array", "pkv_oracle_rope", "pkv_oracle_norm_rope"):
             getattr(lib, name).restype = ctypes.c_int
         for name in ("pkv_oracle_decode_array", "pkv_oracle_paged_decode",
                      "pkv_oracle_paged_decode_rows", "pkv_oracle_kv_append",
@@ -184,6 +186,25 @@ class Oracle:
                                         _ptr(out), _ptr(f64) if with_f64 else None), "rope")
         return (out, f64) if with_f64 else out
 
+    def norm_rope(self, x, positions, weight, eps: float, theta: float, dtype: str,
+                  with_f64: bool = False):
+        """Per-head RMS norm (weight [D], 16-bit patterns) then the rotary
+        embedding of rows x [B, H, D] at positions[b]; one rounding at the end.
+        Returns the rows as 16-bit patterns, plus the float64 values when
+        with_f64."""
+        xb = _u16(x)
+        pos = _i32(positions)
+        wb = _u16(weight)
+        B, H, D = xb.shape
+        if wb.shape != (D,):
+            raise ValueError("weight must hold head_dim values")
+        out = np.empty(xb.shape, dtype=np.uint16)
+        f64 = np.empty(xb.shape, dtype=np.float64) if with_f64 else None
+        _check(self.lib.pkv_oracle_norm_rope(_ptr(xb), _ptr(pos), B, H, D, _ptr(wb), float(eps),
+                                             float(theta), DTYPES[dtype], _ptr(out),
+                                             _ptr(f64) if with_f64 else None), "norm_rope")
+        return (out, f64) if with_f64 else out
+
     def kv_append(self, k_pool, v_pool, k_new, v_new, page_table, positions):
         """Return copies of (k_pool, v_pool) with the new rows written in.
 
@@ -258,6 +279,10 @@ def encode(*a, **k) -> np.ndarray:
 
 def rope(*a, **k):
     return get().rope(*a, **k)
+
+
+def norm_rope(*a, **k):
+    return get().norm_rope(*a, **k)
 
 
 def gather(*a, **k) -> np.ndarray:

@@ -183,6 +183,56 @@ int pkv_oracle_rope(const uint16_t* x, const int32_t* positions, int batch, int 
     return ORC_OK;
 }
 
+/*
+ * Per-head RMS normalisation of q or k before the rotary embedding (the
+ * Q/K-normalised decoders of Experimental LibTorch prefix cache, "Current
+ * execution limits": normalised keys written straight into the attention
+ * arenas).  Row x of head_dim elements becomes
+ *     n_d = x_d * w_d / sqrt(mean_d(x_d^2) + eps),
+ * which is then turned exactly as pkv_oracle_rope turns its rows, at
+ * positions[b]; one rounding to the storage format at the end.  w (16-bit
+ * patterns, head_dim of them) is shared by every head.
+ */
+int pkv_oracle_norm_rope(const uint16_t* x, const int32_t* positions, int batch, int heads,
+                         int head_dim, const uint16_t* w, double eps, double theta, int dtype,
+                         uint16_t* out, double* out_f64) {
+    if (!x || !positions || !w || !out || batch < 0 || heads <= 0 || head_dim <= 0 ||
+        head_dim % 2 || !(theta > 0.0) || !(eps >= 0.0) ||
+        (dtype != ORC_F16 && dtype != ORC_BF16))
+        return ORC_INVALID;
+    const int half = head_dim / 2;
+    double* n = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    if (!n) return ORC_INVALID;
+    for (int b = 0; b < batch; ++b) {
+        for (int h = 0; h < heads; ++h) {
+            const int64_t row = ((int64_t)b * heads + h) * head_dim;
+            double ss = 0.0;
+            for (int d = 0; d < head_dim; ++d) {
+                const double v = pkv_oracle_decode_bits(x[row + d], dtype);
+                ss += v * v;
+            }
+            const double inv_rms = 1.0 / sqrt(ss / head_dim + eps);
+            for (int d = 0; d < head_dim; ++d)
+                n[d] = pkv_oracle_decode_bits(x[row + d], dtype) * inv_rms *
+                       pkv_oracle_decode_bits(w[d], dtype);
+            for (int i = 0; i < half; ++i) {
+                const double ang = (double)positions[b] * pow(theta, -2.0 * i / head_dim);
+                const double c = cos(ang), sn = sin(ang);
+                const double y0 = n[i] * c - n[half + i] * sn;
+                const double y1 = n[half + i] * c + n[i] * sn;
+                if (out_f64) {
+                    out_f64[row + i] = y0;
+                    out_f64[row + half + i] = y1;
+                }
+                out[row + i] = encode_dtype(y0, dtype);
+                out[row + half + i] = encode_dtype(y1, dtype);
+            }
+        }
+    }
+    free(n);
+    return ORC_OK;
+}
+
 /* Decode n elements (used by the tests to pin the decoder). */
 int pkv_oracle_decode_array(const uint16_t* bits, int64_t n, int dtype, double* out) {
     if (!bits || !out || n < 0 || (dtype != ORC_F16 && dtype != ORC_BF16)) return ORC_INVALID;

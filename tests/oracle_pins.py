@@ -503,6 +503,56 @@ def check_multi_query_single_token_and_causality(orc):
     assert np.array_equal(moved[0], base[0])
 
 
+def check_norm_rope_one_hot_closed_form(orc):
+    """A row with one nonzero element a at d = i: the mean square is a^2 / D, so
+    the normalised row is sign(a) sqrt(D) w_i at i (eps = 0), and the rotation
+    at position p turns pair (i, i + D/2) by p * theta^(-2i/D).  With w_i !=
+    w_{i+D/2} this also fixes the order: norm first, then the rotation."""
+    D, theta = 8, 100.0
+    w_vals = [1.5, 0.5, 1.0, 1.0, 0.25, 1.0, 1.0, 2.0]
+    for dt in ("f16", "bf16"):
+        w = bits_of(w_vals, dt)
+        for i, a, p in ((0, 2.0, 3), (1, -0.75, 5), (3, 4.0, 1)):
+            x = np.zeros((1, 1, D), dtype=np.uint16)
+            x[0, 0, i] = bits_of([a], dt)[0]
+            _, f = orc.norm_rope(x, np.array([p], np.int32), w, 0.0, theta, dt, with_f64=True)
+            n = np.sign(a) * np.sqrt(D) * orc.decode_bits(w, dt)[i]
+            ang = p * theta ** (-2.0 * i / D)
+            want = np.zeros(D)
+            want[i] = n * np.cos(ang)
+            want[i + D // 2] = n * np.sin(ang)
+            assert np.allclose(f[0, 0], want, rtol=1e-14, atol=1e-14), (dt, i)
+
+
+def check_norm_rope_scale_invariance_and_weights(orc):
+    """eps = 0: rows x and 2^k x give the same bits (exact power-of-two
+    scaling); the weight multiplies element-wise (position 0: no rotation);
+    with w = 1 the result is the plain rotation times 1 / rms(x); a zero row
+    with eps > 0 stays zero."""
+    rng = np.random.default_rng(41)
+    for dt in ("f16", "bf16"):
+        D = 64
+        x = _rand_bits(rng, (3, 2, D), dt)
+        xd = orc.decode_bits(x, dt)
+        x4 = bits_of(xd * 4.0, dt)
+        pos = np.array([0, 7, 1000], np.int32)
+        w1 = bits_of(np.ones(D), dt)
+        a = orc.norm_rope(x, pos, w1, 0.0, 10000.0, dt)
+        b = orc.norm_rope(x4, pos, w1, 0.0, 10000.0, dt)
+        assert np.array_equal(a, b)
+        w = _rand_bits(rng, (D,), dt)
+        _, fw = orc.norm_rope(x, np.zeros(3, np.int32), w, 1e-6, 10000.0, dt, with_f64=True)
+        _, f1 = orc.norm_rope(x, np.zeros(3, np.int32), w1, 1e-6, 10000.0, dt, with_f64=True)
+        assert np.allclose(fw, f1 * orc.decode_bits(w, dt), rtol=1e-14, atol=0)
+        _, fr = orc.rope(x, pos, 10000.0, dt, with_f64=True)
+        _, fn = orc.norm_rope(x, pos, w1, 0.0, 10000.0, dt, with_f64=True)
+        rms = np.sqrt((xd ** 2).mean(axis=-1, keepdims=True))
+        assert np.allclose(fn, fr / rms, rtol=1e-13, atol=1e-15)
+        z = np.zeros((1, 1, D), np.uint16)
+        zn = orc.norm_rope(z, np.array([3], np.int32), w1, 1e-6, 10000.0, dt)
+        assert (orc.decode_bits(zn, dt) == 0).all()  # +0 or -0
+
+
 ALL_CHECKS = [
     check_decode_f16_all_patterns,
     check_decode_bf16_all_patterns,
@@ -524,4 +574,6 @@ ALL_CHECKS = [
     check_rope_rounds_its_float64_result,
     check_multi_query_vs_causal_sdpa,
     check_multi_query_single_token_and_causality,
+    check_norm_rope_one_hot_closed_form,
+    check_norm_rope_scale_invariance_and_weights,
 ]

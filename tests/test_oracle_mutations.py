@@ -57,6 +57,12 @@ MUTATIONS = [
      "const int n_att = lens[b];"),
     ("multi_query_early_row_sees_all", "n_att > 0 ? n_att : 0, out + r * head_dim",
      "n_att, out + r * head_dim"),
+    ("norm_sum_not_mean", "const double inv_rms = 1.0 / sqrt(ss / head_dim + eps);",
+     "const double inv_rms = 1.0 / sqrt(ss + eps);"),
+    ("norm_weight_of_partner", "pkv_oracle_decode_bits(w[d], dtype);",
+     "pkv_oracle_decode_bits(w[(d + head_dim / 2) % head_dim], dtype);"),
+    ("norm_eps_dropped_twice", "const double inv_rms = 1.0 / sqrt(ss / head_dim + eps);",
+     "const double inv_rms = 1.0 / sqrt(ss / head_dim + 2.0 * eps + 1e-3);"),
 ]
 
 RUNNER = textwrap.dedent("""
