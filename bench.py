@@ -468,6 +468,29 @@ def run_ours(args):
     if dist:
         dist.barrier()
     rope_ms = max_over_ranks(dist, r0.elapsed_time(r1) / KR, dev)
+    # the same with the per-head RMS norm of q and k before the rotation
+    gn = torch.Generator(device=dev).manual_seed(args.seed + 2)
+    wq = (1.0 + 0.3 * torch.randn(w.head_dim, generator=gn, device=dev)).to(w.dtype)
+    wk = (1.0 + 0.3 * torch.randn(w.head_dim, generator=gn, device=dev)).to(w.dtype)
+
+    def rope_norm_step():
+        pkv.paged_decode_step_rope(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens,
+                                   w.scale, rope_theta, out, ws, nw, variant=var,
+                                   q_norm_weight=wq, k_norm_weight=wk, norm_eps=1e-6)
+
+    for _ in range(max(3, args.warmup)):
+        rope_norm_step()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    r0.record(stream)
+    for _ in range(KR):
+        rope_norm_step()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    rope_norm_ms = max_over_ranks(dist, r0.elapsed_time(r1) / KR, dev)
 
     # ---- shared-prefix decode on the prefix-sharing workload (64 sequences,
     # one 2048-token prefix): the cascade against the plain decode ----
@@ -665,6 +688,7 @@ def run_ours(args):
                 "steps": KE},
         "rope_step": {"value": aggregate_gbs(world, by["step"], rope_ms), "unit": UNIT,
                       "ms_per_step": rope_ms, "steps": KR, "rope_theta": rope_theta,
+                      "ms_per_step_with_qk_norm": rope_norm_ms,
                       "what": "paged_decode_step_rope: rotary embedding of q and k_new fused "
                               "into the append CTAs of the plan launch, same bytes"},
         "prefix_sharing": {

@@ -237,10 +237,22 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
  * rotated into q_out (q_out may be q itself, no other overlap); k_new is
  * rotated and v_new copied into the pool as kv_append does (positions[b] < 0:
  * q is still rotated, nothing is written to the pool).  rope_theta must be
- * finite and > 0 (INVALID_ARG).  One kernel launch. */
+ * finite and > 0 (INVALID_ARG).
+ *
+ * Optional per-head RMS norm before the rotation (Experimental LibTorch
+ * prefix cache, "Current execution limits": Q/K-normalised decoders write
+ * normalised keys straight into their attention arenas): with q_norm_weight
+ * (k_norm_weight) non-NULL, every q (k_new) row of each head first becomes
+ *     n_d = x_d * w_d / sqrt(mean_d(x_d^2) + norm_eps),
+ * w [head_dim] in the pool's dtype (device, 2-byte aligned), shared by all
+ * heads; the mean and 1 / rms are formed in double, the product rounded to
+ * fp32 before the rotation, and the result is still rounded once to the
+ * dtype.  Either weight may be NULL (no norm on that side); norm_eps finite
+ * and >= 0 when one is set (INVALID_ARG).  One kernel launch. */
 pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new,
                           const void* v_new, const int32_t* page_table, int table_stride,
                           const int32_t* positions, int batch, int n_q_heads, double rope_theta,
+                          const void* q_norm_weight, const void* k_norm_weight, float norm_eps,
                           void* q_out, uint32_t* dev_status, pkv_stream stream);
 
 /* Materialize each sequence's cached rows as a dense block:
@@ -373,16 +385,19 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
  * kernel).  q holds the step's un-rotated queries; the rotated queries are
  * written into `out`, which the decode reads as its query and then overwrites
  * with the attention output (each (sequence, head) row is read before its own
- * result is written).  Arguments otherwise as for paged_decode_step;
- * rope_theta finite and > 0.  Three launches. */
+ * result is written).  q_norm_weight, k_norm_weight, norm_eps: the optional
+ * per-head RMS norm of kv_append_rope.  Arguments otherwise as for
+ * paged_decode_step; rope_theta finite and > 0.  Three launches. */
 pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const int32_t* positions,
                                   const void* q, void* k_pool, void* v_pool,
                                   const int32_t* page_table, int table_stride,
                                   const int32_t* context_lens, int batch, int n_q_heads,
                                   int n_kv_heads, int head_dim, int page_size, int num_pages,
-                                  pkv_dtype dtype, float scale, double rope_theta, void* out,
-                                  void* workspace, size_t ws_bytes, int num_workers,
-                                  pkv_decode_variant variant, pkv_stream stream);
+                                  pkv_dtype dtype, float scale, double rope_theta,
+                                  const void* q_norm_weight, const void* k_norm_weight,
+                                  float norm_eps, void* out, void* workspace, size_t ws_bytes,
+                                  int num_workers, pkv_decode_variant variant,
+                                  pkv_stream stream);
 
 /* ------------------------------------------------------------------------
  * Shared-prefix decode (CacheIR, "Current Capabilities": batched decode over

@@ -88,7 +88,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "pkv_prefix_cache_match": ([V, V, I, V, I, ctypes.POINTER(I)], I),
         "pkv_prefix_cache_evict": ([V, I, ctypes.POINTER(I)], I),
         "pkv_prefix_cache_pages": ([V], I),
-        "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, V], I),
+        "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, F, V, V, V], I),
         "paged_decode_prefix_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_multi_workspace_size": ([I, I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "pkv_check_bounded_wait": ([ctypes.c_uint32, V, V, V], I),
@@ -97,7 +97,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "paged_decode_attention_prefix": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, I, V, V, Z,
                                            I, I, V], I),
         "paged_decode_step_rope": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F,
-                                    ctypes.c_double, V, V, Z, I, I, V], I),
+                                    ctypes.c_double, V, V, F, V, V, Z, I, I, V], I),
         "kv_gather": ([V, V, I, V, I, I, V, V, V, V], I),
         "paged_decode_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_plan": ([V, I, I, I, I, I, I, I, I, V, Z, V], I),
@@ -335,12 +335,23 @@ def kv_append(pool: Pool, k_new: torch.Tensor, v_new: torch.Tensor, page_table: 
                                     _stream(stream)), "kv_append")
 
 
+def _norm_weights(q_norm_weight, k_norm_weight, dtype, head_dim: int):
+    for name, w in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight)):
+        if w is not None:
+            _dev(w, name, dtype, 1)
+            if w.shape[0] != head_dim:
+                raise ValueError(f"{name} must hold head_dim values")
+
+
 def kv_append_rope(pool: Pool, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                    page_table: torch.Tensor, positions: torch.Tensor, rope_theta: float,
                    q_out: torch.Tensor, dev_status: torch.Tensor | None = None,
-                   stream=None) -> torch.Tensor:
+                   stream=None, q_norm_weight: torch.Tensor | None = None,
+                   k_norm_weight: torch.Tensor | None = None,
+                   norm_eps: float = 1e-6) -> torch.Tensor:
     """Rotary embedding of q [B, Hq, D] (into q_out) and k_new at positions[b],
-    then the append of the rotated k_new and v_new into the pool."""
+    then the append of the rotated k_new and v_new into the pool; with a norm
+    weight [D], the per-head RMS norm of that side comes first."""
     _dev(q, "q", pool.dtype, 3)
     _dev(q_out, "q_out", pool.dtype, 3)
     _dev(k_new, "k_new", pool.dtype, 3)
@@ -356,10 +367,12 @@ def kv_append_rope(pool: Pool, q: torch.Tensor, k_new: torch.Tensor, v_new: torc
         raise ValueError("page_table rows != batch")
     if dev_status is not None:
         _dev(dev_status, "dev_status", torch.int32)
+    _norm_weights(q_norm_weight, k_norm_weight, pool.dtype, pool.head_dim)
     _check(load_library().kv_append_rope(
         pool.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(page_table), page_table.shape[1],
-        _ptr(positions), B, q.shape[1], float(rope_theta), _ptr(q_out), _ptr(dev_status),
-        _stream(stream)), "kv_append_rope")
+        _ptr(positions), B, q.shape[1], float(rope_theta), _ptr(q_norm_weight),
+        _ptr(k_norm_weight), float(norm_eps), _ptr(q_out), _ptr(dev_status), _stream(stream)),
+        "kv_append_rope")
     return q_out
 
 
@@ -570,10 +583,14 @@ def paged_decode_step_rope(k_new: torch.Tensor, v_new: torch.Tensor, positions: 
                            page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
                            rope_theta: float, out: torch.Tensor, workspace: torch.Tensor,
                            num_workers: int = 0, stream=None,
-                           variant: int = VARIANT_AUTO) -> torch.Tensor:
+                           variant: int = VARIANT_AUTO,
+                           q_norm_weight: torch.Tensor | None = None,
+                           k_norm_weight: torch.Tensor | None = None,
+                           norm_eps: float = 1e-6) -> torch.Tensor:
     """paged_decode_step with the rotary embedding of q and k_new at positions[b]
-    (angle base rope_theta) fused into the append; q stays un-rotated, the
-    rotated queries pass through out before the result overwrites them."""
+    (angle base rope_theta) fused into the append, after the optional per-head
+    RMS norm of either side; q stays as given, the rotated queries pass through
+    out before the result overwrites them."""
     B, Hq, Hkv, D, P, NP, dt = _decode_shapes(q, k_pool, v_pool, page_table, out)
     _dev(context_lens, "context_lens", torch.int32, 1)
     _dev(workspace, "workspace", torch.uint8)
@@ -582,11 +599,13 @@ def paged_decode_step_rope(k_new: torch.Tensor, v_new: torch.Tensor, positions: 
     _dev(positions, "positions", torch.int32, 1)
     if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
         raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    _norm_weights(q_norm_weight, k_norm_weight, q.dtype, D)
     _check(load_library().paged_decode_step_rope(
         _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q), _ptr(k_pool), _ptr(v_pool),
         _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
-        float(scale), float(rope_theta), _ptr(out), _ptr(workspace), workspace.numel(),
-        int(num_workers), int(variant), _stream(stream)), "paged_decode_step_rope")
+        float(scale), float(rope_theta), _ptr(q_norm_weight), _ptr(k_norm_weight),
+        float(norm_eps), _ptr(out), _ptr(workspace), workspace.numel(), int(num_workers),
+        int(variant), _stream(stream)), "paged_decode_step_rope")
     return out
 
 

@@ -424,6 +424,9 @@ pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t*
     a.page_size = page_size;
     a.num_pages = num_pages;
     a.q_in = nullptr;  // no rotary embedding unless the caller sets it up
+    a.q_norm_w = nullptr;
+    a.k_norm_w = nullptr;
+    a.norm_eps = 0.0;
     a.q_out = nullptr;
     a.n_q_heads = 0;
     a.bf16 = 0;
@@ -432,6 +435,24 @@ pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t*
 
 // The rotary angles per position unit, theta^(-2i/D) for i < D/2, in double
 // (the kernel multiplies them by each token's position).
+// Norm weights (nullable, 2-byte aligned, head_dim elements) and eps of the
+// optional per-head RMS norm before the rotation.
+bool norm_args_ok(const void* q_norm_weight, const void* k_norm_weight, float norm_eps) {
+    if ((reinterpret_cast<uintptr_t>(q_norm_weight) & 1u) ||
+        (reinterpret_cast<uintptr_t>(k_norm_weight) & 1u))
+        return false;
+    return !(q_norm_weight || k_norm_weight) || (norm_eps >= 0.f && isfinite(norm_eps));
+}
+
+pkv_status set_norm(pkv::AppendArgs* a, const void* q_norm_weight, const void* k_norm_weight,
+                    float norm_eps) {
+    if (!norm_args_ok(q_norm_weight, k_norm_weight, norm_eps)) return PKV_ERR_INVALID_ARG;
+    a->q_norm_w = q_norm_weight;
+    a->k_norm_w = k_norm_weight;
+    a->norm_eps = norm_eps;
+    return PKV_OK;
+}
+
 void set_inv_freq(pkv::AppendArgs* a, double theta, int head_dim) {
     for (int i = 0; i < 64; ++i)
         a->inv_freq[i] = i < head_dim / 2 ? pow(theta, -2.0 * i / head_dim) : 0.0;
@@ -524,9 +545,11 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
 pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new,
                           const void* v_new, const int32_t* page_table, int table_stride,
                           const int32_t* positions, int batch, int n_q_heads, double rope_theta,
+                          const void* q_norm_weight, const void* k_norm_weight, float norm_eps,
                           void* q_out, uint32_t* dev_status, pkv_stream stream) {
     if (!pool || batch < 0 || table_stride <= 0 || n_q_heads <= 0) return PKV_ERR_INVALID_ARG;
     if (!(rope_theta > 0.0 && isfinite(rope_theta))) return PKV_ERR_INVALID_ARG;
+    if (!norm_args_ok(q_norm_weight, k_norm_weight, norm_eps)) return PKV_ERR_INVALID_ARG;
     if (batch == 0) return PKV_OK;
     if (!q || !q_out || !k_new || !v_new || !page_table || !positions) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(q_out) || !aligned16(k_new) || !aligned16(v_new))
@@ -556,6 +579,7 @@ pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new
     a.n_q_heads = n_q_heads;
     set_inv_freq(&a, rope_theta, pool->head_dim);
     a.bf16 = pool->dtype == PKV_BF16;
+    if (set_norm(&a, q_norm_weight, k_norm_weight, norm_eps) != PKV_OK) return PKV_ERR_INVALID_ARG;
     return cuda_status(pkv::launch_rope_append(a, batch, pool->head_dim, dev_status,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -700,10 +724,12 @@ pkv_status step_impl(const void* k_new, const void* v_new, const int32_t* positi
                      const void* q, void* k_pool, void* v_pool, const int32_t* page_table,
                      int table_stride, const int32_t* context_lens, int batch, int n_q_heads,
                      int n_kv_heads, int head_dim, int page_size, int num_pages, pkv_dtype dtype,
-                     float scale, bool rope, double rope_theta, void* out, void* workspace,
+                     float scale, bool rope, double rope_theta, const void* q_norm_weight,
+                     const void* k_norm_weight, float norm_eps, void* out, void* workspace,
                      size_t ws_bytes, int num_workers, pkv_decode_variant variant,
                      pkv_stream stream) {
     if (rope && !(rope_theta > 0.0 && isfinite(rope_theta))) return PKV_ERR_INVALID_ARG;
+    if (rope && !norm_args_ok(q_norm_weight, k_norm_weight, norm_eps)) return PKV_ERR_INVALID_ARG;
     pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
                                          context_lens, true, batch, n_q_heads, n_kv_heads,
                                          head_dim, page_size, num_pages, dtype, scale, out,
@@ -734,6 +760,7 @@ pkv_status step_impl(const void* k_new, const void* v_new, const int32_t* positi
         a.n_q_heads = n_q_heads;
         set_inv_freq(&a, rope_theta, head_dim);
         a.bf16 = dtype == PKV_BF16;
+        if ((st = set_norm(&a, q_norm_weight, k_norm_weight, norm_eps)) != PKV_OK) return st;
     }
     if ((st = do_plan(context_lens, page_table, batch, page_size, table_stride, num_workers,
                       workspace, s, &a, cs)) != PKV_OK)
@@ -758,8 +785,8 @@ pkv_status paged_decode_step(const void* k_new, const void* v_new, const int32_t
                              pkv_stream stream) {
     return step_impl(k_new, v_new, positions, q, k_pool, v_pool, page_table, table_stride,
                      context_lens, batch, n_q_heads, n_kv_heads, head_dim, page_size, num_pages,
-                     dtype, scale, false, 0.0, out, workspace, ws_bytes, num_workers, variant,
-                     stream);
+                     dtype, scale, false, 0.0, nullptr, nullptr, 0.f, out, workspace, ws_bytes,
+                     num_workers, variant, stream);
 }
 
 pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const int32_t* positions,
@@ -767,13 +794,15 @@ pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const in
                                   const int32_t* page_table, int table_stride,
                                   const int32_t* context_lens, int batch, int n_q_heads,
                                   int n_kv_heads, int head_dim, int page_size, int num_pages,
-                                  pkv_dtype dtype, float scale, double rope_theta, void* out,
-                                  void* workspace, size_t ws_bytes, int num_workers,
-                                  pkv_decode_variant variant, pkv_stream stream) {
+                                  pkv_dtype dtype, float scale, double rope_theta,
+                                  const void* q_norm_weight, const void* k_norm_weight,
+                                  float norm_eps, void* out, void* workspace, size_t ws_bytes,
+                                  int num_workers, pkv_decode_variant variant,
+                                  pkv_stream stream) {
     return step_impl(k_new, v_new, positions, q, k_pool, v_pool, page_table, table_stride,
                      context_lens, batch, n_q_heads, n_kv_heads, head_dim, page_size, num_pages,
-                     dtype, scale, true, rope_theta, out, workspace, ws_bytes, num_workers,
-                     variant, stream);
+                     dtype, scale, true, rope_theta, q_norm_weight, k_norm_weight, norm_eps, out,
+                     workspace, ws_bytes, num_workers, variant, stream);
 }
 
 pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool,

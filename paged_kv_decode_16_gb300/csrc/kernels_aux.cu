@@ -83,10 +83,48 @@ __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* c, co
     }
 }
 
+// 1 / rms of a row for the norm before the rotation, in double: the row's
+// hv lanes (consecutive, hv a power of two dividing 32) each hold 8 element
+// pairs; their sums of squares meet in a butterfly over those lanes.
+template <typename T>
+__device__ __forceinline__ double row_inv_rms(const uint4& lo, const uint4& hi, int hv,
+                                              int head_dim, double eps) {
+    const T* a = reinterpret_cast<const T*>(&lo);
+    const T* b = reinterpret_cast<const T*>(&hi);
+    double ss = 0.0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const double x0 = Elem<T>::to(a[e]), x1 = Elem<T>::to(b[e]);
+        ss = fma(x0, x0, ss);
+        ss = fma(x1, x1, ss);
+    }
+    const int lane = threadIdx.x & 31;
+    const unsigned mask = ((1u << hv) - 1u) << (lane & ~(hv - 1));
+    for (int o = hv / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+    return 1.0 / sqrt(ss / head_dim + eps);
+}
+
+// Scale 8 element pairs by inv_rms and their weights (double), then rotate
+// them as rotate8 does.
+template <typename T>
+__device__ __forceinline__ void norm_rotate8(uint4& lo, uint4& hi, const float* c, const float* s,
+                                             const float* wlo, const float* whi, double inv_rms) {
+    T* a = reinterpret_cast<T*>(&lo);
+    T* b = reinterpret_cast<T*>(&hi);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float x0 = (float)((double)Elem<T>::to(a[e]) * inv_rms * (double)wlo[e]);
+        const float x1 = (float)((double)Elem<T>::to(b[e]) * inv_rms * (double)whi[e]);
+        a[e] = Elem<T>::from(fmaf(x0, c[e], -x1 * s[e]));
+        b[e] = Elem<T>::from(fmaf(x1, c[e], x0 * s[e]));
+    }
+}
+
 // One CTA pass over sequences [b0, b0 + nseq): the cos / sin table of their
-// positions (one angle per thread), then every 16-byte vector pair of their q
-// rows (rotated into q_out) and k rows (rotated into the pool), and their v
-// rows (copied).  tbl: 2 * nseq * D/2 floats of shared memory.  Returns the
+// positions (one angle per thread) and the norm weights, then every 16-byte
+// vector pair of their q rows (normalised when q_norm_w is set, rotated into
+// q_out) and k rows (the same with k_norm_w, rotated into the pool), and their
+// v rows (copied).  tbl: kRopeSmemFloats floats of shared memory.  Returns the
 // PKV_DEV_* bits of skipped rows.  Block-collective.
 template <typename T>
 __device__ uint32_t rope_append_pass(const AppendArgs& a, int b0, int nseq, int batch,
@@ -95,12 +133,18 @@ __device__ uint32_t rope_append_pass(const AppendArgs& a, int b0, int nseq, int 
     const int hv = half / 8;  // 16-byte vectors per half row
     float* ctab = tbl;
     float* stab = tbl + nseq * half;
+    float* wq = tbl + 2 * 1024;  // norm weights of q, then of k
+    float* wk = wq + head_dim;
     for (int t = threadIdx.x; t < nseq * half; t += blockDim.x) {
         const int b = b0 + t / half, i = t % half;
         float cv = 1.f, sv = 0.f;
         if (b < batch) rope_cos_sin(a.positions[b], a.inv_freq[i], &cv, &sv);
         ctab[t] = cv;
         stab[t] = sv;
+    }
+    for (int t = threadIdx.x; t < head_dim; t += blockDim.x) {
+        wq[t] = a.q_norm_w ? Elem<T>::to(static_cast<const T*>(a.q_norm_w)[t]) : 1.f;
+        wk[t] = a.k_norm_w ? Elem<T>::to(static_cast<const T*>(a.k_norm_w)[t]) : 1.f;
     }
     __syncthreads();
     uint32_t flags = 0;
@@ -116,7 +160,11 @@ __device__ uint32_t rope_append_pass(const AppendArgs& a, int b0, int nseq, int 
             const int h = r / hv, j = r % hv;
             const long long row = ((long long)b * a.n_q_heads + h) * a.vecs;
             uint4 lo = a.q_in[row + j], hi = a.q_in[row + hv + j];
-            rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j);
+            if (a.q_norm_w)
+                norm_rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j, wq + 8 * j, wq + half + 8 * j,
+                                row_inv_rms<T>(lo, hi, hv, head_dim, a.norm_eps));
+            else
+                rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j);
             a.q_out[row + j] = lo;
             a.q_out[row + hv + j] = hi;
             continue;
@@ -142,7 +190,11 @@ __device__ uint32_t rope_append_pass(const AppendArgs& a, int b0, int nseq, int 
             const long long src = ((long long)b * a.n_kv_heads + h) * a.vecs;
             const long long dst = base + (long long)h * a.page_size * a.vecs;
             uint4 lo = a.k_new[src + j], hi = a.k_new[src + hv + j];
-            rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j);
+            if (a.k_norm_w)
+                norm_rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j, wk + 8 * j, wk + half + 8 * j,
+                                row_inv_rms<T>(lo, hi, hv, head_dim, a.norm_eps));
+            else
+                rotate8<T>(lo, hi, c + 8 * j, sn + 8 * j);
             a.k_pool[dst + j] = lo;
             a.k_pool[dst + hv + j] = hi;
         } else {  // value row: bit copy
@@ -311,7 +363,7 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
     __syncthreads();
     uint32_t f = 0;
     if (aa.q_in) {  // rotary embedding, then the append
-        __shared__ float s_rope[2 * kRopeThreads];
+        __shared__ float s_rope[kRopeSmemFloats];
         f = rope_append_cta(aa, pa.batch, aa.vecs * 8, blockIdx.x - 1, append_ctas, s_rope);
     } else {
         const long long total = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
@@ -608,7 +660,7 @@ cudaError_t launch_append(const AppendArgs& a, int batch, uint32_t* status,
 // Stand-alone rotary + append: each CTA ORs its skipped-row bits into status.
 __global__ void __launch_bounds__(kRopeThreads)
 rope_append_kernel(AppendArgs a, int batch, int head_dim, uint32_t* status) {
-    __shared__ float s_rope[2 * kRopeThreads];
+    __shared__ float s_rope[kRopeSmemFloats];
     __shared__ uint32_t flags;
     pdl_wait();
     pdl_trigger();

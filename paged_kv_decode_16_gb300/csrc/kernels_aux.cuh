@@ -44,8 +44,17 @@ struct AppendArgs {
     uint4* q_out;          // [B][Hq][D] rotated queries
     int n_q_heads;
     int bf16;              // element type of q / k / v: bf16, else fp16
+    // per-head RMS norm before the rotation (null: none): weights [D] in the
+    // element type, shared by all heads; x_d * w_d / sqrt(mean(x^2) + eps)
+    const void* q_norm_w;
+    const void* k_norm_w;
+    double norm_eps;
     double inv_freq[64];   // theta^(-2i/D), i < D/2 (computed on the host)
 };
+
+// Shared memory of a rotary + append pass: the cos / sin table (one angle per
+// thread) and the two norm weight rows.
+constexpr int kRopeSmemFloats = 2 * 1024 + 2 * 128;
 
 // Rotary + append: sequences handled together by one CTA of 1024 threads
 // (one angle per thread: 1024 / (D / 2)), and their cos / sin table.

@@ -238,17 +238,28 @@ def test_rope_entry_points_check_theta_on_host(lib):
         rc = lib.paged_decode_step_rope(V(A * 30), V(A * 31), V(A * 32), V(A), V(A * 8),
                                         V(A * 16), V(A * 24), 4, V(A * 25), 2, 8, 2, 128, 16, 8,
                                         BF16, ctypes.c_float(0.088), ctypes.c_double(theta),
+                                        None, None, ctypes.c_float(0.0),
                                         V(A * 26), V(A * 27), 1 << 20, 0, 0, None)
         assert rc == INVALID
     h = V()
     assert lib.kv_pool_create(8, 16, 2, 128, BF16, V(A), V(A * 2), ctypes.byref(h)) == OK
+    F = ctypes.c_float
+
+    def rope(batch=2, theta=1e4, q_out=A * 9, qw=None, kw=None, eps=0.0):
+        return lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), batch,
+                                  8, ctypes.c_double(theta), None if qw is None else V(qw),
+                                  None if kw is None else V(kw), F(eps), V(q_out), None, None)
     try:
-        assert lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), 2, 8,
-                                  ctypes.c_double(0.0), V(A * 9), None, None) == INVALID
+        assert rope(theta=0.0) == INVALID
         # q_out partly over q is refused; q_out == q (in place) passes the host checks
-        assert lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), 2, 8,
-                                  ctypes.c_double(1e4), V(A * 3 + 256), None, None) == ALIAS
-        assert lib.kv_append_rope(h, V(A * 3), V(A * 4), V(A * 5), V(A * 6), 4, V(A * 7), 0, 8,
-                                  ctypes.c_double(1e4), V(A * 3), None, None) == OK
+        assert rope(q_out=A * 3 + 256) == ALIAS
+        assert rope(batch=0, q_out=A * 3) == OK
+        # the norm before the rotation: 2-byte aligned weights, eps finite and >= 0
+        assert rope(qw=A * 10 + 1) == INVALID
+        assert rope(kw=A * 10 + 1) == INVALID
+        assert rope(qw=A * 10, eps=-1e-6) == INVALID
+        assert rope(kw=A * 10, eps=float("nan")) == INVALID
+        assert rope(batch=0, qw=A * 10 + 1) == INVALID  # checked before the empty batch
+        assert rope(batch=0, qw=A * 10, kw=A * 11, eps=1e-6) == OK
     finally:
         lib.kv_pool_destroy(h)

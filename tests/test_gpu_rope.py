@@ -140,3 +140,77 @@ def test_rope_rejects_bad_theta():
                                torch.empty_like(w.q))
         assert e.value.name == "PKV_ERR_INVALID_ARG"
     pool.destroy()
+
+
+def _norm_weights(dtype, D, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    wq = (1.0 + 0.3 * torch.randn(D, generator=g, device="cuda")).to(dtype)
+    wk = (1.0 + 0.3 * torch.randn(D, generator=g, device="cuda")).to(dtype)
+    return wq, wk
+
+
+@pytest.mark.parametrize("sides", ["both", "q_only", "k_only"])
+@pytest.mark.parametrize("dtype,D,theta", [(torch.bfloat16, 128, 1.0e6),
+                                           (torch.float16, 128, 10000.0),
+                                           (torch.float16, 64, 10000.0),
+                                           (torch.bfloat16, 64, 500000.0)])
+def test_kv_append_rope_norm_matches_oracle(dtype, D, theta, sides):
+    """Per-head RMS norm (weights [D], eps 1e-6) before the rotation: rotated q
+    and k rows within one ulp of the oracle's single rounding (bitwise for all
+    but at most 1 in 200), v bit for bit."""
+    w = _case(37, dtype, D)
+    table, lens, _ = to_dev(w)
+    pos_h = np.array([int(w.context_lens[0]) - 1, 0, -1, int(w.context_lens[3]) - 1, 5, 2],
+                     dtype=np.int32)
+    pos = torch.from_numpy(pos_h).cuda()
+    wq, wk = _norm_weights(dtype, D, 38)
+    qw = wq if sides != "k_only" else None
+    kw = wk if sides != "q_only" else None
+    eps = 1e-6
+    pool = pkv.kv_pool_create(w.num_pages, w.page_size, w.n_kv_heads, w.head_dim, w.dtype,
+                              w.k_pool, w.v_pool)
+    before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+    q_out = torch.empty_like(w.q)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.kv_append_rope(pool, w.q, w.k_new, w.v_new, table, pos, theta, q_out, dev_status=st,
+                       q_norm_weight=qw, k_norm_weight=kw, norm_eps=eps)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    dn = w.dtype_name
+    q_ref = (oracle.norm_rope(wl.to_bits(w.q), pos_h, wl.to_bits(qw), eps, theta, dn)
+             if qw is not None else oracle.rope(wl.to_bits(w.q), pos_h, theta, dn))
+    k_ref = (oracle.norm_rope(wl.to_bits(w.k_new), pos_h, wl.to_bits(kw), eps, theta, dn)
+             if kw is not None else oracle.rope(wl.to_bits(w.k_new), pos_h, theta, dn))
+    kp_ref, vp_ref = oracle.kv_append(before[0], before[1], k_ref, wl.to_bits(w.v_new),
+                                      w.page_table, pos_h)
+    assert_rounded_rows_equal(wl.to_bits(q_out), q_ref, "normalised rotated q")
+    assert_rounded_rows_equal(wl.to_bits(w.k_pool), kp_ref, "k pool")
+    assert np.array_equal(wl.to_bits(w.v_pool), vp_ref), "v pool (bit copy)"
+    pool.destroy()
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_step_rope_norm_matches_oracle(variant):
+    """paged_decode_step_rope with both norms: pools and attention output
+    against the oracle's decode of the normalised, rotated q and k."""
+    w = wl.make("llama3_8b", seed=3, device="cuda", batch=12)
+    table, lens, pos = to_dev(w)
+    dn = w.dtype_name
+    theta, eps = 500000.0, 1e-6
+    wq, wk = _norm_weights(w.dtype, w.head_dim, 39)
+    before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+    ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, variant=variant)
+    out = torch.full_like(w.q, float("nan"))
+    pkv.paged_decode_step_rope(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens,
+                               w.scale, theta, out, ws, variant=variant, q_norm_weight=wq,
+                               k_norm_weight=wk, norm_eps=eps)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(ws) == 0
+    q_ref = oracle.norm_rope(wl.to_bits(w.q), w.positions, wl.to_bits(wq), eps, theta, dn)
+    k_ref = oracle.norm_rope(wl.to_bits(w.k_new), w.positions, wl.to_bits(wk), eps, theta, dn)
+    kp, vp = oracle.kv_append(before[0], before[1], k_ref, wl.to_bits(w.v_new), w.page_table,
+                              w.positions)
+    assert_rounded_rows_equal(wl.to_bits(w.k_pool), kp, "k pool")
+    assert np.array_equal(wl.to_bits(w.v_pool), vp)
+    ref = oracle.paged_decode(q_ref, kp, vp, w.page_table, w.context_lens, w.scale, dn)
+    assert_close(out, ref, what="rms-norm + rope step")
