@@ -245,9 +245,9 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
  * (k_norm_weight) non-NULL, every q (k_new) row of each head first becomes
  *     n_d = x_d * w_d / sqrt(mean_d(x_d^2) + norm_eps),
  * w [head_dim] in the pool's dtype (device, 2-byte aligned), shared by all
- * heads; the mean and 1 / rms are formed in double, the product rounded to
- * fp32 before the rotation, and the result is still rounded once to the
- * dtype.  Either weight may be NULL (no norm on that side); norm_eps finite
+ * heads; the mean square (a compensated fp32 sum of exact squares), 1 / rms
+ * and the product are formed in fp32 before the rotation, and the result is
+ * still rounded once to the dtype.  Either weight may be NULL (no norm on that side); norm_eps finite
  * and >= 0 when one is set (INVALID_ARG).  One kernel launch. */
 pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new,
                           const void* v_new, const int32_t* page_table, int table_stride,

@@ -426,7 +426,7 @@ pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t*
     a.q_in = nullptr;  // no rotary embedding unless the caller sets it up
     a.q_norm_w = nullptr;
     a.k_norm_w = nullptr;
-    a.norm_eps = 0.0;
+    a.norm_eps = 0.f;
     a.q_out = nullptr;
     a.n_q_heads = 0;
     a.bf16 = 0;

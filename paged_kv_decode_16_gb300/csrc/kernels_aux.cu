@@ -83,38 +83,43 @@ __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* c, co
     }
 }
 
-// 1 / rms of a row for the norm before the rotation, in double: the row's
-// hv lanes (consecutive, hv a power of two dividing 32) each hold 8 element
-// pairs; their sums of squares meet in a butterfly over those lanes.
+// 1 / rms of a row for the norm before the rotation: the row's hv lanes
+// (consecutive, hv a power of two dividing 32) each hold 8 element pairs.  The
+// square of a 16-bit value is exact in fp32 and each lane adds its 16 squares
+// with a compensated (Kahan) sum; the lane sums meet in a butterfly; sqrt and
+// the division are correctly rounded.  A few fp32 roundings in all, far below
+// an ulp of the 16-bit result (fp64 would cost more on this part).
 template <typename T>
-__device__ __forceinline__ double row_inv_rms(const uint4& lo, const uint4& hi, int hv,
-                                              int head_dim, double eps) {
+__device__ __forceinline__ float row_inv_rms(const uint4& lo, const uint4& hi, int hv,
+                                             int head_dim, float eps) {
     const T* a = reinterpret_cast<const T*>(&lo);
     const T* b = reinterpret_cast<const T*>(&hi);
-    double ss = 0.0;
+    float sum = 0.f, comp = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const double x0 = Elem<T>::to(a[e]), x1 = Elem<T>::to(b[e]);
-        ss = fma(x0, x0, ss);
-        ss = fma(x1, x1, ss);
+    for (int e = 0; e < 16; ++e) {
+        const float x = Elem<T>::to(e < 8 ? a[e] : b[e - 8]);
+        const float y = x * x - comp;
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
     }
     const int lane = threadIdx.x & 31;
     const unsigned mask = ((1u << hv) - 1u) << (lane & ~(hv - 1));
-    for (int o = hv / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
-    return 1.0 / sqrt(ss / head_dim + eps);
+    for (int o = hv / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(mask, sum, o);
+    return 1.0f / sqrtf(sum / (float)head_dim + eps);
 }
 
-// Scale 8 element pairs by inv_rms and their weights (double), then rotate
-// them as rotate8 does.
+// Scale 8 element pairs by inv_rms and their weights, then rotate them as
+// rotate8 does.
 template <typename T>
 __device__ __forceinline__ void norm_rotate8(uint4& lo, uint4& hi, const float* c, const float* s,
-                                             const float* wlo, const float* whi, double inv_rms) {
+                                             const float* wlo, const float* whi, float inv_rms) {
     T* a = reinterpret_cast<T*>(&lo);
     T* b = reinterpret_cast<T*>(&hi);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const float x0 = (float)((double)Elem<T>::to(a[e]) * inv_rms * (double)wlo[e]);
-        const float x1 = (float)((double)Elem<T>::to(b[e]) * inv_rms * (double)whi[e]);
+        const float x0 = Elem<T>::to(a[e]) * inv_rms * wlo[e];
+        const float x1 = Elem<T>::to(b[e]) * inv_rms * whi[e];
         a[e] = Elem<T>::from(fmaf(x0, c[e], -x1 * s[e]));
         b[e] = Elem<T>::from(fmaf(x1, c[e], x0 * s[e]));
     }

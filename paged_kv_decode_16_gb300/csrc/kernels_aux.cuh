@@ -48,7 +48,7 @@ struct AppendArgs {
     // element type, shared by all heads; x_d * w_d / sqrt(mean(x^2) + eps)
     const void* q_norm_w;
     const void* k_norm_w;
-    double norm_eps;
+    float norm_eps;
     double inv_freq[64];   // theta^(-2i/D), i < D/2 (computed on the host)
 };
 
