@@ -247,8 +247,10 @@ pkv_status kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
  * w [head_dim] in the pool's dtype (device, 2-byte aligned), shared by all
  * heads; the mean square (a compensated fp32 sum of exact squares), 1 / rms
  * and the product are formed in fp32 before the rotation, and the result is
- * still rounded once to the dtype.  Either weight may be NULL (no norm on that side); norm_eps finite
- * and >= 0 when one is set (INVALID_ARG).  One kernel launch. */
+ * still rounded once to the dtype.  Either weight may be NULL (no norm on
+ * that side); norm_eps finite and >= 0 when one is set (INVALID_ARG); with
+ * norm_eps = 0 an all-zero row has no norm and gives NaN, as the formula
+ * does.  One kernel launch. */
 pkv_status kv_append_rope(const pkv_pool* pool, const void* q, const void* k_new,
                           const void* v_new, const int32_t* page_table, int table_stride,
                           const int32_t* positions, int batch, int n_q_heads, double rope_theta,
