@@ -2,10 +2,13 @@
  * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV decode library.
  *
  * One decode step of grouped-query attention (GQA) for a batch of sequences,
- * each with exactly one new query token, over a KV cache stored in fixed-size
- * pages that sequences reach through their own page-table rows (rows may share
+ * each with one new query token, over a KV cache stored in fixed-size pages
+ * that sequences reach through their own page-table rows (rows may share
  * pages, e.g. a common prompt prefix), plus the append of the step's new K/V
- * rows into the page pool.
+ * rows into the page pool.  Around it: the rotary embedding (with an optional
+ * per-head RMS norm) fused into the append, a shared-prefix decode that reads
+ * a common prefix once per KV head, several causal query tokens per sequence,
+ * and a host radix cache of prompt prefixes over the pool.
  *
  * Where the operations are defined (page title, section):
  *   - CacheIR, "Compiler Example": the decode graph lowers attention into
