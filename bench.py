@@ -284,6 +284,59 @@ def cpu_oracle_sample(w, target_s: float = 12.0, one_core_s: float = 4.0):
     return res
 
 
+def prefix_cache_sample(seed: int) -> dict:
+    """The host prefix cache on a serving-like request stream: 512 requests,
+    each one of 16 system prompts of 1024 tokens plus a private 512-token
+    suffix (page size 16); per request the longest cached prefix is matched,
+    the missing pages allocated, the prompt inserted, and the request's own
+    references released.  The pool is bookkeeping only (its addresses are never
+    touched)."""
+    import ctypes
+
+    import numpy as np
+
+    import paged_kv_decode_16_gb300 as pkv
+
+    lib = pkv.load_library()
+    h = ctypes.c_void_p()
+    if lib.kv_pool_create(65536, 16, 8, 128, 1, ctypes.c_void_p(1 << 20),
+                          ctypes.c_void_p(1 << 40), ctypes.byref(h)) != 0:
+        return {"error": "kv_pool_create"}
+    rng = np.random.default_rng(seed)
+    systems = [rng.integers(0, 128000, size=1024).astype(np.int32) for _ in range(16)]
+    reqs = [np.concatenate([systems[int(rng.integers(16))],
+                            rng.integers(0, 128000, size=512).astype(np.int32)])
+            for _ in range(512)]
+    cache = pkv.PrefixCache(h)
+    t_match = t_insert = 0.0
+    matched = total = 0
+    for toks in reqs:
+        t0 = time.perf_counter()
+        got = cache.match(toks)
+        t1 = time.perf_counter()
+        need = len(toks) // 16 - len(got)
+        fresh = (ctypes.c_int32 * need)()
+        lib.kv_pool_alloc_pages(h, need, fresh)
+        row = np.array(got + list(fresh), dtype=np.int32)
+        t2 = time.perf_counter()
+        cache.insert(toks, row)
+        t3 = time.perf_counter()
+        lib.kv_pool_release_pages(h, row.ctypes.data, len(row))
+        t_match += t1 - t0
+        t_insert += t3 - t2
+        matched += len(got)
+        total += len(toks) // 16
+    pages = cache.pages()
+    cache.destroy()
+    lib.kv_pool_destroy(h)
+    n = len(reqs)
+    return {"what": "host radix prefix cache (pkv_prefix_cache_*): match + insert per request, "
+                    "through the Python binding",
+            "requests": n, "tokens_per_request": 1536, "us_per_match": t_match / n * 1e6,
+            "us_per_insert": t_insert / n * 1e6, "matched_page_fraction": matched / total,
+            "cached_pages": pages}
+
+
 # ---------------------------------------------------------------------------
 def run_reference(args):
     """Reference arm: the float64 oracle on the host cores, same metric/unit."""
@@ -701,6 +754,7 @@ def run_ours(args):
             "gbs_logical_plain": (pby["kv_logical"] + pby["qo"]) / (plain_ms * 1e-3) / 1e9},
         "multi_query": multi,
         "other_workloads": others,
+        "prefix_cache": prefix_cache_sample(args.seed),
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "device_status": status,

@@ -14,6 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -270,8 +271,10 @@ class PrefixCache:
 
     @staticmethod
     def _i32(xs):
-        a = (ctypes.c_int32 * max(len(xs), 1))(*[int(x) for x in xs])
-        return a
+        # contiguous int32 numpy arrays are passed without a copy
+        if isinstance(xs, np.ndarray) and xs.dtype == np.int32 and xs.flags.c_contiguous:
+            return xs.ctypes.data if xs.size else None
+        return (ctypes.c_int32 * max(len(xs), 1))(*[int(x) for x in xs])
 
     def insert(self, tokens, pages) -> int:
         """Cache the full pages of `tokens` stored in `pages`; returns how many

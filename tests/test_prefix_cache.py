@@ -189,3 +189,19 @@ def test_threads_keep_the_books(pool):
     assert 4096 - lib.kv_pool_free_count(h) == n   # only the cache holds pages
     c.destroy()
     assert lib.kv_pool_free_count(h) == 4096
+
+
+def test_numpy_token_arrays_match_lists(pool):
+    """int32 numpy arrays (passed without a copy) give what lists give."""
+    import numpy as np
+    lib, h = pool
+    c = pkv.PrefixCache(h)
+    toks = list(range(3000, 3048))
+    pages = alloc(lib, h, 3)
+    assert c.insert(np.array(toks, dtype=np.int32), pages) == 3
+    assert c.match(np.array(toks, dtype=np.int32)) == pages
+    assert c.match(toks) == pages
+    release(lib, h, pages)
+    release(lib, h, pages)
+    release(lib, h, pages)
+    c.destroy()
