@@ -72,10 +72,12 @@ def parse_args():
     ap.add_argument("--profile-only", action="store_true",
                     help="only the warm-up and timed steps (for profiler captures): no copy "
                          "peak, clock sampling, end-to-end leg or CPU baseline")
-    ap.add_argument("--profile-path", choices=["step", "prefix"], default="step",
+    ap.add_argument("--profile-path", choices=["step", "prefix", "multi"], default="step",
                     help="with --profile-only: 'prefix' runs, on the prefix_sharing workload, "
                          "warmup + steps calls of paged_decode_attention_prefix and then one "
-                         "paged_decode_attention (4 launches per call, then 3)")
+                         "paged_decode_attention (4 launches per call, then 3); 'multi' runs "
+                         "warmup + steps calls of paged_decode_attention_multi with 8 query "
+                         "tokens per sequence on the step's cache (3 launches per call)")
     return ap.parse_args()
 
 
@@ -431,6 +433,26 @@ def run_ours(args):
         pkv.paged_decode_combine(out, w.n_kv_heads, ws, nw, variant=var)
 
     peak, peak_kind = measured_peak()
+    if args.profile_only and args.profile_path == "multi":
+        gq = torch.Generator(device=dev).manual_seed(args.seed + 8)
+        qm = torch.randn(B, 8, w.n_q_heads, w.head_dim, generator=gq, device=dev,
+                         dtype=torch.float32).to(w.dtype)
+        om = torch.empty_like(qm)
+        wsm = pkv.alloc_multi_workspace(B, 8, w.n_q_heads, w.n_kv_heads, w.head_dim, nw,
+                                        device=dev, variant=var)
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_decode_attention_multi(qm, w.k_pool, w.v_pool, table, lens, w.scale, om,
+                                             wsm, nw, variant=var)
+        torch.cuda.synchronize()
+        status = pkv.pkv_read_device_status(wsm)
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "workload": args.workload, "path": "multi",
+                              "steps": args.steps, "warmup": args.warmup,
+                              "device_status": status}))
+        pool.destroy()
+        if dist:
+            dist.destroy_process_group()
+        return 0 if status == 0 else 1
     if args.profile_only and args.profile_path == "prefix":
         wp = wl.make("prefix_sharing", seed=args.seed, device=dev)
         tp = torch.from_numpy(wp.page_table).to(dev)
