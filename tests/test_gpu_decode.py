@@ -420,3 +420,26 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     out, ws, status = run_gpu(w, append=False)
     assert status == 0
     assert_close(out, oracle_full(w, append=False), strict=True, what="after the timeout check")
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_batch_beyond_the_plans_shared_memory(variant):
+    """5000 sequences (lengths 0..59): the plan's prefix sums no longer fit its
+    shared memory (4096 sequences) and are searched in global memory; the
+    fused step's append CTAs each take many sequences."""
+    rng = np.random.default_rng(55)
+    lens = rng.integers(0, 60, size=5000)
+    w = wl.make_random(55, batch=5000, n_q_heads=8, n_kv_heads=2, head_dim=64, page_size=16,
+                       dtype=torch.float16, lens=lens, device="cuda", poison=True)
+    out, ws, status = run_gpu(w, append=False, variant=variant)
+    assert status == 0
+    assert_close(out, oracle_full(w, append=False), what="B=5000 decode")
+    # the fused step: append at L - 1 (sequences with L = 0 skip), then attention
+    before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+    table, lens_d, pos = to_dev(w)
+    out2 = torch.full_like(w.q, float("nan"))
+    pkv.paged_decode_step(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens_d,
+                          w.scale, out2, ws, variant=variant)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(ws) == 0
+    assert_close(out2, oracle_full(w, before, append=True), what="B=5000 step")
