@@ -443,3 +443,25 @@ def test_batch_beyond_the_plans_shared_memory(variant):
     torch.cuda.synchronize()
     assert pkv.pkv_read_device_status(ws) == 0
     assert_close(out2, oracle_full(w, before, append=True), what="B=5000 step")
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("P", [64, 256])
+def test_large_pages(P, variant):
+    """Pages of 64 and 256 tokens (a 16-token chunk is one slice of a page):
+    decode and the fused step against the oracle."""
+    rng = np.random.default_rng(60 + P)
+    lens = rng.integers(1, 2000, size=9)
+    w = wl.make_random(60 + P, batch=9, n_q_heads=16, n_kv_heads=4, head_dim=128, page_size=P,
+                       dtype=torch.bfloat16, lens=lens, device="cuda", poison=True)
+    out, ws, status = run_gpu(w, append=False, variant=variant)
+    assert status == 0
+    assert_close(out, oracle_full(w, append=False), what=f"P={P} decode")
+    before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
+    table, lens_d, pos = to_dev(w)
+    out2 = torch.full_like(w.q, float("nan"))
+    pkv.paged_decode_step(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens_d,
+                          w.scale, out2, ws, variant=variant)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(ws) == 0
+    assert_close(out2, oracle_full(w, before, append=True), what=f"P={P} step")
