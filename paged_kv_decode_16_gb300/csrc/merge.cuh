@@ -142,6 +142,80 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
     }
 }
 
+// merge_rows for one warp and up to 32 segments, kRowBatch rows at a time:
+// the m / l loads of all the batch's rows go out together, then their o loads
+// kWarpBlock segments at a time, so up to kWarpBlock segments cost the rows
+// two rounds of loads instead of two each.  Every row's arithmetic is
+// merge_row's and merge_rows' (the same butterflies, the same multiply-add
+// order over the segments), so the results are the same bits.  (The decode
+// kernel calls this; its loads in flight are sized to keep the kernel's
+// register count.)
+constexpr int kRowBatch = 4;
+constexpr int kWarpBlock = 4;
+
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows_warp(const Segs& sg, int ns, int nrows, int lane,
+                                                const RowOut& out_rows) {
+    constexpr int Q = D / 4;
+    static_assert(Q <= 32, "one vector per lane");
+    if (ns > 32) {
+        merge_rows<T, D>(sg, ns, nrows, 0, 1, lane, out_rows);
+        return;
+    }
+    const bool act = lane < Q;
+    for (int g0 = 0; g0 < nrows; g0 += kRowBatch) {
+        float m[kRowBatch], l[kRowBatch], wl[kRowBatch], den[kRowBatch];
+#pragma unroll
+        for (int r = 0; r < kRowBatch; ++r) {
+            const bool ok = lane < ns && g0 + r < nrows;
+            m[r] = ok ? __ldcg(sg.m(lane, g0 + r)) : -INFINITY;
+            l[r] = ok ? __ldcg(sg.l(lane, g0 + r)) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < kRowBatch; ++r) {
+            float M = m[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+            wl[r] = merge_weight(m[r], M);
+            float d = fmaf(wl[r], l[r], 0.f);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(kFull, d, o);
+            den[r] = d;
+        }
+        float4 x[kRowBatch];
+#pragma unroll
+        for (int r = 0; r < kRowBatch; ++r) x[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < ns; s0 += kWarpBlock) {
+            float4 v[kRowBatch][kWarpBlock];
+#pragma unroll
+            for (int r = 0; r < kRowBatch; ++r)
+#pragma unroll
+                for (int j = 0; j < kWarpBlock; ++j) {
+                    const int s = s0 + j;
+                    v[r][j] = act && s < ns && g0 + r < nrows
+                                  ? __ldcg(reinterpret_cast<const float4*>(sg.o(s, g0 + r)) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int r = 0; r < kRowBatch; ++r)
+#pragma unroll
+                for (int j = 0; j < kWarpBlock; ++j) {
+                    const int s = s0 + j;
+                    const float w = __shfl_sync(kFull, wl[r], s & 31);
+                    if (s < ns) {
+                        x[r].x = fmaf(w, v[r][j].x, x[r].x);
+                        x[r].y = fmaf(w, v[r][j].y, x[r].y);
+                        x[r].z = fmaf(w, v[r][j].z, x[r].z);
+                        x[r].w = fmaf(w, v[r][j].w, x[r].w);
+                    }
+                }
+        }
+#pragma unroll
+        for (int r = 0; r < kRowBatch; ++r)
+            if (act && g0 + r < nrows) merge_store<T, D>(x[r], den[r], lane, out_rows(g0 + r));
+    }
+}
+
 // A split segment whose arrival a decode warp reports after its main loop.
 struct PendingMerge {
     int u;       // unit
@@ -163,8 +237,8 @@ __device__ __noinline__ void merge_unit(const DecodeParams& p, const PendingMerg
     const int h = uidx / p.sub_groups;
     const int sgi = uidx - h * p.sub_groups;
     T* out = static_cast<T*>(p.out);
-    merge_rows<T, D>(sg, us.count(), p.rows.rows(sgi), 0, 1, lane,
-                     [&](int g) { return out + p.rows.row(b, h, sgi, g) * D; });
+    merge_rows_warp<T, D>(sg, us.count(), p.rows.rows(sgi), lane,
+                          [&](int g) { return out + p.rows.row(b, h, sgi, g) * D; });
 }
 
 // After a decode warp's main loop: report its split segments (at most two,
