@@ -465,3 +465,33 @@ def test_large_pages(P, variant):
     torch.cuda.synchronize()
     assert pkv.pkv_read_device_status(ws) == 0
     assert_close(out2, oracle_full(w, before, append=True), what=f"P={P} step")
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("hq,hkv,d", [(64, 4, 128), (32, 4, 64), (24, 8, 128)],
+                         ids=["rows16", "rows8_d64", "rows3"])
+def test_kernel_merge_equals_combine_few_segments(hq, hkv, d, variant):
+    """The decode kernel's merge (rows of a unit four at a time) and the combine
+    kernel give the same bits for units of 3, 8 and 16 rows split over a few
+    workers (at most 32 segments each), and both match the oracle."""
+    rng = np.random.default_rng(80 + hq + d)
+    lens = rng.integers(300, 4000, size=6)
+    w = wl.make_random(80 + hq + d, batch=6, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                       page_size=16, dtype=torch.bfloat16, lens=lens, device="cuda")
+    table, lens_d, _ = to_dev(w)
+    nw = 50
+    ws = pkv.alloc_workspace(w.batch, hq, hkv, d, num_workers=nw, variant=variant)
+    outs = []
+    for merge in (True, False):
+        o = torch.full_like(w.q, float("nan"))
+        pkv.paged_decode_plan(lens_d, hq, hkv, d, w.page_size, table.shape[1], ws,
+                              num_workers=nw, variant=variant)
+        pkv.paged_decode_run(w.q, w.k_pool, w.v_pool, table, w.scale, o, ws, num_workers=nw,
+                             variant=variant, merge=merge)
+        if not merge:
+            pkv.paged_decode_combine(o, hkv, ws, num_workers=nw, variant=variant)
+        torch.cuda.synchronize()
+        assert pkv.pkv_read_device_status(ws) == 0
+        outs.append(o)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert_close(outs[0], oracle_full(w), what=f"{hq}/{hkv} heads, D={d}, kernel merge")
