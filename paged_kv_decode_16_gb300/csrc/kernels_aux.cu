@@ -426,7 +426,8 @@ cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
 // ---------------------------------------------------------------------------
 // Combine: one CTA per unit (sequence, KV head, sub-group); units finished by
 // a single worker and empty sequences exit at once.  Each warp merges rows of
-// the unit with merge_rows, the routine the decode kernels' own merge uses.
+// the unit with merge_rows (the decode kernels' own merge does the same
+// arithmetic, several rows per warp).
 // ---------------------------------------------------------------------------
 constexpr int kCombineWarps = 8;
 
