@@ -11,9 +11,10 @@
 // a warp per row finds M and the denominator (lane t takes segments t, t+32,
 // ... in order; the lane sums meet in a fixed butterfly), then each output
 // vector sums its weighted o_s in segment order straight from the slots.  The
-// stand-alone combine kernels and the decode kernels (the warp that finishes
-// the last segment of a unit merges it after its own chunk stream) call the
-// same routines, so the two paths give the same bits.
+// stand-alone combine kernels (merge_rows, a warp per row) and the decode
+// kernels (the warp that finishes the last segment of a unit merges it after
+// its own chunk stream: merge_rows_warp, several rows per warp) do the same
+// arithmetic in the same order, so the two paths give the same bits.
 #pragma once
 
 #include "common.cuh"
