@@ -11,6 +11,9 @@ over many chunk totals, worker counts and random unit layouts, that:
 * worker_of(f) is the range holding f;
 * the slots of all segments are distinct and below U + NW, and a unit that lies
   in one range has exactly one segment.
+
+A second program checks RowShape, the map from a unit's rows to rows of q /
+out when a sequence has several query tokens.
 """
 from __future__ import annotations
 
@@ -117,6 +120,74 @@ def test_schedule_ranges_and_slots(tmp_path):
     src = tmp_path / "schedule_check.cu"
     exe = tmp_path / "schedule_check"
     src.write_text(PROGRAM)
+    build = subprocess.run([nvcc, "-std=c++17", "-I", INCLUDE, "-I", CSRC, str(src), "-o",
+                            str(exe)], capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.startswith("ok"), run.stdout + run.stderr
+
+
+ROWSHAPE_PROGRAM = r"""
+#include <cstdio>
+#include <vector>
+#include "common.cuh"
+using namespace pkv;
+
+int main() {
+    long long checks = 0;
+    const int B = 3, Hkv = 2;
+    for (int group = 1; group <= 12; ++group)
+    for (int hpu = 1; hpu <= group; ++hpu) {
+        if (group % hpu) continue;
+        for (int qn = 1; qn <= 64; qn += (qn < 20 ? 1 : 7))
+        for (int qpu = 1; qpu <= qn && qpu * hpu <= 32; ++qpu) {
+            const int tiles = (qn + qpu - 1) / qpu;
+            const int hq = group * Hkv;
+            RowShape rs{qn, qpu, hpu, group / hpu, group, hq};
+            const int sub_groups = rs.head_blocks * tiles;
+            std::vector<int> hit((size_t)B * qn * hq, 0);
+            for (int b = 0; b < B; ++b)
+            for (int h = 0; h < Hkv; ++h)
+            for (int sg = 0; sg < sub_groups; ++sg) {
+                const int n = rs.rows(sg);
+                if (n < 1 || n > qpu * hpu) { printf("FAIL rows\n"); return 1; }
+                for (int r = 0; r < n; ++r) {
+                    const long long row = rs.row(b, h, sg, r);
+                    if (row < 0 || row >= (long long)B * qn * hq) { printf("FAIL range\n"); return 1; }
+                    hit[row]++;
+                    // the row's token is query(sg, r), its head belongs to KV head h
+                    const long long j = (row / hq) % qn, head = row % hq;
+                    if (j != rs.query(sg, r) || head / group != h || row / ((long long)qn * hq) != b) {
+                        printf("FAIL token/head g=%d hpu=%d qn=%d qpu=%d\n", group, hpu, qn, qpu);
+                        return 1;
+                    }
+                }
+            }
+            for (size_t i = 0; i < hit.size(); ++i)
+                if (hit[i] != 1) {
+                    printf("FAIL cover g=%d hpu=%d qn=%d qpu=%d row=%zu n=%d\n", group, hpu, qn, qpu, i, hit[i]);
+                    return 1;
+                }
+            ++checks;
+        }
+    }
+    printf("ok %lld\n", checks);
+    return 0;
+}
+"""
+
+
+def test_row_shape_covers_every_query_row_once(tmp_path):
+    """RowShape (several query tokens per sequence): for every tile length,
+    head block and query count, the rows of all units (b, KV head, sub-group)
+    hit each row of q / out [B][Qn][Hq] exactly once, at the token query()
+    names and a head of the unit's KV head."""
+    nvcc = _nvcc()
+    if not nvcc:
+        pytest.skip("nvcc is needed to build the host check against the CUDA header")
+    src = tmp_path / "rowshape_check.cu"
+    exe = tmp_path / "rowshape_check"
+    src.write_text(ROWSHAPE_PROGRAM)
     build = subprocess.run([nvcc, "-std=c++17", "-I", INCLUDE, "-I", CSRC, str(src), "-o",
                             str(exe)], capture_output=True, text=True)
     assert build.returncode == 0, build.stderr
