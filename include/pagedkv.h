@@ -188,7 +188,8 @@ pkv_status pkv_prefix_cache_destroy(pkv_prefix_cache* cache);
  * table row, each held by the caller).  Pages of a prefix already cached are
  * left as they are (the first insertion wins); new ones gain the cache's
  * reference.  *n_new (nullable): pages newly cached.  Errors: INVALID_ARG
- * (page id outside the pool), REFCOUNT (a page that is not allocated). */
+ * (page id outside the pool), REFCOUNT (a new page that is not allocated);
+ * on an error nothing is cached. */
 pkv_status pkv_prefix_cache_insert(pkv_prefix_cache* cache, const int32_t* tokens, int n_tokens,
                                    const int32_t* pages, int* n_new);
 

@@ -268,6 +268,10 @@ class PrefixCache:
         self._h = ctypes.c_void_p()
         _check(load_library().pkv_prefix_cache_create(h, ctypes.byref(self._h)),
                "pkv_prefix_cache_create")
+        ps = ctypes.c_int()
+        _check(load_library().kv_pool_info(h, None, ctypes.byref(ps), None, None, None),
+               "kv_pool_info")
+        self._page_size = ps.value
 
     @staticmethod
     def _i32(xs):
@@ -288,13 +292,13 @@ class PrefixCache:
     def match(self, tokens, max_pages: int | None = None) -> list[int]:
         """Pages of the longest cached whole-page prefix of `tokens` (retained
         for the caller)."""
-        cap = len(tokens) if max_pages is None else int(max_pages)
+        cap = len(tokens) // self._page_size if max_pages is None else int(max_pages)
         out = (ctypes.c_int32 * max(cap, 1))()
         n = ctypes.c_int()
         _check(load_library().pkv_prefix_cache_match(self._h, self._i32(tokens), len(tokens), out,
                                                      cap, ctypes.byref(n)),
                "pkv_prefix_cache_match")
-        return list(out[:n.value])
+        return out[:n.value]
 
     def evict(self, n_pages: int) -> int:
         n = ctypes.c_int()

@@ -15,6 +15,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <memory>
 #include <mutex>
 #include <unordered_map>
@@ -33,16 +34,26 @@ struct Node {
     std::unordered_map<uint64_t, std::vector<std::unique_ptr<Node>>> children;
 };
 
-// FNV-1a over the bytes of the token ids.
+// Hash of a page's token ids, two ids per step: h = (rotl(h, 23) ^ w) * K over
+// 64-bit words w (K = 2^64 / golden ratio, odd), then the splitmix64 finaliser
+// so that every input bit reaches the bucket index.  Only spreads the
+// children over buckets: lookups compare the tokens in full.  (A byte-wise
+// FNV-1a took ~8 us of a 96-page match.)
 uint64_t hash_tokens(const int32_t* t, int n) {
-    uint64_t h = 1469598103934665603ull;
-    for (int i = 0; i < n; ++i) {
-        uint32_t v = (uint32_t)t[i];
-        for (int b = 0; b < 4; ++b) {
-            h ^= (v >> (8 * b)) & 0xffu;
-            h *= 1099511628211ull;
-        }
+    constexpr uint64_t K = 0x9e3779b97f4a7c15ull;
+    uint64_t h = (uint64_t)n * K;
+    int i = 0;
+    for (; i + 1 < n; i += 2) {
+        uint64_t w;
+        std::memcpy(&w, t + i, sizeof(w));
+        h = (((h << 23) | (h >> 41)) ^ w) * K;
     }
+    if (i < n) h = (((h << 23) | (h >> 41)) ^ (uint64_t)(uint32_t)t[i]) * K;
+    h ^= h >> 30;
+    h *= 0xbf58476d1ce4e5b9ull;
+    h ^= h >> 27;
+    h *= 0x94d049bb133111ebull;
+    h ^= h >> 31;
     return h;
 }
 
@@ -142,28 +153,35 @@ pkv_status pkv_prefix_cache_insert(pkv_prefix_cache* cache, const int32_t* token
     std::lock_guard<std::mutex> lk(cache->mu);
     Node* n = &cache->root;
     const uint64_t now = ++cache->clock;
-    int added = 0;
-    for (int i = 0; i < full; ++i) {
+    // the part of the path already cached
+    int i = 0;
+    for (; i < full; ++i) {
         const int32_t* t = tokens + (long long)i * P;
-        const uint64_t h = hash_tokens(t, P);
-        Node* c = find_child(n, t, P, h);
-        if (!c) {
-            // the cache's own reference; the caller must hold the page
-            const pkv_status st = kv_pool_retain_pages(cache->pool, &pages[i], 1);
-            if (st != PKV_OK) return st;
-            auto node = std::make_unique<Node>();
-            node->tokens.assign(t, t + P);
-            node->page = pages[i];
-            node->parent = n;
-            c = node.get();
-            n->children[h].push_back(std::move(node));
-            ++cache->pages;
-            ++added;
-        }
+        Node* c = find_child(n, t, P, hash_tokens(t, P));
+        if (!c) break;
         c->last_use = now;
         n = c;
     }
-    if (n_new) *n_new = added;
+    // pages i .. full-1 are new (nothing lies below a node that is missing):
+    // the cache's references to all of them in one step, all or nothing (the
+    // caller must hold each page), then the chain of nodes
+    if (i < full) {
+        const pkv_status st = kv_pool_retain_pages(cache->pool, pages + i, full - i);
+        if (st != PKV_OK) return st;
+    }
+    for (int j = i; j < full; ++j) {
+        const int32_t* t = tokens + (long long)j * P;
+        auto node = std::make_unique<Node>();
+        node->tokens.assign(t, t + P);
+        node->page = pages[j];
+        node->parent = n;
+        node->last_use = now;
+        Node* c = node.get();
+        n->children[hash_tokens(t, P)].push_back(std::move(node));
+        n = c;
+    }
+    cache->pages += full - i;
+    if (n_new) *n_new = full - i;
     return PKV_OK;
 }
 

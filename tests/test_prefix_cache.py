@@ -153,6 +153,15 @@ def test_insert_checks(pool):
     with pytest.raises(pkv.PagedKVError) as e:   # page 7 is not allocated
         c.insert(list(range(16)), [7])
     assert e.value.name == "PKV_ERR_REFCOUNT"
+    # all or nothing: a prompt whose last new page is not allocated caches none
+    # of its new pages and leaves their counts alone
+    got = alloc(lib, h, 2)
+    with pytest.raises(pkv.PagedKVError) as e:
+        c.insert(list(range(48)), got + [7])
+    assert e.value.name == "PKV_ERR_REFCOUNT"
+    assert c.pages() == 0 and c.match(list(range(48))) == []
+    assert [lib.kv_pool_refcount(h, p) for p in got] == [1, 1]
+    release(lib, h, got)
     c.destroy()
 
 
