@@ -17,6 +17,7 @@
 #include <algorithm>
 #include <cstring>
 #include <memory>
+#include <new>
 #include <mutex>
 #include <unordered_map>
 #include <vector>
@@ -26,13 +27,37 @@
 
 namespace {
 
+struct Node;
+struct NodeFree {
+    void operator()(Node* n) const;
+};
+using NodePtr = std::unique_ptr<Node, NodeFree>;
+
+// One allocation per node: the node, then its page's token ids.
 struct Node {
-    std::vector<int32_t> tokens;  // the page's token ids (empty at the root)
     int32_t page = -1;
+    int ntok = 0;  // token ids of the page (0 at the root)
     Node* parent = nullptr;
     uint64_t last_use = 0;
-    std::unordered_map<uint64_t, std::vector<std::unique_ptr<Node>>> children;
+    std::unordered_multimap<uint64_t, NodePtr> children;  // by hash_tokens of their ids
+
+    const int32_t* tokens() const { return reinterpret_cast<const int32_t*>(this + 1); }
+    int32_t* tokens() { return reinterpret_cast<int32_t*>(this + 1); }
+
+    static NodePtr make(const int32_t* t, int n) {
+        void* mem = ::operator new(sizeof(Node) + sizeof(int32_t) * (size_t)n);
+        Node* node = new (mem) Node;
+        node->ntok = n;
+        std::memcpy(node->tokens(), t, sizeof(int32_t) * (size_t)n);
+        return NodePtr(node);
+    }
 };
+static_assert(alignof(Node) >= alignof(int32_t), "token ids follow the node");
+
+void NodeFree::operator()(Node* n) const {
+    n->~Node();
+    ::operator delete(n);
+}
 
 // Hash of a page's token ids, two ids per step: h = (rotl(h, 23) ^ w) * K over
 // 64-bit words w (K = 2^64 / golden ratio, odd), then the splitmix64 finaliser
@@ -58,11 +83,11 @@ uint64_t hash_tokens(const int32_t* t, int n) {
 }
 
 Node* find_child(Node* n, const int32_t* t, int len, uint64_t h) {
-    auto it = n->children.find(h);
-    if (it == n->children.end()) return nullptr;
-    for (auto& c : it->second)
-        if ((int)c->tokens.size() == len && std::equal(c->tokens.begin(), c->tokens.end(), t))
-            return c.get();
+    auto range = n->children.equal_range(h);
+    for (auto it = range.first; it != range.second; ++it) {
+        Node* c = it->second.get();
+        if (c->ntok == len && std::equal(c->tokens(), c->tokens() + len, t)) return c;
+    }
     return nullptr;
 }
 
@@ -72,7 +97,7 @@ struct pkv_prefix_cache {
     pkv_pool* pool = nullptr;
     int page_size = 0;
     std::mutex mu;  // guards the tree; taken before the pool's own lock
-    Node root;
+    Node root;  // no token ids follow it: tokens() of the root is never read
     uint64_t clock = 0;
     int pages = 0;  // nodes below the root
 };
@@ -81,42 +106,38 @@ namespace {
 
 // Release every page below n (children first) and drop the nodes.
 void release_subtree(pkv_prefix_cache* c, Node* n) {
-    for (auto& kv : n->children)
-        for (auto& ch : kv.second) {
-            release_subtree(c, ch.get());
-            kv_pool_release_pages(c->pool, &ch->page, 1);
-            --c->pages;
-        }
+    for (auto& kv : n->children) {
+        Node* ch = kv.second.get();
+        release_subtree(c, ch);
+        kv_pool_release_pages(c->pool, &ch->page, 1);
+        --c->pages;
+    }
     n->children.clear();
 }
 
 // The least recently used leaf whose page only the cache references.
 Node* lru_evictable_leaf(pkv_prefix_cache* c, Node* n, Node* best) {
-    for (auto& kv : n->children)
-        for (auto& ch : kv.second) {
-            Node* x = ch.get();
-            if (x->children.empty()) {
-                if (kv_pool_refcount(c->pool, x->page) == 1 &&
-                    (!best || x->last_use < best->last_use))
-                    best = x;
-            } else {
-                best = lru_evictable_leaf(c, x, best);
-            }
+    for (auto& kv : n->children) {
+        Node* x = kv.second.get();
+        if (x->children.empty()) {
+            if (kv_pool_refcount(c->pool, x->page) == 1 &&
+                (!best || x->last_use < best->last_use))
+                best = x;
+        } else {
+            best = lru_evictable_leaf(c, x, best);
         }
+    }
     return best;
 }
 
 void remove_leaf(Node* leaf) {
     Node* p = leaf->parent;
-    const uint64_t h = hash_tokens(leaf->tokens.data(), (int)leaf->tokens.size());
-    auto it = p->children.find(h);
-    auto& v = it->second;
-    for (size_t i = 0; i < v.size(); ++i)
-        if (v[i].get() == leaf) {
-            v.erase(v.begin() + (long)i);
-            break;
+    auto range = p->children.equal_range(hash_tokens(leaf->tokens(), leaf->ntok));
+    for (auto it = range.first; it != range.second; ++it)
+        if (it->second.get() == leaf) {
+            p->children.erase(it);
+            return;
         }
-    if (v.empty()) p->children.erase(it);
 }
 
 }  // namespace
@@ -171,13 +192,12 @@ pkv_status pkv_prefix_cache_insert(pkv_prefix_cache* cache, const int32_t* token
     }
     for (int j = i; j < full; ++j) {
         const int32_t* t = tokens + (long long)j * P;
-        auto node = std::make_unique<Node>();
-        node->tokens.assign(t, t + P);
+        NodePtr node = Node::make(t, P);
         node->page = pages[j];
         node->parent = n;
         node->last_use = now;
         Node* c = node.get();
-        n->children[hash_tokens(t, P)].push_back(std::move(node));
+        n->children.emplace(hash_tokens(t, P), std::move(node));
         n = c;
     }
     cache->pages += full - i;
