@@ -200,8 +200,10 @@ pkv_status pkv_prefix_cache_match(pkv_prefix_cache* cache, const int32_t* tokens
                                   int32_t* pages_out, int max_pages, int* n_pages);
 
 /* Free up to n_pages cached pages: least recently used leaves whose page only
- * the cache still references (a leaf's parent becomes a leaf in turn).
- * *n_freed (nullable): pages returned to the pool. */
+ * the cache still references (a leaf's parent becomes a leaf in turn; a page
+ * that another thread releases during the call waits for the next call).
+ * O(cached pages + n_pages log cached pages).  *n_freed (nullable): pages
+ * returned to the pool. */
 pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_freed);
 
 /* Pages currently cached (-1 for NULL). */

@@ -15,9 +15,11 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <functional>
 #include <cstring>
 #include <memory>
 #include <new>
+#include <queue>
 #include <mutex>
 #include <unordered_map>
 #include <vector>
@@ -115,19 +117,22 @@ void release_subtree(pkv_prefix_cache* c, Node* n) {
     n->children.clear();
 }
 
-// The least recently used leaf whose page only the cache references.
-Node* lru_evictable_leaf(pkv_prefix_cache* c, Node* n, Node* best) {
+// Leaves whose page only the cache references, by last use (oldest on top).
+// Every insert or match stamps the nodes of one path with a fresh clock
+// value, so no two leaves share a stamp and the order is total.
+using LeafHeap = std::priority_queue<std::pair<uint64_t, Node*>,
+                                     std::vector<std::pair<uint64_t, Node*>>,
+                                     std::greater<std::pair<uint64_t, Node*>>>;
+
+void collect_evictable_leaves(pkv_prefix_cache* c, Node* n, LeafHeap& heap) {
     for (auto& kv : n->children) {
         Node* x = kv.second.get();
         if (x->children.empty()) {
-            if (kv_pool_refcount(c->pool, x->page) == 1 &&
-                (!best || x->last_use < best->last_use))
-                best = x;
+            if (kv_pool_refcount(c->pool, x->page) == 1) heap.emplace(x->last_use, x);
         } else {
-            best = lru_evictable_leaf(c, x, best);
+            collect_evictable_leaves(c, x, heap);
         }
     }
-    return best;
 }
 
 void remove_leaf(Node* leaf) {
@@ -233,15 +238,27 @@ pkv_status pkv_prefix_cache_match(pkv_prefix_cache* cache, const int32_t* tokens
 pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_freed) {
     if (!cache || n_pages < 0) return PKV_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(cache->mu);
+    // the least recently used evictable leaf, one at a time: a parent whose
+    // last child goes becomes a leaf itself and joins the heap
+    LeafHeap heap;
+    if (n_pages > 0) collect_evictable_leaves(cache, &cache->root, heap);
     int freed = 0;
-    while (freed < n_pages) {
-        Node* leaf = lru_evictable_leaf(cache, &cache->root, nullptr);
-        if (!leaf) break;
+    while (freed < n_pages && !heap.empty()) {
+        Node* leaf = heap.top().second;
+        heap.pop();
+        if (kv_pool_refcount(cache->pool, leaf->page) != 1) continue;  // retained meanwhile
         const pkv_status st = kv_pool_release_pages(cache->pool, &leaf->page, 1);
-        if (st != PKV_OK) return st;
+        if (st != PKV_OK) {
+            if (n_freed) *n_freed = freed;
+            return st;
+        }
+        Node* parent = leaf->parent;
         remove_leaf(leaf);
         --cache->pages;
         ++freed;
+        if (parent != &cache->root && parent->children.empty() &&
+            kv_pool_refcount(cache->pool, parent->page) == 1)
+            heap.emplace(parent->last_use, parent);
     }
     if (n_freed) *n_freed = freed;
     return PKV_OK;

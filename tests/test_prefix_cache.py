@@ -144,6 +144,66 @@ def test_eviction_frees_lru_leaves_only_the_cache_holds(pool):
     assert lib.kv_pool_free_count(h) == 4096
 
 
+def test_eviction_order_matches_a_model(pool):
+    """One page at a time, evict frees exactly the least recently used leaf
+    whose page only the cache holds, as a model of the tree predicts: every
+    match and insert stamps the nodes of its path with a fresh clock value;
+    a parent whose last child goes becomes a leaf."""
+    lib, h = pool
+    c = pkv.PrefixCache(h)
+    rnd = random.Random(11)
+    P = 16
+    systems = [[rnd.randrange(50) for _ in range(P * rnd.randint(1, 4))] for _ in range(6)]
+    stamp, page = {}, {}     # path (tuple of page token tuples) -> last use, page id
+    clock = 0
+    held = []                # references the requests still hold
+
+    def pages_of(toks):
+        return [tuple(toks[i * P:(i + 1) * P]) for i in range(len(toks) // P)]
+
+    for _ in range(60):
+        toks = systems[rnd.randrange(6)] + [rnd.randrange(50) for _ in range(P * rnd.randint(0, 3))]
+        got = c.match(toks)
+        clock += 1
+        keys = pages_of(toks)
+        for k in range(len(got)):
+            stamp[tuple(keys[:k + 1])] = clock
+        fresh = alloc(lib, h, len(keys) - len(got)) if len(keys) > len(got) else []
+        row = got + fresh
+        c.insert(toks, row)
+        clock += 1
+        for k in range(len(keys)):
+            path = tuple(keys[:k + 1])
+            page.setdefault(path, row[k])
+            stamp[path] = clock
+        if rnd.random() < 0.7:
+            release(lib, h, row)
+        else:
+            held.append(row)
+    assert c.pages() == len(page)
+
+    def expected():
+        leaves = [q for q in page if not any(len(o) == len(q) + 1 and o[:-1] == q for o in page)]
+        free = [q for q in leaves if lib.kv_pool_refcount(h, page[q]) == 1]
+        return min(free, key=lambda q: stamp[q]) if free else None
+
+    evicted = 0
+    while True:
+        q = expected()
+        if q is None:
+            assert c.evict(1) == 0
+            break
+        assert c.evict(1) == 1
+        assert lib.kv_pool_refcount(h, page[q]) == 0, f"evicted the wrong page after {evicted}"
+        del page[q]
+        evicted += 1
+    assert evicted > 10 and c.pages() == len(page)
+    for row in held:
+        release(lib, h, row)
+    c.destroy()
+    assert lib.kv_pool_free_count(h) == 4096
+
+
 def test_insert_checks(pool):
     lib, h = pool
     c = pkv.PrefixCache(h)
