@@ -286,6 +286,15 @@ def cpu_oracle_sample(w, target_s: float = 12.0, one_core_s: float = 4.0):
     return res
 
 
+def host_sample(fn, *args) -> dict:
+    """A host-only side measurement: its failure is reported under its own key
+    instead of costing the whole line."""
+    try:
+        return fn(*args)
+    except Exception as e:  # noqa: BLE001 (reported in the line)
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
 def prefix_cache_sample(seed: int) -> dict:
     """The host prefix cache on a serving-like request stream: 512 requests,
     each one of 16 system prompts of 1024 tokens plus a private 512-token
@@ -776,7 +785,7 @@ def run_ours(args):
             "gbs_logical_plain": (pby["kv_logical"] + pby["qo"]) / (plain_ms * 1e-3) / 1e9},
         "multi_query": multi,
         "other_workloads": others,
-        "prefix_cache": prefix_cache_sample(args.seed),
+        "prefix_cache": host_sample(prefix_cache_sample, args.seed),
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "device_status": status,
