@@ -69,6 +69,12 @@ def parse_args():
     ap.add_argument("--num-workers", type=int, default=0)
     ap.add_argument("--variant", choices=["auto", "cuda_cores", "tensor_cores"], default="auto",
                     help="decode kernel (auto = tensor cores)")
+    ap.add_argument("--report", action="store_true",
+                    help="per-configuration results instead of the bench line: for each named "
+                         "workload the step's GPU time (L2 flushed, median of 50 after 10 "
+                         "warm-up; and warm back to back), GB/s, %% of the same-run copy peak, "
+                         "seqs/s, max abs / rel error of every output against the oracle, and "
+                         "the oracle's time on all host cores and on one (median of 3 after 1)")
     ap.add_argument("--profile-only", action="store_true",
                     help="only the warm-up and timed steps (for profiler captures): no copy "
                          "peak, clock sampling, end-to-end leg or CPU baseline")
@@ -237,6 +243,25 @@ def copy_peak_gbs(torch, dev) -> float:
     return 2 * n * 2 / (best * 1e-3) / 1e9
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def _oracle_rate(w, q, kp, vp, target_s: float):
     """Sequences one by one (all query heads), in a fixed random order, for
     about target_s seconds: (bytes, sequences, seconds)."""
@@ -261,28 +286,46 @@ def _oracle_rate(w, q, kp, vp, target_s: float):
     return nbytes, seqs, time.perf_counter() - t0
 
 
-def cpu_oracle_sample(w, target_s: float = 12.0, one_core_s: float = 4.0):
-    """Time the oracle on host copies of the workload, on all host cores (the
-    reported value) and then on one core."""
+def oracle_full_median(w, q, kp, vp, reps: int = 3) -> float:
+    """Seconds of one float64 oracle pass over the whole batch: the median of
+    `reps` passes after one warm-up pass (input generation and copies excluded)."""
+    import oracle
+
+    times = []
+    for i in range(reps + 1):
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, kp, vp, w.page_table, w.context_lens, w.scale, w.dtype_name)
+        if i:
+            times.append(time.perf_counter() - t0)
+    return statistics.median(times)
+
+
+def cpu_oracle_sample(w, one_core: bool = True):
+    """Time the oracle on host copies of the whole workload, on all host cores
+    (the reported value) and then on one core: median of 3 passes after one
+    warm-up pass each."""
     import oracle
     from paged_kv_decode_16_gb300 import workloads as wl
 
     q = wl.to_bits(w.q)
     kp, vp = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
+    by = step_bytes(w)["decode"]
     cores = oracle.max_threads()
-    nbytes, seqs, dt = _oracle_rate(w, q, kp, vp, target_s)
-    res = {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-           "seqs_per_s": seqs / dt,
-           "sample": f"{seqs} sequences x all {w.n_q_heads} query heads of the {w.name} "
-                     f"workload, float64 oracle with OpenMP over query heads, {dt:.1f} s"}
-    if one_core_s > 0:
+    dt = oracle_full_median(w, q, kp, vp)
+    res = {"value": by / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "cpu_model": cpu_model(), "seconds_per_pass": dt, "seqs_per_s": w.batch / dt,
+           "sample": f"the whole {w.name} batch ({w.batch} sequences x {w.n_q_heads} query "
+                     f"heads), float64 oracle with OpenMP over query rows; median of 3 passes "
+                     f"after 1 warm-up pass"}
+    if one_core:
         oracle.set_threads(1)
         try:
-            nb1, s1, dt1 = _oracle_rate(w, q, kp, vp, one_core_s)
+            dt1 = oracle_full_median(w, q, kp, vp)
         finally:
             oracle.set_threads(cores)
-        res["one_core"] = {"value": nb1 / dt1 / 1e9, "unit": UNIT, "seqs_per_s": s1 / dt1,
-                           "sample": f"{s1} sequences, {dt1:.1f} s on 1 thread"}
+        res["one_core"] = {"value": by / dt1 / 1e9, "unit": UNIT, "seqs_per_s": w.batch / dt1,
+                           "seconds_per_pass": dt1,
+                           "sample": "the same passes on 1 thread (median of 3 after 1)"}
     return res
 
 
@@ -349,6 +392,15 @@ def prefix_cache_sample(seed: int) -> dict:
 
 
 # ---------------------------------------------------------------------------
+def reference_step(w, q, kp, vp, target_s: float) -> dict:
+    """One reference-arm step: the oracle over sequences of the workload (all
+    query heads each, fixed random order) for about target_s seconds."""
+    nbytes, seqs, dt = _oracle_rate(w, q, kp, vp, target_s)
+    return {"value": nbytes / dt / 1e9, "seqs_per_s": seqs / dt,
+            "sample": f"{seqs} sequences x all {w.n_q_heads} query heads of the {w.name} "
+                      f"workload, float64 oracle with OpenMP over query heads, {dt:.2f} s"}
+
+
 def run_reference(args):
     """Reference arm: the float64 oracle on the host cores, same metric/unit."""
     ws, rank, _ = dist_info()
@@ -356,23 +408,23 @@ def run_reference(args):
         return 0
     import torch  # noqa: F401  (workload tensors live on the CPU here)
 
+    import oracle
     from paged_kv_decode_16_gb300 import workloads as wl
     w = wl.make(args.workload, seed=args.seed, device="cpu")
+    kp, vp = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
     if w.append:
-        import oracle
-        kp, vp = oracle.kv_append(wl.to_bits(w.k_pool), wl.to_bits(w.v_pool),
-                                  wl.to_bits(w.k_new), wl.to_bits(w.v_new), w.page_table,
-                                  w.positions)
-        w.k_pool = torch.from_numpy(kp.view("int16")).view(w.dtype)
-        w.v_pool = torch.from_numpy(vp.view("int16")).view(w.dtype)
+        kp, vp = oracle.kv_append(kp, vp, wl.to_bits(w.k_new), wl.to_bits(w.v_new),
+                                  w.page_table, w.positions)
+    q = wl.to_bits(w.q)
     # about 150 s in all: each step samples at least one sequence (a few ms)
     budget = min(12.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, target_s=budget, one_core_s=0)
+        reference_step(w, q, kp, vp, budget)
     vals, seqs = [], []
+    r = None
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = cpu_oracle_sample(w, target_s=budget, one_core_s=0)
+        r = reference_step(w, q, kp, vp, budget)
         vals.append(r["value"])
         seqs.append(r["seqs_per_s"])
     wall = time.perf_counter() - t0
@@ -386,8 +438,9 @@ def run_reference(args):
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
                    "storage_dtype": w.dtype_name, "seed": args.seed},
         "seqs_per_s": statistics.mean(seqs) if seqs else 0.0,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"] if vals else None,
-                         "kind": "oracle", "sample": r["sample"] if vals else ""},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": r["sample"] if r else ""},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -802,10 +855,148 @@ def run_ours(args):
     return 0
 
 
+def _errors(got, ref):
+    """max |gpu - ref| and max |gpu - ref| / max(|ref|, 0.2) over every element."""
+    import numpy as np
+    err = np.abs(got - ref)
+    return float(err.max(initial=0.0)), float((err / np.maximum(np.abs(ref), 0.2)).max(initial=0.0))
+
+
+def run_report(args):
+    """Per-configuration results of the five named workloads (one GPU)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import paged_kv_decode_16_gb300 as pkv
+    from paged_kv_decode_16_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    stream = torch.cuda.current_stream(dev)
+    copy_peak = copy_peak_gbs(torch, dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def cold_ms(fn, n=50, warm=10):
+        for _ in range(warm):
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.fill_(1.0)  # untimed write of twice the L2 size
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def warm_ms(fn, n=500):
+        for _ in range(20):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    rows = []
+    for name in wl.NAMES:
+        w = wl.make(name, seed=args.seed, device=dev)
+        table = torch.from_numpy(w.page_table).to(dev)
+        lens = torch.from_numpy(w.context_lens).to(dev)
+        pos = torch.from_numpy(w.positions).to(dev)
+        out = torch.empty_like(w.q)
+        ws = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, device=dev)
+        kb, vb = wl.to_bits(w.k_pool), wl.to_bits(w.v_pool)
+
+        def step():
+            pkv.paged_decode_step(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens,
+                                  w.scale, out, ws)
+
+        step()
+        torch.cuda.synchronize()
+        status = pkv.pkv_read_device_status(ws)
+        kp, vp = oracle.kv_append(kb, vb, wl.to_bits(w.k_new), wl.to_bits(w.v_new),
+                                  w.page_table, w.positions)
+        append_exact = bool(np.array_equal(kp, wl.to_bits(w.k_pool)) and
+                            np.array_equal(vp, wl.to_bits(w.v_pool)))
+        q_bits = wl.to_bits(w.q)
+        ref = oracle.paged_decode(q_bits, kp, vp, w.page_table, w.context_lens, w.scale,
+                                  w.dtype_name)
+        got = out.float().cpu().numpy().astype(np.float64)
+        max_abs, max_rel = _errors(got, ref)
+        by = step_bytes(w)
+        t_cold, t_warm = cold_ms(step), warm_ms(step)
+        cores = oracle.max_threads()
+        cpu_all = oracle_full_median(w, q_bits, kp, vp)
+        oracle.set_threads(1)
+        try:
+            cpu_one = oracle_full_median(w, q_bits, kp, vp)
+        finally:
+            oracle.set_threads(cores)
+        r = {"workload": name, "call": "paged_decode_step (append + plan + decode + combine)",
+             "batch": w.batch, "bytes": by["step"], "ms_cold": t_cold, "ms_warm": t_warm,
+             "gbs_cold": by["step"] / (t_cold * 1e-3) / 1e9,
+             "gbs_warm": by["step"] / (t_warm * 1e-3) / 1e9,
+             "pct_of_copy_peak_cold": 100.0 * by["step"] / (t_cold * 1e-3) / 1e9 / copy_peak,
+             "seqs_per_s_cold": w.batch / (t_cold * 1e-3), "max_abs_err": max_abs,
+             "max_rel_err": max_rel, "append_bit_exact": append_exact, "device_status": status,
+             "cpu_oracle_s_all_cores": cpu_all, "cpu_oracle_s_one_core": cpu_one,
+             "cpu_cores": cores}
+        rows.append(r)
+        print(json.dumps(r), flush=True)
+        if name == "prefix_sharing":
+            wsp = pkv.alloc_prefix_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                             device=dev)
+            out2 = torch.empty_like(w.q)
+
+            def cascade():
+                pkv.paged_decode_attention_prefix(w.q, w.k_pool, w.v_pool, table, lens, w.scale,
+                                                  w.prefix_len, out2, wsp)
+
+            cascade()
+            torch.cuda.synchronize()
+            st2 = pkv.pkv_read_device_status(wsp)
+            a2, r2 = _errors(out2.float().cpu().numpy().astype(np.float64), ref)
+            c_cold, c_warm = cold_ms(cascade), warm_ms(cascade)
+            uniq = by["kv_unique"] + by["qo"]
+            r = {"workload": name, "call": "paged_decode_attention_prefix (cascade, no append)",
+                 "batch": w.batch, "bytes": uniq, "ms_cold": c_cold, "ms_warm": c_warm,
+                 "gbs_cold": uniq / (c_cold * 1e-3) / 1e9, "gbs_warm": uniq / (c_warm * 1e-3) / 1e9,
+                 "pct_of_copy_peak_cold": 100.0 * uniq / (c_cold * 1e-3) / 1e9 / copy_peak,
+                 "seqs_per_s_cold": w.batch / (c_cold * 1e-3), "max_abs_err": a2,
+                 "max_rel_err": r2, "device_status": st2}
+            rows.append(r)
+            print(json.dumps(r), flush=True)
+        del w, table, lens, pos, out, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"copy_peak_gbs": copy_peak, "cpu_model": cpu_model(),
+                      "gpu": torch.cuda.get_device_name(dev)}))
+    print("| config | call | GPU µs (L2 flushed / warm) | GB/s (flushed) | % of copy peak | "
+          "seqs/s | max abs err | max rel err | oracle s (all cores / 1 core) |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for r in rows:
+        cpu = (f"{r['cpu_oracle_s_all_cores']:.3f} / {r['cpu_oracle_s_one_core']:.2f}"
+               if "cpu_oracle_s_all_cores" in r else "—")
+        print(f"| {r['workload']} | {r['call'].split(' ')[0]} | {r['ms_cold'] * 1e3:.1f} / "
+              f"{r['ms_warm'] * 1e3:.1f} | {r['gbs_cold']:.0f} | {r['pct_of_copy_peak_cold']:.1f} | "
+              f"{r['seqs_per_s_cold']:.3g} | {r['max_abs_err']:.2e} | {r['max_rel_err']:.2e} | "
+              f"{cpu} |")
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.report:
+        return run_report(args)
     return run_ours(args)
 
 

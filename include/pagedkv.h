@@ -209,6 +209,25 @@ pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_f
 /* Pages currently cached (-1 for NULL). */
 int pkv_prefix_cache_pages(const pkv_prefix_cache* cache);
 
+/* Counters of a cache since its creation or the last reset (CacheIR,
+ * "Current Capabilities": prefix-cache reuse with hit/miss counters).  A
+ * lookup is one successful pkv_prefix_cache_match; it asks for
+ * min(max_pages, n_tokens / page_size) whole pages. */
+typedef struct pkv_prefix_cache_stats {
+    uint64_t lookups;         /* match calls */
+    uint64_t hits;            /* lookups that matched at least one page */
+    uint64_t misses;          /* lookups that matched none */
+    uint64_t pages_hit;       /* pages handed out by matches */
+    uint64_t pages_missed;    /* pages asked for and not found */
+    uint64_t pages_inserted;  /* pages newly cached by inserts */
+    uint64_t pages_evicted;   /* pages returned to the pool by evictions */
+} pkv_prefix_cache_stats;
+
+/* Copy the counters to *out (host); reset != 0 zeroes them afterwards, in
+ * the same locked step.  INVALID_ARG for a NULL cache or out. */
+pkv_status pkv_prefix_cache_get_stats(pkv_prefix_cache* cache, int reset,
+                                      pkv_prefix_cache_stats* out);
+
 /* ------------------------------------------------------------------------
  * Per-step KV append
  * (TorchInferno, "OpenAI-Compatible Serving" knob list: KV-append kernel;
@@ -492,12 +511,19 @@ pkv_status paged_decode_attention_multi(const void* q, const void* k_pool, const
  *   - Every GPU that loads the library holds the array until the process exits.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current) and caches it; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The cached address belongs to the device's
+ *     context of that moment: resetting the device (cudaDeviceReset) after the
+ *     first call is not supported.
+ *   - Operands must be on the current device: the call runs on it and uses its
+ *     array.
  *   - All calls share the one array and it keeps the last call's contents; the
  *     plan kernel of each call rewrites every field that must start fresh (the
  *     header, counters and the status word), so nothing needs clearing by the
  *     caller.  Calls that overlap on the GPU (on different streams, or from
- *     different threads without ordering) race on the array: order them. */
+ *     different threads without ordering) race on the array: order them.
+ *   - Data errors (page ids outside the pool, lengths beyond the table row)
+ *     are skipped and flagged in the array's status word, as in the workspace
+ *     of paged_decode_attention; pkv_read_no_alloc_status reads it. */
 #define PKV_NO_ALLOC_SCRATCH_BYTES (32u << 20)
 
 pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool,
@@ -513,6 +539,13 @@ pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, co
  * synchronises with the device.  Returns DEVICE_CHECK when any bit is set,
  * OK otherwise (CUDA on a failed copy). */
 pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out);
+
+/* The same for the last paged_decode_attention_no_alloc call on the current
+ * device: the PKV_DEV_* bits in the status word of the library's fixed
+ * scratch (which the caller never sees).  Synchronises with the device;
+ * returns DEVICE_CHECK when any bit is set, OK otherwise (CUDA on a failed
+ * copy or address lookup). */
+pkv_status pkv_read_no_alloc_status(uint32_t* status_out);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ __all__ = [
     "check_bounded_wait",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
-    "pkv_read_device_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
+    "pkv_read_device_status", "pkv_read_no_alloc_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
     "VARIANT_AUTO", "VARIANT_CUDA_CORES", "VARIANT_TENSOR_CORES",
 ]
 
@@ -42,6 +42,10 @@ VARIANT_AUTO, VARIANT_CUDA_CORES, VARIANT_TENSOR_CORES = 0, 1, 2
 # size of the library's fixed device scratch (PKV_NO_ALLOC_SCRATCH_BYTES)
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
 _DT = {torch.float16: 0, torch.bfloat16: 1}
+
+# fields of pkv_prefix_cache_stats, in order (all uint64)
+PREFIX_STATS_FIELDS = ("lookups", "hits", "misses", "pages_hit", "pages_missed",
+                       "pages_inserted", "pages_evicted")
 
 _lib = None
 
@@ -89,6 +93,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "pkv_prefix_cache_match": ([V, V, I, V, I, ctypes.POINTER(I)], I),
         "pkv_prefix_cache_evict": ([V, I, ctypes.POINTER(I)], I),
         "pkv_prefix_cache_pages": ([V], I),
+        "pkv_prefix_cache_get_stats": ([V, I, V], I),
         "kv_append_rope": ([V, V, V, V, V, I, V, I, I, ctypes.c_double, V, V, F, V, V, V], I),
         "paged_decode_prefix_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "paged_decode_multi_workspace_size": ([I, I, I, I, I, I, I, ctypes.POINTER(Z)], I),
@@ -111,6 +116,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         "paged_decode_attention_no_alloc": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, I, I,
                                              V], I),
         "pkv_read_device_status": ([V, ctypes.POINTER(ctypes.c_uint32)], I),
+        "pkv_read_no_alloc_status": ([ctypes.POINTER(ctypes.c_uint32)], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -149,17 +155,30 @@ def _stream(stream):
     return torch.cuda.current_stream().cuda_stream
 
 
+def _on_current_device(t) -> bool:
+    # the library launches on the current device's stream and, for the
+    # allocation-free call, uses that device's scratch: operands elsewhere
+    # would be read by the wrong GPU
+    idx = t.device.index
+    return idx is None or idx == torch.cuda.current_device()
+
+
 def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
-    """A contiguous CUDA tensor (of dtype / ndim when given), else raise."""
+    """A contiguous CUDA tensor on the current device (of dtype / ndim when
+    given), else raise."""
     try:
         ok = (t.is_cuda and t.is_contiguous() and (dtype is None or t.dtype == dtype)
-              and (ndim is None or t.dim() == ndim))
+              and (ndim is None or t.dim() == ndim) and _on_current_device(t))
     except AttributeError:
         raise TypeError(f"{name} must be a torch tensor") from None
     if ok:
         return t
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
+    if not _on_current_device(t):
+        raise ValueError(f"{name} is on {t.device} but the current device is "
+                         f"cuda:{torch.cuda.current_device()}: call inside "
+                         f"torch.cuda.device({t.device})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -308,6 +327,14 @@ class PrefixCache:
 
     def pages(self) -> int:
         return load_library().pkv_prefix_cache_pages(self._h)
+
+    def stats(self, reset: bool = False) -> dict:
+        """Lookup, hit and miss counters and pages inserted / evicted
+        (pkv_prefix_cache_get_stats); reset zeroes them after reading."""
+        buf = (ctypes.c_uint64 * len(PREFIX_STATS_FIELDS))()
+        _check(load_library().pkv_prefix_cache_get_stats(self._h, int(bool(reset)), buf),
+               "pkv_prefix_cache_get_stats")
+        return dict(zip(PREFIX_STATS_FIELDS, (int(x) for x in buf)))
 
     def destroy(self) -> None:
         if self._h:
@@ -656,4 +683,14 @@ def pkv_read_device_status(workspace: torch.Tensor) -> int:
     code = load_library().pkv_read_device_status(_ptr(workspace), ctypes.byref(v))
     if code not in (0, 7):
         _check(code, "pkv_read_device_status")
+    return v.value
+
+
+def pkv_read_no_alloc_status() -> int:
+    """The status word of the last paged_decode_attention_no_alloc call on the
+    current device (synchronises)."""
+    v = ctypes.c_uint32()
+    code = load_library().pkv_read_no_alloc_status(ctypes.byref(v))
+    if code not in (0, 7):
+        _check(code, "pkv_read_no_alloc_status")
     return v.value

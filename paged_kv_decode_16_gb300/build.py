@@ -4,11 +4,16 @@ Each translation unit is compiled in parallel with
 ``-gencode arch=compute_103a,code=sm_103a -O3 -lineinfo`` and the objects are
 linked into ``paged_kv_decode_16_gb300/_build/libpagedkv.so`` (static CUDA
 runtime, so loading it needs no GPU).  Rebuilds only when a source or header
-is newer than the library.
+is newer than the library.  Concurrent builds (two test processes, a test and
+the benchmark) take an exclusive file lock on ``_build/.lock`` and compile
+into an object directory of their own, so they never share a half-written
+object; the second one to get the lock finds the library up to date.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
+import contextlib
+import fcntl
 import glob
 import os
 import shutil
@@ -51,19 +56,38 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
+@contextlib.contextmanager
+def _build_lock():
+    os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".lock"), "w") as f:
+        fcntl.flock(f, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(f, fcntl.LOCK_UN)
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     """Compile every source for sm_103a and link libpagedkv.so; return its path."""
     if not force and up_to_date():
         return LIB
+    with _build_lock():
+        if not force and up_to_date():  # built by another process meanwhile
+            return LIB
+        return _build_locked(verbose, ptxas_verbose)
+
+
+def _build_locked(verbose: bool, ptxas_verbose: bool) -> str:
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    obj_dir = os.path.join(OUT_DIR, f"obj{os.getpid()}")
+    os.makedirs(obj_dir, exist_ok=True)
     common = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
               *ARCH]
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src: str):
-        obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, "-c", src, "-o", obj, *common]
         if src.endswith(".cpp"):
             cmd = [nvcc, "-x", "cu", "-c", src, "-o", obj, *common]
@@ -81,12 +105,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             objs.append(obj)
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB + f".tmp{os.getpid()}"
+    # the temporary name keeps the .so suffix: nvcc picks the link step from it
+    tmp = os.path.join(OUT_DIR, f"libpagedkv.tmp{os.getpid()}.so")
     cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
     os.replace(tmp, LIB)
+    shutil.rmtree(obj_dir, ignore_errors=True)
     return LIB
 
 

@@ -841,8 +841,7 @@ pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, co
     return do_combine(batch, n_q_heads, head_dim, dtype, out, scratch, s, cs);
 }
 
-pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
-    if (!workspace || !status_out) return PKV_ERR_INVALID_ARG;
+static pkv_status read_status(const void* workspace, uint32_t* status_out) {
     WsHeader h;
     if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -853,6 +852,19 @@ pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
     for (int i = 0; i < n; ++i) v |= h.append_status[i];
     *status_out = v;
     return v ? PKV_ERR_DEVICE_CHECK : PKV_OK;
+}
+
+pkv_status pkv_read_device_status(const void* workspace, uint32_t* status_out) {
+    if (!workspace || !status_out) return PKV_ERR_INVALID_ARG;
+    return read_status(workspace, status_out);
+}
+
+pkv_status pkv_read_no_alloc_status(uint32_t* status_out) {
+    if (!status_out) return PKV_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const pkv_status st = no_alloc_scratch(&scratch);
+    if (st != PKV_OK) return st;
+    return read_status(scratch, status_out);
 }
 
 }  // extern "C"

@@ -12,6 +12,9 @@
 // node; a match hands the caller one more reference per matched page, so a
 // page stays allocated while any sequence or the cache uses it.  Eviction
 // removes least-recently-used leaves whose page only the cache still holds.
+// Counters of lookups, hits, misses and pages moved in and out are kept under
+// the same lock (CacheIR, "Current Capabilities": prefix-cache reuse with
+// hit/miss counters).
 #include <stdint.h>
 
 #include <algorithm>
@@ -102,6 +105,7 @@ struct pkv_prefix_cache {
     Node root;  // no token ids follow it: tokens() of the root is never read
     uint64_t clock = 0;
     int pages = 0;  // nodes below the root
+    pkv_prefix_cache_stats stats{};
 };
 
 namespace {
@@ -206,6 +210,7 @@ pkv_status pkv_prefix_cache_insert(pkv_prefix_cache* cache, const int32_t* token
         n = c;
     }
     cache->pages += full - i;
+    cache->stats.pages_inserted += (uint64_t)(full - i);
     if (n_new) *n_new = full - i;
     return PKV_OK;
 }
@@ -232,6 +237,13 @@ pkv_status pkv_prefix_cache_match(pkv_prefix_cache* cache, const int32_t* tokens
     const pkv_status st = kv_pool_retain_pages(cache->pool, pages_out, k);
     if (st != PKV_OK) return st;
     *n_pages = k;
+    // whole pages the lookup could have served (at most max_pages)
+    const long long asked = std::min<long long>(max_pages, n_tokens / P);
+    pkv_prefix_cache_stats& s = cache->stats;
+    ++s.lookups;
+    if (k > 0) ++s.hits; else ++s.misses;
+    s.pages_hit += (uint64_t)k;
+    s.pages_missed += (uint64_t)(asked - k);
     return PKV_OK;
 }
 
@@ -249,6 +261,7 @@ pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_f
         if (kv_pool_refcount(cache->pool, leaf->page) != 1) continue;  // retained meanwhile
         const pkv_status st = kv_pool_release_pages(cache->pool, &leaf->page, 1);
         if (st != PKV_OK) {
+            cache->stats.pages_evicted += (uint64_t)freed;
             if (n_freed) *n_freed = freed;
             return st;
         }
@@ -260,6 +273,7 @@ pkv_status pkv_prefix_cache_evict(pkv_prefix_cache* cache, int n_pages, int* n_f
             kv_pool_refcount(cache->pool, parent->page) == 1)
             heap.emplace(parent->last_use, parent);
     }
+    cache->stats.pages_evicted += (uint64_t)freed;
     if (n_freed) *n_freed = freed;
     return PKV_OK;
 }
@@ -268,6 +282,15 @@ int pkv_prefix_cache_pages(const pkv_prefix_cache* cache) {
     if (!cache) return -1;
     std::lock_guard<std::mutex> lk(const_cast<pkv_prefix_cache*>(cache)->mu);
     return cache->pages;
+}
+
+pkv_status pkv_prefix_cache_get_stats(pkv_prefix_cache* cache, int reset,
+                                      pkv_prefix_cache_stats* out) {
+    if (!cache || !out) return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(cache->mu);
+    *out = cache->stats;
+    if (reset) cache->stats = pkv_prefix_cache_stats{};
+    return PKV_OK;
 }
 
 }  // extern "C"

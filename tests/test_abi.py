@@ -263,3 +263,33 @@ def test_rope_entry_points_check_theta_on_host(lib):
         assert rope(batch=0, qw=A * 10, kw=A * 11, eps=1e-6) == OK
     finally:
         lib.kv_pool_destroy(h)
+
+
+def test_no_alloc_status_reader_rejects_null(lib):
+    assert lib.pkv_read_no_alloc_status(None) == INVALID
+
+
+class _FakeCudaTensor:
+    """Stands in for a contiguous CUDA tensor (no GPU needed for the binding's checks)."""
+
+    def __init__(self, index):
+        import torch
+        self.is_cuda = True
+        self.dtype = torch.bfloat16
+        self.device = torch.device("cuda", index)
+
+    def is_contiguous(self):
+        return True
+
+    def dim(self):
+        return 3
+
+
+def test_binding_rejects_operands_on_another_device(monkeypatch):
+    import torch
+    t = _FakeCudaTensor(1)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(ValueError, match="current device is cuda:0"):
+        pkv._dev(t, "q", torch.bfloat16, 3)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    assert pkv._dev(t, "q", torch.bfloat16, 3) is t

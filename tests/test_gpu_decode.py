@@ -9,18 +9,9 @@ import torch
 import oracle
 import paged_kv_decode_16_gb300 as pkv
 from paged_kv_decode_16_gb300 import workloads as wl
-from gpu_helpers import (VARIANT_IDS, VARIANTS, assert_close, errors, oracle_full, oracle_rows,
-                         run_gpu, to_dev)
+from gpu_helpers import VARIANT_IDS, VARIANTS, assert_close, oracle_full, run_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
-
-
-def _sample_rows(w, rng, n_random=48):
-    """All heads of the first, last and two middle sequences plus random rows."""
-    seqs = sorted({0, w.batch - 1, w.batch // 2, w.batch // 3})
-    rows = [(b, h) for b in seqs for h in range(w.n_q_heads)]
-    rows += [(int(rng.integers(w.batch)), int(rng.integers(w.n_q_heads))) for _ in range(n_random)]
-    return np.array(rows, dtype=np.int32)
 
 
 @pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
@@ -30,14 +21,10 @@ def test_named_workload_matches_oracle(name, variant):
     before = (wl.to_bits(w.k_pool), wl.to_bits(w.v_pool))
     out, ws, status = run_gpu(w, variant=variant)
     assert status == 0
-    got = out.float().cpu().numpy().astype(np.float64)
-    if name == "tiny":
-        ref = oracle_full(w, before)
-        assert_close(got, ref, strict=True, what=name)
-    else:
-        rows = _sample_rows(w, np.random.default_rng(1))
-        ref = oracle_rows(w, rows, before)
-        assert_close(got[rows[:, 0], rows[:, 1]], ref, strict=True, what=name)
+    # every output element against the oracle (under a second of oracle time
+    # per workload on the host cores)
+    ref = oracle_full(w, before)
+    assert_close(out, ref, strict=True, what=name)
     if w.append:
         # the append itself is bit-exact against the oracle's
         kp, vp = oracle.kv_append(*before, wl.to_bits(w.k_new), wl.to_bits(w.v_new),

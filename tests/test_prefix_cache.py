@@ -274,3 +274,54 @@ def test_numpy_token_arrays_match_lists(pool):
     release(lib, h, pages)
     release(lib, h, pages)
     c.destroy()
+
+
+def test_counters_match_a_model(pool):
+    """Hit/miss counters and page counts against the brute-force model."""
+    lib, h = pool
+    P = 16
+    rnd = random.Random(17)
+    c = pkv.PrefixCache(h)
+    model = {}
+    held = []
+    exp = dict.fromkeys(pkv.PREFIX_STATS_FIELDS, 0)
+    for _ in range(80):
+        toks = []
+        for _ in range(rnd.randint(0, 5)):
+            toks += [rnd.randint(0, 3)] * P
+        toks += [9] * rnd.randint(0, P - 1)
+        pages = alloc(lib, h, (len(toks) + P - 1) // P)
+        held.append(pages)
+        exp["pages_inserted"] += c.insert(toks, pages)
+        for k in range(1, len(toks) // P + 1):
+            model.setdefault(tuple(toks[:k * P]), pages[k - 1])
+        q = []
+        for _ in range(rnd.randint(0, 6)):
+            q += [rnd.randint(0, 3)] * P
+        q += [9] * rnd.randint(0, P - 1)
+        cap = rnd.choice([None, 0, 1, 3])
+        got = c.match(q, cap)
+        want = _model_match(model, q, P)[:cap]
+        assert got == want
+        asked = len(q) // P if cap is None else min(cap, len(q) // P)
+        exp["lookups"] += 1
+        exp["hits" if got else "misses"] += 1
+        exp["pages_hit"] += len(got)
+        exp["pages_missed"] += asked - len(got)
+        release(lib, h, got)
+    assert exp["pages_inserted"] == len(model)
+    assert c.stats() == exp
+    for pages in held:
+        release(lib, h, pages)
+    freed = c.evict(7)
+    assert freed == 7
+    exp["pages_evicted"] = 7
+    assert c.stats(reset=True) == exp
+    assert c.stats() == dict.fromkeys(pkv.PREFIX_STATS_FIELDS, 0)
+    c.destroy()
+
+
+def test_stats_rejects_null(pool):
+    lib, _ = pool
+    buf = (ctypes.c_uint64 * 7)()
+    assert lib.pkv_prefix_cache_get_stats(None, 0, buf) == 1
