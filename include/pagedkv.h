@@ -433,17 +433,22 @@ pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const in
  *
  * For a batch whose rows all begin with the same prefix_tokens tokens stored
  * in the same pages (columns 0 .. prefix_tokens/P - 1 of every table row equal
- * to row 0's), the prefix is attended once per KV head for all B*G query rows
- * (tensor-core tiles of up to 16 rows read each prefix chunk once), each
- * sequence's own tokens are attended as usual, and the two partial states of
- * every (sequence, head) are merged: out equals paged_decode_attention's
- * within the decode tolerance.  prefix_tokens > 0, a multiple of page_size, at
- * most table_stride * page_size (INVALID_ARG); every context_lens[b] >=
- * prefix_tokens (else PKV_DEV_BAD_LEN); rows that do not start with row 0's
- * prefix pages set PKV_DEV_BAD_PREFIX (their results are then wrong).  Both
- * read through pkv_read_device_status(workspace).  Four launches: one holding
- * both plans, the query gather and the prefix check; the two decodes; the
- * merge.
+ * to row 0's), the prefix is attended once per KV head for all B*G query rows,
+ * each sequence's own tokens are attended as usual, and the two partial states
+ * of every (sequence, head) are merged: out equals paged_decode_attention's
+ * within the decode tolerance.  The prefix pass runs on 128-row tiles of the
+ * fifth-generation tensor cores (tcgen05, accumulators in tensor memory; each
+ * prefix chunk is read once per tile) for the tensor-core variant (AUTO), and
+ * as a decode of 8-row virtual units on CUDA cores for the CUDA-core variant.
+ * prefix_tokens > 0, a multiple of page_size, at most table_stride *
+ * page_size (INVALID_ARG); every context_lens[b] >= prefix_tokens (else
+ * PKV_DEV_BAD_LEN); rows that do not start with row 0's prefix pages set
+ * PKV_DEV_BAD_PREFIX (their results are then wrong).  Both read through
+ * pkv_read_device_status(workspace).  Four launches: one holding the plans,
+ * the query gather and the prefix check; the prefix pass; the suffix decode;
+ * the merge.  The workspace size depends on the device's SM count (the
+ * prefix pass is split into one wave of tiles): query it on the device that
+ * decodes.
  * ------------------------------------------------------------------------ */
 pkv_status paged_decode_prefix_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                                               int head_dim, int num_workers,

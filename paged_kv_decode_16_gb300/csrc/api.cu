@@ -253,11 +253,13 @@ EncodeTiledFn encode_fn() {
 }
 
 std::mutex g_map_mu;
-std::map<std::tuple<const void*, long long, int, int>, CUtensorMap> g_maps;
+std::map<std::tuple<const void*, long long, int, int, int>, CUtensorMap> g_maps;
 
+// box_rows: rows of one box (16: a chunk of the pool; 128: a tensor-core row
+// tile of gathered query rows)
 pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dtype,
-                    CUtensorMap* out) {
-    const auto key = std::make_tuple(pool, rows, head_dim, (int)dtype);
+                    CUtensorMap* out, int box_rows = pkv::kChunk) {
+    const auto key = std::make_tuple(pool, rows, head_dim, (int)dtype, box_rows);
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
         auto it = g_maps.find(key);
@@ -272,7 +274,7 @@ pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dt
     memset(&m, 0, sizeof(m));
     const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)pkv::kChunk};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -873,37 +875,78 @@ pkv_status pkv_read_no_alloc_status(uint32_t* status_out) {
 namespace {
 struct PrefixSetup {
     DecodeSetup real, virt;  // suffix pass (real units), prefix pass (virtual units)
+    // prefix pass on tensor-core row tiles (tensor-core variant): tiles of
+    // tile_rows rows per KV head, up to max_splits ranges of the prefix each
+    bool umma = false;
+    int tile_rows = 0, tiles = 0, max_splits = 0;
     size_t qv_off, v_off, s_off, total;
 };
 
+constexpr int kMaxPrefixSplits = 64;
+
+// Ranges of the prefix per (KV head, row tile): enough tensor-core CTAs for
+// one wave over the GPU (dtype < 0: the larger of the two dtypes' counts,
+// for sizing a workspace before the dtype is known).
+pkv_status prefix_splits(int head_dim, int dtype, long long tiles_total, int* splits) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    int per_sm = 0;
+    for (int dt = 0; dt < 2; ++dt)
+        if (dtype < 0 || dtype == dt) {
+            const int n = pkv::prefix_umma_ctas_per_sm((pkv_dtype)dt, head_dim);
+            per_sm = n > per_sm ? n : per_sm;
+        }
+    if (per_sm <= 0) return PKV_ERR_CUDA;
+    const long long s = (long long)sms * per_sm / (tiles_total > 0 ? tiles_total : 1);
+    *splits = (int)(s < 1 ? 1 : (s > kMaxPrefixSplits ? kMaxPrefixSplits : s));
+    return PKV_OK;
+}
+
 // The prefix pass: one sequence (the shared prefix) whose every KV head serves
-// all B*G query rows of that head, in sub-groups of gs_v rows, gs_v a multiple
-// of the real sub-group size so that every real unit lies in one virtual unit.
+// all B*G query rows of that head.  Tensor-core variant: row tiles of up to
+// 128 rows (a multiple of the real sub-group size, so that every real unit
+// lies in one tile) on the fifth-generation tensor cores.  CUDA-core variant:
+// a virtual decode in sub-groups of gs_v rows, gs_v a multiple of the real
+// sub-group size.  dtype < 0: size for either dtype.
 pkv_status setup_prefix(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
-                        pkv_dtype dtype, int num_workers, int variant, PrefixSetup* ps) {
-    pkv_status st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype,
-                                 num_workers, variant, &ps->real);
+                        int dtype, int num_workers, int variant, PrefixSetup* ps) {
+    pkv_status st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                                 dtype < 0 ? PKV_BF16 : (pkv_dtype)dtype, num_workers, variant,
+                                 &ps->real);
     if (st != PKV_OK) return st;
-    // virtual units of up to one m16 tile (16 rows) on tensor cores, 8 on CUDA
-    // cores (32-row units, two tiles per warp, measured slower here: the pass
-    // is not limited by its L2 re-reads of the prefix)
-    const int max_gs = resolve_variant(variant) == PKV_VARIANT_TENSOR_CORES ? 16 : 8;
     const long long group_v = (long long)batch * ps->real.group;
     if (group_v * n_kv_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
-    int gs_v = ps->real.gs;
-    for (int k = max_gs / ps->real.gs; k >= 1; --k)
-        if (group_v % (k * ps->real.gs) == 0) {
-            gs_v = k * ps->real.gs;
-            break;
-        }
-    if ((st = setup_decode(1, (int)(group_v * n_kv_heads), n_kv_heads, head_dim, page_size, dtype,
-                           num_workers, variant, &ps->virt, gs_v)) != PKV_OK)
-        return st;
+    size_t prefix_bytes = 0;
+    if (resolve_variant(variant) == PKV_VARIANT_TENSOR_CORES) {
+        ps->umma = true;
+        ps->tile_rows = (pkv::kPrefixTileRows / ps->real.gs) * ps->real.gs;
+        ps->tiles = (int)((group_v + ps->tile_rows - 1) / ps->tile_rows);
+        if ((st = prefix_splits(head_dim, dtype, (long long)ps->tiles * n_kv_heads,
+                                &ps->max_splits)) != PKV_OK)
+            return st;
+        prefix_bytes = (size_t)n_kv_heads * ps->tiles * ps->max_splits *
+                       (size_t)(pkv::kPrefixTileRows * (head_dim + 2)) * 4;
+    } else {
+        const int max_gs = 8;  // virtual units of up to 8 rows on CUDA cores
+        int gs_v = ps->real.gs;
+        for (int k = max_gs / ps->real.gs; k >= 1; --k)
+            if (group_v % (k * ps->real.gs) == 0) {
+                gs_v = k * ps->real.gs;
+                break;
+            }
+        if ((st = setup_decode(1, (int)(group_v * n_kv_heads), n_kv_heads, head_dim, page_size,
+                               dtype < 0 ? PKV_BF16 : (pkv_dtype)dtype, num_workers, variant,
+                               &ps->virt, gs_v)) != PKV_OK)
+            return st;
+        prefix_bytes = ps->virt.ws.total;
+    }
     // the suffix pass's workspace first: its header is the call's status word
     const size_t qv_bytes = align256((size_t)batch * n_q_heads * head_dim * 2);
     ps->s_off = 0;
     ps->v_off = align256(ps->real.ws.total);
-    ps->qv_off = ps->v_off + align256(ps->virt.ws.total);
+    ps->qv_off = ps->v_off + align256(prefix_bytes);
     ps->total = ps->qv_off + qv_bytes;
     return PKV_OK;
 }
@@ -920,8 +963,8 @@ pkv_status paged_decode_prefix_workspace_size(int batch, int n_q_heads, int n_kv
         return PKV_OK;
     }
     PrefixSetup ps;
-    pkv_status st = setup_prefix(batch, n_q_heads, n_kv_heads, head_dim, 16, PKV_BF16,
-                                 num_workers, variant, &ps);
+    pkv_status st = setup_prefix(batch, n_q_heads, n_kv_heads, head_dim, 16, -1, num_workers,
+                                 variant, &ps);
     if (st != PKV_OK) return st;
     *bytes = ps.total;
     return PKV_OK;
@@ -955,12 +998,14 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int skip = prefix_tokens / page_size;
     const int hq_v = (int)((long long)batch * ps.real.group * n_kv_heads);
-    // one launch: the plans of the suffixes (each row from column skip on,
-    // lengths minus prefix_tokens) and of the prefix (one sequence of
-    // prefix_tokens read through row 0), the gather of the query rows per KV
-    // head, and the check that every row starts with row 0's prefix pages
+    // one launch: the plan of the suffixes (each row from column skip on,
+    // lengths minus prefix_tokens), on CUDA cores the plan of the prefix's
+    // virtual decode (one sequence of prefix_tokens read through row 0), the
+    // gather of the query rows per KV head, and the check that every row starts
+    // with row 0's prefix pages
     const pkv::PlanArgs pv = plan_args(nullptr, page_table, 1, page_size, table_stride,
-                                       num_workers, ws_v, ps.virt, 0, prefix_tokens);
+                                       num_workers, ws_v, ps.umma ? ps.real : ps.virt, 0,
+                                       prefix_tokens);
     const pkv::PlanArgs pss = plan_args(context_lens, page_table + skip, batch, page_size,
                                         table_stride, num_workers, ws_s, ps.real, skip);
     pkv::CascadeGather g;
@@ -973,34 +1018,73 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
     g.table = page_table;
     g.table_stride = table_stride;
     g.share_cols = skip;
-    if ((st = cuda_status(pkv::launch_cascade_plan(pss, pv, g, cs))) != PKV_OK) return st;
+    g.plan_virtual = ps.umma ? 0 : 1;
     uint32_t* call_status = &reinterpret_cast<WsHeader*>(ws_s)->status;
-    if ((st = do_run(qv, k_pool, v_pool, page_table, table_stride, 1, hq_v, n_kv_heads, head_dim,
-                     page_size, num_pages, dtype, scale, out, ws_v, ps.virt, false, cs, true,
-                     call_status)) != PKV_OK)
-        return st;
+    uint8_t* wv = static_cast<uint8_t*>(ws_v);
+    pkv::CascadeArgs c;
+    int splits = 0;
+    if (ps.umma) {
+        // the tensor maps first: nothing is launched if one cannot be made
+        const long long pool_rows = (long long)num_pages * n_kv_heads * page_size;
+        if (pool_rows > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // 32-bit row coordinate
+        CUtensorMap qm, km, vm;
+        if ((st = pool_map(qv, (long long)hq_v, head_dim, dtype, &qm, pkv::kPrefixTileRows)) !=
+                PKV_OK ||
+            (st = pool_map(k_pool, pool_rows, head_dim, dtype, &km)) != PKV_OK ||
+            (st = pool_map(v_pool, pool_rows, head_dim, dtype, &vm)) != PKV_OK)
+            return st;
+        const int chunks = prefix_tokens / pkv::kChunk;
+        splits = ps.max_splits < chunks ? ps.max_splits : chunks;
+        if ((st = cuda_status(pkv::launch_cascade_plan(pss, pv, g, cs))) != PKV_OK) return st;
+        pkv::PrefixUmmaArgs pa;
+        pa.table = page_table;
+        pa.num_pages = num_pages;
+        pa.n_kv_heads = n_kv_heads;
+        pa.page_size = page_size;
+        pa.chunks = chunks;
+        pa.splits = splits;
+        pa.rows = (int)((long long)batch * ps.real.group);
+        pa.tile_rows = ps.tile_rows;
+        pa.tiles = ps.tiles;
+        pa.scale_log2 = scale * 1.4426950408889634f;
+        pa.partials = reinterpret_cast<float*>(wv);
+        pa.status = call_status;
+        if ((st = cuda_status(pkv::launch_prefix_umma(dtype, head_dim, pa, qm, km, vm, cs))) !=
+            PKV_OK)
+            return st;
+        c.v_partials = pa.partials;
+        c.v_hdr = nullptr;
+    } else {
+        if ((st = cuda_status(pkv::launch_cascade_plan(pss, pv, g, cs))) != PKV_OK) return st;
+        if ((st = do_run(qv, k_pool, v_pool, page_table, table_stride, 1, hq_v, n_kv_heads,
+                         head_dim, page_size, num_pages, dtype, scale, out, ws_v, ps.virt, false,
+                         cs, true, call_status)) != PKV_OK)
+            return st;
+        c.v_partials = reinterpret_cast<const float*>(wv + ps.virt.ws.partials);
+        c.v_hdr = reinterpret_cast<const WsHeader*>(wv);
+    }
     if ((st = do_run(q, k_pool, v_pool, page_table + skip, table_stride, batch, n_q_heads,
                      n_kv_heads, head_dim, page_size, num_pages, dtype, scale, out, ws_s, ps.real,
                      false, cs, true)) != PKV_OK)
         return st;
-    uint8_t* wv = static_cast<uint8_t*>(ws_v);
     uint8_t* wsu = static_cast<uint8_t*>(ws_s);
-    pkv::CascadeArgs c;
     c.s_partials = reinterpret_cast<const float*>(wsu + ps.real.ws.partials);
     c.s_prefix = reinterpret_cast<const int32_t*>(wsu + ps.real.ws.prefix);
     c.s_lens = reinterpret_cast<const int32_t*>(wsu + ps.real.ws.lens_eff);
     c.s_hdr = reinterpret_cast<const WsHeader*>(wsu);
-    c.v_partials = reinterpret_cast<const float*>(wv + ps.virt.ws.partials);
-    c.v_hdr = reinterpret_cast<const WsHeader*>(wv);
     c.out = out;
     c.units_per_b = ps.real.units_per_b;
     c.sub_groups = ps.real.sub_groups;
     c.gs = ps.real.gs;
     c.group = ps.real.group;
     c.n_q_heads = n_q_heads;
-    c.v_gs = ps.virt.gs;
-    c.v_sub = ps.virt.sub_groups;
+    c.v_gs = ps.umma ? 0 : ps.virt.gs;
+    c.v_sub = ps.umma ? 0 : ps.virt.sub_groups;
     c.v_nch = (prefix_tokens + 15) / 16;
+    c.umma = ps.umma ? 1 : 0;
+    c.v_tile_rows = ps.tile_rows;
+    c.v_tiles = ps.tiles;
+    c.v_splits = splits;
     return cuda_status(pkv::launch_cascade_combine(dtype, head_dim, c, (int)ps.real.units, cs));
 }
 

@@ -137,6 +137,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// 2-D tensor copy (cp.async.bulk.tensor) of one box at element coordinates
+// (x, y) of `map` into shared memory, completing on `bar`.  x times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2^x with the hardware approximation (flushes subnormal results to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start while the previous kernel in the
 // stream still runs; pdl_wait() blocks until that kernel has completed and its
@@ -189,6 +208,15 @@ struct Cvt<__half> {
         return *reinterpret_cast<uint32_t*>(&h);
     }
 };
+
+// P in two bf16 pieces: hi = bf16(p), lo = bf16(p - hi).  bf16 keeps 8
+// significant bits, too few for P (an output that cancels would carry ~2^-9
+// relative error); hi + lo carries ~16.  fp16 P (11 bits) is used as is.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = Cvt<__nv_bfloat16>::pack2(a, b);
+    const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xffff0000u);
+    lo = Cvt<__nv_bfloat16>::pack2(a - ha, b - hb);
+}
 
 __host__ __device__ constexpr int next_pow2(int x) {
     return x <= 1 ? 1 : (x <= 2 ? 2 : (x <= 4 ? 4 : (x <= 8 ? 8 : 16)));

@@ -40,12 +40,6 @@
 
 namespace pkv {
 
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Reduce-scatter of a[GP] across the lanes that share a token (lane bits
 // below LPT).  Level with mask M halves the live values; the lane with bit M
 // set keeps the upper half.  Returns the complete sum of value index

@@ -41,15 +41,6 @@
 
 namespace pkv {
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -88,15 +79,6 @@ struct Mma<__half> {
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
 };
-
-// P in two bf16 pieces: hi = bf16(p), lo = bf16(p - hi).  bf16 keeps 8
-// significant bits, too few for P (an output that cancels would carry ~2^-9
-// relative error); hi + lo carries ~16.  fp16 P (11 bits) is used as is.
-__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-    hi = Cvt<__nv_bfloat16>::pack2(a, b);
-    const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xffff0000u);
-    lo = Cvt<__nv_bfloat16>::pack2(a - ha, b - hb);
-}
 
 // Byte offset of (row r, 16-byte column j) inside one [16 x 128 B] box written
 // by a 128-byte-swizzled tensor copy into a 1024-byte aligned buffer.

@@ -395,7 +395,7 @@ cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
         return;
     }
     if (blockIdx.x == 1) {
-        plan_cta(pv, 0);
+        if (g.plan_virtual) plan_cta(pv, 0);
         return;
     }
     const int c = blockIdx.x - 2;
@@ -461,19 +461,21 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
 
 // ---------------------------------------------------------------------------
 // Cascade combine (shared-prefix decode).  The prefix pass ran the shared
-// prefix once per KV head for all B*G query rows (virtual units of gs_v rows,
-// rows in b-major, head-minor order); the suffix pass ran each sequence's own
-// tokens.  Both left only partial states.  One CTA per real unit (sequence,
-// KV head, sub-group of gs rows): its rows sit at rows ro .. ro+gs-1 of one
-// virtual unit (gs divides gs_v).  The prefix segments, then the suffix
-// segments, are merged as one list with merge_rows.
+// prefix once per KV head for all B*G query rows (rows in b-major, head-minor
+// order): as 128-row tensor-core tiles split over ranges of the prefix
+// (prefix_umma.cu), or as a virtual decode of gs_v-row units; the suffix pass
+// ran each sequence's own tokens.  Both left only partial states.  One CTA per
+// real unit (sequence, KV head, sub-group of gs rows): its rows sit at rows
+// ro .. ro+gs-1 of one tile or virtual unit (gs divides both).  The prefix
+// segments, then the suffix segments, are merged as one list with merge_rows.
 // ---------------------------------------------------------------------------
+template <class Pre>
 struct CascadeSegs {
-    SlotSegs pre;  // the virtual unit's segments (rows offset by ro)
+    Pre pre;  // the prefix pass's segments (rows offset by ro)
     int ro, np;
     SlotSegs suf;  // the unit's own segments
-    __device__ __forceinline__ const float* o(int s, int g) const {
-        return s < np ? pre.o(s, ro + g) : suf.o(s - np, g);
+    __device__ __forceinline__ const float4* o4(int s, int g, int v) const {
+        return s < np ? pre.o4(s, ro + g, v) : suf.o4(s - np, g, v);
     }
     __device__ __forceinline__ const float* m(int s, int g) const {
         return s < np ? pre.m(s, ro + g) : suf.m(s - np, g);
@@ -483,7 +485,9 @@ struct CascadeSegs {
     }
 };
 
-template <typename T, int D>
+// kUmma: the prefix pass ran on the tensor-core row tiles (prefix_umma.cu);
+// else as a virtual decode of gs_v-row units.
+template <typename T, int D, bool kUmma>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 cascade_combine_kernel(CascadeArgs c) {
     const int u = blockIdx.x;
@@ -493,12 +497,6 @@ cascade_combine_kernel(CascadeArgs c) {
     const int sgi = uidx - h * c.sub_groups;
     const int gs = c.gs;
     T* o = static_cast<T*>(c.out) + ((long long)b * c.n_q_heads + h * c.group + sgi * gs) * D;
-    // the prefix side: the virtual unit holding this unit's rows
-    const int r0 = b * c.group + sgi * gs;             // row among head h's B*G rows
-    const int vu = h * c.v_sub + r0 / c.v_gs, ro = r0 % c.v_gs;
-    const UnitSegments pv = unit_segments(c.v_hdr->chunks_per_worker, c.v_hdr->extra_chunks, vu,
-                                          vu * c.v_nch, c.v_nch);
-    const int np = c.v_nch > 0 && c.v_hdr->num_workers > 0 ? pv.count() : 0;
     // the suffix side: this unit's own segments
     const int L = c.s_lens[b];
     const int nch = (L + kChunk - 1) / kChunk;
@@ -507,21 +505,42 @@ cascade_combine_kernel(CascadeArgs c) {
         sv = unit_segments(c.s_hdr->chunks_per_worker, c.s_hdr->extra_chunks, u,
                            c.s_prefix[b] + uidx * nch, nch);
     const int ns = sv.count();
-    pdl_wait();  // the partial states of both passes are complete from here on
-    pdl_trigger();
-    const CascadeSegs sg{SlotSegs{c.v_partials, pv.base, partial_slot_floats(c.v_gs, D), c.v_gs, D},
-                         ro, np,
-                         SlotSegs{c.s_partials, sv.base, partial_slot_floats(gs, D), gs, D}};
-    merge_rows<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
-                     [&](int g) { return o + (long long)g * D; });
+    const SlotSegs suf{c.s_partials, sv.base, partial_slot_floats(gs, D), gs, D};
+    // the prefix side: the rows of this unit among head h's B*G rows
+    const int r0 = b * c.group + sgi * gs;
+    if constexpr (kUmma) {
+        const int t = r0 / c.v_tile_rows, ro = r0 - t * c.v_tile_rows;
+        pdl_wait();  // the partial states of both passes are complete from here on
+        pdl_trigger();
+        const CascadeSegs<TileSegs> sg{
+            TileSegs{c.v_partials, (long long)(h * c.v_tiles + t) * c.v_splits, D}, ro,
+            c.v_splits, suf};
+        merge_rows<T, D>(sg, c.v_splits + ns, gs, threadIdx.x >> 5, kCombineWarps,
+                         threadIdx.x & 31, [&](int g) { return o + (long long)g * D; });
+    } else {
+        // the virtual unit holding this unit's rows
+        const int vu = h * c.v_sub + r0 / c.v_gs, ro = r0 % c.v_gs;
+        const UnitSegments pv = unit_segments(c.v_hdr->chunks_per_worker,
+                                              c.v_hdr->extra_chunks, vu, vu * c.v_nch, c.v_nch);
+        const int np = c.v_nch > 0 && c.v_hdr->num_workers > 0 ? pv.count() : 0;
+        pdl_wait();  // the partial states of both passes are complete from here on
+        pdl_trigger();
+        const CascadeSegs<SlotSegs> sg{
+            SlotSegs{c.v_partials, pv.base, partial_slot_floats(c.v_gs, D), c.v_gs, D}, ro, np,
+            suf};
+        merge_rows<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+                         [&](int g) { return o + (long long)g * D; });
+    }
 }
 
 cudaError_t launch_cascade_combine(pkv_dtype dtype, int head_dim, const CascadeArgs& c,
                                    int units, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
-#define PKV_CASCADE(T, D) \
-    return launch_pdl(cascade_combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32), 0, \
-                      stream, c)
+#define PKV_CASCADE(T, D)                                                                  \
+    return c.umma ? launch_pdl(cascade_combine_kernel<T, D, true>, dim3(units),             \
+                               dim3(kCombineWarps * 32), 0, stream, c)                      \
+                  : launch_pdl(cascade_combine_kernel<T, D, false>, dim3(units),            \
+                               dim3(kCombineWarps * 32), 0, stream, c)
     if (dtype == PKV_BF16) {
         if (head_dim == 128) PKV_CASCADE(__nv_bfloat16, 128);
         PKV_CASCADE(__nv_bfloat16, 64);

@@ -84,7 +84,40 @@ struct CascadeArgs {
     void* out;
     int units_per_b, sub_groups, gs, group, n_q_heads;  // real units
     int v_gs, v_sub, v_nch;                              // virtual units per KV head, chunks
+    // prefix pass on the tensor-core tiles (prefix_umma.cu) instead: v_partials
+    // holds its slots, v_tiles tiles of v_tile_rows rows per KV head, v_splits
+    // slots per tile
+    int umma, v_tile_rows, v_tiles, v_splits;
 };
+
+// Shared-prefix pass on the fifth-generation tensor cores (prefix_umma.cu):
+// grid (splits, tiles, n_kv_heads); CTA (s, t, h) attends query rows
+// [t * tile_rows, t * tile_rows + 128) of KV head h (rows of qv, [Hkv][rows][D])
+// over its balanced range of the prefix's chunks and writes one partial
+// state: o as 8-float groups (element (r, d) at ((d / 8) * 128 + r) * 8 +
+// d % 8), then m [128], then l [128] -- 128 * D + 256 floats per slot, slot
+// (h * tiles + t) * splits + s.
+struct PrefixUmmaArgs {
+    const int32_t* table;  // the prefix's page ids (row 0 of the page table)
+    int num_pages, n_kv_heads, page_size;
+    int chunks;            // 16-token chunks of the prefix
+    int splits;            // ranges of chunks per (KV head, tile), 1 .. chunks
+    int rows;              // query rows per KV head (B * G)
+    int tile_rows;         // rows of a tile that belong to it (<= 128)
+    int tiles;             // tiles per KV head
+    float scale_log2;      // scale * log2(e)
+    float* partials;
+    uint32_t* status;
+};
+
+constexpr int kPrefixTileRows = 128;  // rows of one tensor-core tile (and of a partial slot)
+
+cudaError_t launch_prefix_umma(pkv_dtype dtype, int head_dim, const PrefixUmmaArgs& a,
+                               const CUtensorMap& qmap, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t stream);
+
+// CTAs of the prefix kernel that fit on one SM (0 on an error).
+int prefix_umma_ctas_per_sm(pkv_dtype dtype, int head_dim);
 
 // The query gather and prefix check of the shared-prefix decode's plan launch.
 struct CascadeGather {
@@ -93,6 +126,7 @@ struct CascadeGather {
     int batch, n_kv_heads, group, vecs;
     const int32_t* table;  // rows 1 .. B-1 must start with row 0's first share_cols ids
     int table_stride, share_cols;
+    int plan_virtual;      // nonzero: CTA 1 plans the prefix pass's virtual decode
 };
 
 // One launch: the suffix pass's plan (ps, whose header receives the check's

@@ -52,6 +52,28 @@ struct SlotSegs {
         return partials + (base + s) * stride + (long long)gs * d + g;
     }
     __device__ __forceinline__ const float* l(int s, int g) const { return m(s, g) + gs; }
+    // output vector v (floats 4v .. 4v+3) of row g
+    __device__ __forceinline__ const float4* o4(int s, int g, int v) const {
+        return reinterpret_cast<const float4*>(o(s, g)) + v;
+    }
+};
+
+// Segment s of a shared-prefix row tile (prefix_umma.cu): slots base, base + 1,
+// ... of kPrefixTileRows rows, o stored as 8-float groups (element (g, d) at
+// ((d / 8) * rows + g) * 8 + d % 8), then m [rows], then l [rows].
+struct TileSegs {
+    static constexpr int kRows = 128;
+    const float* partials;
+    long long base;
+    int d;
+    __device__ __forceinline__ const float* slot(int s) const {
+        return partials + (base + s) * (long long)(kRows * d + 2 * kRows);
+    }
+    __device__ __forceinline__ const float4* o4(int s, int g, int v) const {
+        return reinterpret_cast<const float4*>(slot(s) + ((v >> 1) * kRows + g) * 8) + (v & 1);
+    }
+    __device__ __forceinline__ const float* m(int s, int g) const { return slot(s) + kRows * d + g; }
+    __device__ __forceinline__ const float* l(int s, int g) const { return m(s, g) + kRows; }
 };
 
 constexpr int kMergeBlock = 8;  // segments whose loads are in flight together
@@ -124,7 +146,7 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
             for (int j = 0; j < kMergeBlock; ++j) {
                 const int s = s0 + j;
                 v[j] = act && s < ns
-                           ? __ldcg(reinterpret_cast<const float4*>(sg.o(s, g)) + lane)
+                           ? __ldcg(sg.o4(s, g, lane))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
                 w[j] = s >= ns ? 0.f
                        : ns <= 32 ? __shfl_sync(kFull, mr.w, s & 31)
@@ -194,7 +216,7 @@ __device__ __forceinline__ void merge_rows_warp(const Segs& sg, int ns, int nrow
                 for (int j = 0; j < kWarpBlock; ++j) {
                     const int s = s0 + j;
                     v[r][j] = act && s < ns && g0 + r < nrows
-                                  ? __ldcg(reinterpret_cast<const float4*>(sg.o(s, g0 + r)) + lane)
+                                  ? __ldcg(sg.o4(s, g0 + r, lane))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
