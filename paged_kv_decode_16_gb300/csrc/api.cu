@@ -289,6 +289,80 @@ pkv_status pool_map(const void* pool, long long rows, int head_dim, pkv_dtype dt
     return PKV_OK;
 }
 
+// q [B][Hq][D] as a 3-D tensor (D, Hq, B) whose box is 64 elements x `group`
+// heads x tile_rows / group sequences: the rows of one shared-prefix tile of
+// a KV head in sequence-major order (128-byte swizzle).  Cached like the
+// pool maps.
+std::map<std::tuple<const void*, int, int, int, int, int, int>, CUtensorMap> g_qmaps;
+
+pkv_status q_tile_map(const void* q, int batch, int n_q_heads, int head_dim, pkv_dtype dtype,
+                      int group, int tile_rows, CUtensorMap* out) {
+    const auto key = std::make_tuple(q, batch, n_q_heads, head_dim, (int)dtype, group, tile_rows);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_qmaps.find(key);
+        if (it != g_qmaps.end()) {
+            *out = it->second;
+            return PKV_OK;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    CUtensorMap m;
+    memset(&m, 0, sizeof(m));
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_q_heads, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_q_heads * head_dim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(tile_rows / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (fn(&m, dt, 3, const_cast<void*>(q), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_qmaps.size() > 256) g_qmaps.clear();
+    g_qmaps[key] = m;
+    *out = m;
+    return PKV_OK;
+}
+
+// The shared-prefix pass's partial slots (128 * D + 256 floats each; o is the
+// first 128 * D) as a 3-D fp32 tensor (D, 128 rows, slots) with boxes of 32
+// floats x 128 rows x 1 slot (128-byte swizzle), for the pass's tensor stores.
+std::map<std::tuple<const void*, int, long long>, CUtensorMap> g_omaps;
+
+pkv_status prefix_slots_map(void* partials, int head_dim, long long slots, CUtensorMap* out) {
+    const auto key = std::make_tuple((const void*)partials, head_dim, slots);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_omaps.find(key);
+        if (it != g_omaps.end()) {
+            *out = it->second;
+            return PKV_OK;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    CUtensorMap m;
+    memset(&m, 0, sizeof(m));
+    const int rows = pkv::kPrefixTileRows;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)rows, (cuuint64_t)slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 4,
+                                   (cuuint64_t)(rows * (head_dim + 2)) * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, partials, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_omaps.size() > 256) g_omaps.clear();
+    g_omaps[key] = m;
+    *out = m;
+    return PKV_OK;
+}
+
 // The plan inputs of one decode.  skip_cols: the decoded range starts
 // skip_cols table columns into each row (table points at that column) and the
 // lengths count from the row's start; uniform_len >= 0: every sequence has
@@ -905,11 +979,10 @@ pkv_status prefix_splits(int head_dim, int dtype, long long tiles_total, int* sp
 }
 
 // The prefix pass: one sequence (the shared prefix) whose every KV head serves
-// all B*G query rows of that head.  Tensor-core variant: row tiles of up to
-// 128 rows (a multiple of the real sub-group size, so that every real unit
-// lies in one tile) on the fifth-generation tensor cores.  CUDA-core variant:
-// a virtual decode in sub-groups of gs_v rows, gs_v a multiple of the real
-// sub-group size.  dtype < 0: size for either dtype.
+// all B*G query rows of that head.  Tensor-core variant (G <= 128): row tiles
+// of up to 128 rows, whole sequences each, on the fifth-generation tensor
+// cores.  Otherwise a virtual decode in sub-groups of gs_v rows, gs_v a
+// multiple of the real sub-group size.  dtype < 0: size for either dtype.
 pkv_status setup_prefix(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                         int dtype, int num_workers, int variant, PrefixSetup* ps) {
     pkv_status st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size,
@@ -919,9 +992,12 @@ pkv_status setup_prefix(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
     const long long group_v = (long long)batch * ps->real.group;
     if (group_v * n_kv_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
     size_t prefix_bytes = 0;
-    if (resolve_variant(variant) == PKV_VARIANT_TENSOR_CORES) {
+    if (resolve_variant(variant) == PKV_VARIANT_TENSOR_CORES &&
+        ps->real.group <= pkv::kPrefixTileRows) {
+        // a tile holds whole sequences (all G rows of each), so every real unit
+        // lies in one tile and Q comes as one box of G heads x sequences
         ps->umma = true;
-        ps->tile_rows = (pkv::kPrefixTileRows / ps->real.gs) * ps->real.gs;
+        ps->tile_rows = (pkv::kPrefixTileRows / ps->real.group) * ps->real.group;
         ps->tiles = (int)((group_v + ps->tile_rows - 1) / ps->tile_rows);
         if ((st = prefix_splits(head_dim, dtype, (long long)ps->tiles * n_kv_heads,
                                 &ps->max_splits)) != PKV_OK)
@@ -942,8 +1018,9 @@ pkv_status setup_prefix(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
             return st;
         prefix_bytes = ps->virt.ws.total;
     }
-    // the suffix pass's workspace first: its header is the call's status word
-    const size_t qv_bytes = align256((size_t)batch * n_q_heads * head_dim * 2);
+    // the suffix pass's workspace first: its header is the call's status word;
+    // the gathered query rows last (CUDA-core variant only)
+    const size_t qv_bytes = ps->umma ? 0 : align256((size_t)batch * n_q_heads * head_dim * 2);
     ps->s_off = 0;
     ps->v_off = align256(ps->real.ws.total);
     ps->qv_off = ps->v_off + align256(prefix_bytes);
@@ -1010,7 +1087,7 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
                                         table_stride, num_workers, ws_s, ps.real, skip);
     pkv::CascadeGather g;
     g.q = static_cast<const uint4*>(q);
-    g.qv = static_cast<uint4*>(qv);
+    g.qv = ps.umma ? nullptr : static_cast<uint4*>(qv);
     g.batch = batch;
     g.n_kv_heads = n_kv_heads;
     g.group = ps.real.group;
@@ -1027,9 +1104,11 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
         // the tensor maps first: nothing is launched if one cannot be made
         const long long pool_rows = (long long)num_pages * n_kv_heads * page_size;
         if (pool_rows > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // 32-bit row coordinate
-        CUtensorMap qm, km, vm;
-        if ((st = pool_map(qv, (long long)hq_v, head_dim, dtype, &qm, pkv::kPrefixTileRows)) !=
-                PKV_OK ||
+        CUtensorMap qm, km, vm, om;
+        const long long slots = (long long)n_kv_heads * ps.tiles * ps.max_splits;
+        if ((st = q_tile_map(q, batch, n_q_heads, head_dim, dtype, ps.real.group, ps.tile_rows,
+                             &qm)) != PKV_OK ||
+            (st = prefix_slots_map(wv, head_dim, slots, &om)) != PKV_OK ||
             (st = pool_map(k_pool, pool_rows, head_dim, dtype, &km)) != PKV_OK ||
             (st = pool_map(v_pool, pool_rows, head_dim, dtype, &vm)) != PKV_OK)
             return st;
@@ -1044,13 +1123,14 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
         pa.chunks = chunks;
         pa.splits = splits;
         pa.rows = (int)((long long)batch * ps.real.group);
+        pa.group = ps.real.group;
         pa.tile_rows = ps.tile_rows;
         pa.tiles = ps.tiles;
         pa.scale_log2 = scale * 1.4426950408889634f;
         pa.partials = reinterpret_cast<float*>(wv);
         pa.status = call_status;
-        if ((st = cuda_status(pkv::launch_prefix_umma(dtype, head_dim, pa, qm, km, vm, cs))) !=
-            PKV_OK)
+        if ((st = cuda_status(pkv::launch_prefix_umma(dtype, head_dim, pa, qm, km, vm, om,
+                                                      cs))) != PKV_OK)
             return st;
         c.v_partials = pa.partials;
         c.v_hdr = nullptr;

@@ -382,10 +382,11 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
 }
 
 // Plan launch of the shared-prefix decode: CTA 0 plans the suffix pass, CTA 1
-// the prefix pass; CTAs 2 .. 2+k-1 gather the query rows of every KV head in
-// sequence-major order (qv[h][b*G + g] = q[b][h*G + g]) and check that every
-// table row starts with row 0's prefix pages (PKV_DEV_BAD_PREFIX into the
-// suffix header's status slot of the CTA).
+// the prefix pass's virtual decode (CUDA-core variant); CTAs 2 .. 2+k-1 gather
+// the query rows of every KV head in sequence-major order (qv[h][b*G + g] =
+// q[b][h*G + g]; CUDA-core variant, qv non-null) and check that every table
+// row starts with row 0's prefix pages (PKV_DEV_BAD_PREFIX into the suffix
+// header's status slot of the CTA).
 __global__ void __launch_bounds__(1024)
 cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
     pdl_wait();
@@ -400,7 +401,7 @@ cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
     }
     const int c = blockIdx.x - 2;
     const long long stride = (long long)k * blockDim.x;
-    const long long total = (long long)g.batch * g.n_kv_heads * g.group * g.vecs;
+    const long long total = g.qv ? (long long)g.batch * g.n_kv_heads * g.group * g.vecs : 0;
     for (long long idx = (long long)c * blockDim.x + threadIdx.x; idx < total; idx += stride) {
         const int vec = (int)(idx % g.vecs);
         const long long row = idx / g.vecs;  // (h * B + b) * G + gi in qv
@@ -649,8 +650,10 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 
 cudaError_t launch_cascade_plan(const PlanArgs& ps, const PlanArgs& pv, const CascadeGather& g,
                                 cudaStream_t stream) {
-    // gather + check CTAs: about 4 K vectors (64 KiB of q) each, at most kMaxAppendCtas
-    const long long total = (long long)g.batch * g.n_kv_heads * g.group * g.vecs;
+    // gather + check CTAs: about 4 K vectors (64 KiB of q, or of table cells when
+    // nothing is gathered) each, at most kMaxAppendCtas
+    const long long total = g.qv ? (long long)g.batch * g.n_kv_heads * g.group * g.vecs
+                                 : (long long)(g.batch - 1) * g.share_cols;
     int k = (int)((total + 4095) / 4096);
     k = k < 1 ? 1 : (k > kMaxAppendCtas ? kMaxAppendCtas : k);
     return launch_pdl(cascade_plan_kernel, dim3(2 + k), dim3(1024), 0, stream, ps, pv, g, k);

@@ -92,18 +92,21 @@ struct CascadeArgs {
 
 // Shared-prefix pass on the fifth-generation tensor cores (prefix_umma.cu):
 // grid (splits, tiles, n_kv_heads); CTA (s, t, h) attends query rows
-// [t * tile_rows, t * tile_rows + 128) of KV head h (rows of qv, [Hkv][rows][D])
-// over its balanced range of the prefix's chunks and writes one partial
-// state: o as 8-float groups (element (r, d) at ((d / 8) * 128 + r) * 8 +
-// d % 8), then m [128], then l [128] -- 128 * D + 256 floats per slot, slot
-// (h * tiles + t) * splits + s.
+// [t * tile_rows, (t + 1) * tile_rows) of KV head h -- row b * G + g is
+// q[b][h * G + g], read through a 3-D tensor map of q ([B][Hq][D], boxes of
+// 64 x G x tile_rows / G) -- over its balanced range of the prefix's chunks
+// and writes one partial
+// state: o [128][D], then m [128], then l [128] -- 128 * D + 256 floats per
+// slot, slot (h * tiles + t) * splits + s; o goes through `omap`, a 3-D fp32
+// tensor map of the slots (D, 128, slots) with boxes of 32 x 128 x 1.
 struct PrefixUmmaArgs {
     const int32_t* table;  // the prefix's page ids (row 0 of the page table)
     int num_pages, n_kv_heads, page_size;
     int chunks;            // 16-token chunks of the prefix
     int splits;            // ranges of chunks per (KV head, tile), 1 .. chunks
     int rows;              // query rows per KV head (B * G)
-    int tile_rows;         // rows of a tile that belong to it (<= 128)
+    int group;             // G
+    int tile_rows;         // rows of a tile that belong to it: a multiple of G, <= 128
     int tiles;             // tiles per KV head
     float scale_log2;      // scale * log2(e)
     float* partials;
@@ -114,7 +117,8 @@ constexpr int kPrefixTileRows = 128;  // rows of one tensor-core tile (and of a 
 
 cudaError_t launch_prefix_umma(pkv_dtype dtype, int head_dim, const PrefixUmmaArgs& a,
                                const CUtensorMap& qmap, const CUtensorMap& kmap,
-                               const CUtensorMap& vmap, cudaStream_t stream);
+                               const CUtensorMap& vmap, const CUtensorMap& omap,
+                               cudaStream_t stream);
 
 // CTAs of the prefix kernel that fit on one SM (0 on an error).
 int prefix_umma_ctas_per_sm(pkv_dtype dtype, int head_dim);
@@ -122,7 +126,7 @@ int prefix_umma_ctas_per_sm(pkv_dtype dtype, int head_dim);
 // The query gather and prefix check of the shared-prefix decode's plan launch.
 struct CascadeGather {
     const uint4* q;        // [B][Hkv * G][D] as 16-byte vectors
-    uint4* qv;             // [Hkv][B * G][D]: qv[h][b*G + g] = q[b][h*G + g]
+    uint4* qv;             // [Hkv][B * G][D]: qv[h][b*G + g] = q[b][h*G + g]; null: no gather
     int batch, n_kv_heads, group, vecs;
     const int32_t* table;  // rows 1 .. B-1 must start with row 0's first share_cols ids
     int table_stride, share_cols;

@@ -59,8 +59,7 @@ struct SlotSegs {
 };
 
 // Segment s of a shared-prefix row tile (prefix_umma.cu): slots base, base + 1,
-// ... of kPrefixTileRows rows, o stored as 8-float groups (element (g, d) at
-// ((d / 8) * rows + g) * 8 + d % 8), then m [rows], then l [rows].
+// ... of 128 rows each: o [128][d], then m [128], then l [128].
 struct TileSegs {
     static constexpr int kRows = 128;
     const float* partials;
@@ -70,7 +69,7 @@ struct TileSegs {
         return partials + (base + s) * (long long)(kRows * d + 2 * kRows);
     }
     __device__ __forceinline__ const float4* o4(int s, int g, int v) const {
-        return reinterpret_cast<const float4*>(slot(s) + ((v >> 1) * kRows + g) * 8) + (v & 1);
+        return reinterpret_cast<const float4*>(slot(s) + (long long)g * d) + v;
     }
     __device__ __forceinline__ const float* m(int s, int g) const { return slot(s) + kRows * d + g; }
     __device__ __forceinline__ const float* l(int s, int g) const { return m(s, g) + kRows; }

@@ -16,8 +16,9 @@
 //   P  = 2^(S*scale*log2e - m)  one thread per row, read with tcgen05.ld
 //   O  = O * 2^(m_old - m) + P V   tcgen05.mma M=128, N=D, K=block tokens
 //
-// with S and O in tensor memory (one lane per query row).  Q, K and V arrive
-// by TMA (cp.async.bulk.tensor, 128-byte swizzle, [64 x rows] boxes); P is
+// with S and O in tensor memory (one lane per query row).  Q (a 3-D box of
+// G heads x tile_rows / G sequences straight from q), K and V arrive by TMA
+// (cp.async.bulk.tensor, 128-byte swizzle, 64-element inner boxes); P is
 // written to shared memory in the same swizzled K-major layout (bf16 P as a
 // high part plus a bf16 residual, two MMAs, as in the warp-level decode
 // kernel), the high part over K and the residual over Q, both consumed by
@@ -26,10 +27,18 @@
 // heads x 64 sequences x 4 heads of a group take two tiles per KV head --
 // instead of once per 16-row warp tile.
 //
-// The CTA leaves one partial state of its 128 rows: o as groups of 8 floats
-// (group j of row r at (j * 128 + r) * 8, so that a warp's stores are
-// contiguous), then m [128] (base-2 units) and l [128].  The cascade's merge
-// combines the splits with the suffix pass's partial states.
+// The CTA leaves one partial state of its 128 rows: o [128][D] (fp32, staged
+// in swizzled shared memory and written by TMA tensor stores), then m [128]
+// (base-2 units) and l [128].  The cascade's merge combines the splits with
+// the suffix pass's partial states.
+//
+// The pass reads only the caller's inputs (q, row 0 of the page table, the
+// pools) and writes only its own slots and the call's status word.  The
+// kernel before it in the stream is the call's plan launch, which writes
+// neither inputs nor slots and itself waited for every earlier kernel before
+// this one could start; so the copies and products run before the
+// programmatic-dependency wait, overlapping the plan, and only the status
+// word (which the plan resets) is written after it.
 //
 // Every wait is bounded: on a timeout the CTA records PKV_DEV_TIMEOUT, waits
 // (bounded) for its copies or MMAs still in flight, frees its tensor memory
@@ -74,6 +83,10 @@ struct PrefixLayout {
     static constexpr int kTmemCols = kColsS + D <= 256 ? 256 : 512;
     // barriers and slots, alignment slack; at least 80 KiB, so that no more
     // CTAs share an SM than its 512 tensor-memory columns serve
+    // o staged for the tensor stores: D / 32 column blocks of [128 rows x 128 B]
+    // over the Q and K regions (free once the last product is done)
+    static constexpr int kOutBlocks = D / 32;
+    static_assert(kOutBlocks * kTileRows * 128 <= kOffV, "o fits the Q and K regions");
     static constexpr int kUsed = kOffBar + 64 + 1024;
     static constexpr int kBytes = kUsed > 80 * 1024 ? kUsed : 80 * 1024;
     static_assert(kTmemCols <= 256, "two CTAs per SM share the tensor memory");
@@ -83,7 +96,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap) {
+                   const __grid_constant__ CUtensorMap vmap,
+                   const __grid_constant__ CUtensorMap omap) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr bool kSplitP = kBf16;
     using Lay = PrefixLayout<D, kSplitP>;
@@ -109,6 +123,8 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
                      : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap))
                      : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&omap))
+                     : "memory");
     }
     tc_fence_before();
     __syncthreads();
@@ -117,19 +133,19 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
     // this thread's row: tensor-memory lane tid (warp w reaches lanes 32w..32w+31)
     const uint32_t row_s = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t row_o = row_s + Lay::kColsS;
-    pdl_wait();  // the query rows come from the plan launch's gather
-    pdl_trigger();
+    pdl_trigger();  // the next kernel waits for this grid's completion itself
 
     const int split = blockIdx.x, tile = blockIdx.y, h = blockIdx.z;
     const int per = a.chunks / a.splits, ext = a.chunks - per * a.splits;
     const int c0 = split * per + min(split, ext);
     const int cn = per + (split < ext ? 1 : 0);
-    const int qrow = h * a.rows + tile * a.tile_rows;  // the tile's first row of qv
+    const int qseq = tile * (a.tile_rows / a.group);  // the tile's first sequence
     const int nblk = (cn + kBlockChunks - 1) / kBlockChunks;
     const float sl2 = a.scale_log2;
 
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t ph_load = 0, ph_mma = 0;
+    uint32_t flags = 0;         // PKV_DEV_* bits, written after the dependency wait
     uint64_t* stuck = nullptr;  // a wait that gave up: its barrier (and phase below)
     uint32_t stuck_phase = 0;
     for (int blk = 0; blk < nblk; ++blk) {
@@ -145,21 +161,21 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
                 const int tok = (cb + lane) * kChunk;
                 const int page = __ldg(a.table + tok / a.page_size);
                 good = page >= 0 && page < a.num_pages;
-                if (good)
-                    y = (page * a.n_kv_heads + h) * a.page_size + tok % a.page_size;
-                else
-                    set_status(a.status, PKV_DEV_BAD_PAGE);
+                if (good) y = (page * a.n_kv_heads + h) * a.page_size + tok % a.page_size;
             }
             const uint32_t goodm = __ballot_sync(kFull, good);
             const uint32_t badm = __ballot_sync(kFull, lane < nch && !good);
+            if (badm) flags |= PKV_DEV_BAD_PAGE;
             if (lane == 0) {
                 *bad_slot = badm;
-                const uint32_t bytes = (uint32_t)Lay::kQBytes +
+                // a Q box is tile_rows rows (rows past them keep stale data: their
+                // results are never read)
+                const uint32_t bytes = (uint32_t)(Lay::kBoxes * a.tile_rows * 128) +
                                        (uint32_t)__popc(goodm) * 2u * kChunk * D * 2u;
                 mbar_arrive_expect_tx(bar_load, bytes);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_2d(base + Lay::kOffQ + bx * Lay::kQBlock, &qmap, bx * 64, qrow,
-                                bar_load);
+                    tma_load_3d(base + Lay::kOffQ + bx * Lay::kQBlock, &qmap, bx * 64,
+                                h * a.group, qseq, bar_load);
             }
             __syncwarp();
             if (good)
@@ -212,25 +228,29 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
         ph_mma ^= 1u;
         tc_fence_after();
 
-        // ---- online softmax of row tid over the block (base 2)
+        // ---- online softmax of row tid over the block (base 2): the row's
+        // scores come out of tensor memory once (the loads are warp-collective:
+        // the block length is the same for every thread)
+        uint32_t r[kBlockTok / 32][32];
+#pragma unroll
+        for (int jb = 0; jb < kBlockTok / 32; ++jb)
+            if (jb * 32 < ntok) tmem_ld32(row_s + jb * 32, r[jb]);
         float mx = -INFINITY;
-        for (int j = 0; j < ntok; j += 32) {
-            uint32_t r[32];
-            tmem_ld32(row_s + j, r);
+#pragma unroll
+        for (int jb = 0; jb < kBlockTok / 32; ++jb)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const int t = j + e;
+                const int t = jb * 32 + e;
                 const bool ok = t < ntok && !((badm >> (t >> 4)) & 1u);
-                mx = ok ? fmaxf(mx, __uint_as_float(r[e]) * sl2) : mx;
+                mx = ok ? fmaxf(mx, __uint_as_float(r[jb][e]) * sl2) : mx;
             }
-        }
         const float m_new = fmaxf(m_run, mx);
         const float m_ref = m_new == -INFINITY ? 0.f : m_new;  // no token yet: weights 0
         const float alpha = fast_exp2(m_run - m_ref);
         float sum = 0.f;
-        for (int j = 0; j < ntok; j += 32) {
-            uint32_t r[32];
-            tmem_ld32(row_s + j, r);
+#pragma unroll
+        for (int jb = 0; jb < kBlockTok / 32; ++jb) {
+            const int j = jb * 32;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int t0 = j + 8 * q;  // the 8-token piece t0 .. t0+7 of row tid
@@ -239,7 +259,7 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
                 for (int e = 0; e < 8; ++e) {
                     const int t = t0 + e;
                     const bool ok = t < ntok && !((badm >> (t >> 4)) & 1u);
-                    p[e] = ok ? fast_exp2(__uint_as_float(r[8 * q + e]) * sl2 - m_ref) : 0.f;
+                    p[e] = ok ? fast_exp2(__uint_as_float(r[jb][8 * q + e]) * sl2 - m_ref) : 0.f;
                     sum += p[e];
                 }
                 if (t0 < ntok) {
@@ -307,37 +327,37 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
         tc_fence_after();
     }
 
+    pdl_wait();  // the plan launch has reset the status word
     if (!stuck) {
-        // the partial state of row tid: o in 8-float groups, then m and l
-        float* slot = a.partials + ((long long)(h * a.tiles + tile) * a.splits + split) *
-                                       (long long)(kTileRows * D + 2 * kTileRows);
-        if (nblk > 0) {
+        if (flags && lane == 0) set_status(a.status, flags);
+        // the partial state of row tid: o staged in swizzled shared memory
+        // (row tid, 16-byte piece c of column block jb at piece c ^ (tid & 7)),
+        // then D / 32 tensor stores of [128 rows x 32 floats]; m and l stored
+        // directly (coalesced)
+        const long long slot = (long long)(h * a.tiles + tile) * a.splits + split;
 #pragma unroll
-            for (int j = 0; j < D; j += 32) {
-                uint32_t r[32];
-                tmem_ld32(row_o + j, r);
+        for (int jb = 0; jb < Lay::kOutBlocks; ++jb) {
+            uint32_t o[32];
+            tmem_ld32(row_o + jb * 32, o);
+            uint8_t* row = base + jb * kTileRows * 128 + tid * 128;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float4* dst =
-                        reinterpret_cast<float4*>(slot + ((j / 8 + q) * kTileRows + tid) * 8);
-                    dst[0] = make_float4(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1]),
-                                         __uint_as_float(r[8 * q + 2]),
-                                         __uint_as_float(r[8 * q + 3]));
-                    dst[1] = make_float4(__uint_as_float(r[8 * q + 4]),
-                                         __uint_as_float(r[8 * q + 5]),
-                                         __uint_as_float(r[8 * q + 6]),
-                                         __uint_as_float(r[8 * q + 7]));
-                }
-            }
-        } else {
-            for (int j = 0; j < D; j += 4)
-                *reinterpret_cast<float4*>(slot + ((j / 8) * kTileRows + tid) * 8 + (j & 4)) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(row + ((c ^ (tid & 7)) << 4)) =
+                    make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         }
-        slot[kTileRows * D + tid] = m_run;
-        slot[kTileRows * D + kTileRows + tid] = l_run;
+        float* ml = a.partials + slot * (long long)(kTileRows * D + 2 * kTileRows) + kTileRows * D;
+        ml[tid] = m_run;
+        ml[kTileRows + tid] = l_run;
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            for (int jb = 0; jb < Lay::kOutBlocks; ++jb)
+                tma_store_3d(&omap, base + jb * kTileRows * 128, jb * 32, 0, (int)slot);
+            bulk_commit_group();
+            bulk_wait_group_all();  // the stores are done before the CTA leaves
+        }
     } else {
-        if (tid == 0) set_status(a.status, PKV_DEV_TIMEOUT);
+        if (tid == 0) set_status(a.status, flags | PKV_DEV_TIMEOUT);
         mbar_wait_bounded(stuck, stuck_phase);  // what is still in flight lands first
     }
     tc_fence_before();
@@ -345,42 +365,59 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
     if (warp == 0) tmem_dealloc(tmem, Lay::kTmemCols);
 }
 
+// Dynamic shared memory opt-in and the largest shared-memory carveout (two
+// CTAs of up to 113 KiB per SM), once per process and instantiation.
 template <typename T, int D>
-cudaError_t launch_t(const PrefixUmmaArgs& a, const CUtensorMap& qm, const CUtensorMap& km,
-                     const CUtensorMap& vm, cudaStream_t stream) {
+cudaError_t prepare_t() {
     using Lay = PrefixLayout<D, std::is_same<T, __nv_bfloat16>::value>;
     auto fn = prefix_umma_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::kBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(fn, dim3(a.splits, a.tiles, a.n_kv_heads), dim3(kUmmaThreads),
-                      (size_t)Lay::kBytes, stream, a, qm, km, vm);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    return e;
 }
 
 template <typename T, int D>
+cudaError_t launch_t(const PrefixUmmaArgs& a, const CUtensorMap& qm, const CUtensorMap& km,
+                     const CUtensorMap& vm, const CUtensorMap& om, cudaStream_t stream) {
+    using Lay = PrefixLayout<D, std::is_same<T, __nv_bfloat16>::value>;
+    const cudaError_t e = prepare_t<T, D>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(prefix_umma_kernel<T, D>, dim3(a.splits, a.tiles, a.n_kv_heads),
+                      dim3(kUmmaThreads), (size_t)Lay::kBytes, stream, a, qm, km, vm, om);
+}
+
+// CTAs per SM: what the SM's shared memory holds (each CTA also reserves the
+// driver's per-block share), at most two (tensor-memory columns).
+template <typename T, int D>
 int ctas_per_sm_t() {
     using Lay = PrefixLayout<D, std::is_same<T, __nv_bfloat16>::value>;
-    auto fn = prefix_umma_kernel<T, D>;
-    int n = 0;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes) !=
+    int dev = 0, smem = 0, reserved = 0;
+    if (prepare_t<T, D>() != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kUmmaThreads, Lay::kBytes) !=
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
             cudaSuccess)
         return 0;
-    return n;
+    const int n = smem / (Lay::kBytes + reserved);
+    const int by_tmem = 512 / Lay::kTmemCols;
+    return n < by_tmem ? n : by_tmem;
 }
 
 }  // namespace
 
 cudaError_t launch_prefix_umma(pkv_dtype dtype, int head_dim, const PrefixUmmaArgs& a,
                                const CUtensorMap& qmap, const CUtensorMap& kmap,
-                               const CUtensorMap& vmap, cudaStream_t stream) {
+                               const CUtensorMap& vmap, const CUtensorMap& omap,
+                               cudaStream_t stream) {
     if (a.splits <= 0 || a.tiles <= 0) return cudaSuccess;
     if (dtype == PKV_BF16)
-        return head_dim == 128 ? launch_t<__nv_bfloat16, 128>(a, qmap, kmap, vmap, stream)
-                               : launch_t<__nv_bfloat16, 64>(a, qmap, kmap, vmap, stream);
-    return head_dim == 128 ? launch_t<__half, 128>(a, qmap, kmap, vmap, stream)
-                           : launch_t<__half, 64>(a, qmap, kmap, vmap, stream);
+        return head_dim == 128 ? launch_t<__nv_bfloat16, 128>(a, qmap, kmap, vmap, omap, stream)
+                               : launch_t<__nv_bfloat16, 64>(a, qmap, kmap, vmap, omap, stream);
+    return head_dim == 128 ? launch_t<__half, 128>(a, qmap, kmap, vmap, omap, stream)
+                           : launch_t<__half, 64>(a, qmap, kmap, vmap, omap, stream);
 }
 
 int prefix_umma_ctas_per_sm(pkv_dtype dtype, int head_dim) {

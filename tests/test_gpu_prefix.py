@@ -50,6 +50,8 @@ CASES = [
     (5, 28, 4, 128, 32, torch.float16, 256, 700),      # group 7
     (6, 16, 16, 64, 16, torch.float16, 96, 0),         # no suffixes at all, group 1
     (9, 32, 8, 64, 32, torch.bfloat16, 1024, 2000),
+    (7, 28, 1, 128, 16, torch.float16, 64, 100),       # group 28: tiles of 4 sequences
+    (40, 28, 4, 128, 32, torch.bfloat16, 96, 33),      # group 7: three tiles, the last partial
 ]
 
 
