@@ -1114,7 +1114,14 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
             return st;
         const int chunks = prefix_tokens / pkv::kChunk;
         splits = ps.max_splits < chunks ? ps.max_splits : chunks;
+        // plan, then the suffixes, then the prefix pass: it needs nothing the
+        // suffix pass writes, so its CTAs take the SMs the suffix pass's warps
+        // leave, and its partial states are fresh in L2 for the merge
         if ((st = cuda_status(pkv::launch_cascade_plan(pss, pv, g, cs))) != PKV_OK) return st;
+        if ((st = do_run(q, k_pool, v_pool, page_table + skip, table_stride, batch, n_q_heads,
+                         n_kv_heads, head_dim, page_size, num_pages, dtype, scale, out, ws_s,
+                         ps.real, false, cs, true)) != PKV_OK)
+            return st;
         pkv::PrefixUmmaArgs pa;
         pa.table = page_table;
         pa.num_pages = num_pages;
@@ -1142,11 +1149,11 @@ pkv_status paged_decode_attention_prefix(const void* q, const void* k_pool, cons
             return st;
         c.v_partials = reinterpret_cast<const float*>(wv + ps.virt.ws.partials);
         c.v_hdr = reinterpret_cast<const WsHeader*>(wv);
+        if ((st = do_run(q, k_pool, v_pool, page_table + skip, table_stride, batch, n_q_heads,
+                         n_kv_heads, head_dim, page_size, num_pages, dtype, scale, out, ws_s,
+                         ps.real, false, cs, true)) != PKV_OK)
+            return st;
     }
-    if ((st = do_run(q, k_pool, v_pool, page_table + skip, table_stride, batch, n_q_heads,
-                     n_kv_heads, head_dim, page_size, num_pages, dtype, scale, out, ws_s, ps.real,
-                     false, cs, true)) != PKV_OK)
-        return st;
     uint8_t* wsu = static_cast<uint8_t*>(ws_s);
     c.s_partials = reinterpret_cast<const float*>(wsu + ps.real.ws.partials);
     c.s_prefix = reinterpret_cast<const int32_t*>(wsu + ps.real.ws.prefix);

@@ -34,11 +34,13 @@
 //
 // The pass reads only the caller's inputs (q, row 0 of the page table, the
 // pools) and writes only its own slots and the call's status word.  The
-// kernel before it in the stream is the call's plan launch, which writes
-// neither inputs nor slots and itself waited for every earlier kernel before
-// this one could start; so the copies and products run before the
-// programmatic-dependency wait, overlapping the plan, and only the status
-// word (which the plan resets) is written after it.
+// kernel before it in the stream is the call's suffix pass, which writes
+// neither inputs nor these slots and waited for every earlier kernel (the
+// plan launch included) before this one could start; so the copies and
+// products run before the programmatic-dependency wait -- the CTAs take the
+// SMs that the suffix pass's warps leave -- and the results are written
+// after it.  The wait also keeps the order for the merge that follows: this
+// grid completes only after the suffix pass has.
 //
 // Every wait is bounded: on a timeout the CTA records PKV_DEV_TIMEOUT, waits
 // (bounded) for its copies or MMAs still in flight, frees its tensor memory
@@ -327,7 +329,7 @@ prefix_umma_kernel(const PrefixUmmaArgs a, const __grid_constant__ CUtensorMap q
         tc_fence_after();
     }
 
-    pdl_wait();  // the plan launch has reset the status word
+    pdl_wait();  // the suffix pass is complete (and the plan long before it)
     if (!stuck) {
         if (flags && lane == 0) set_status(a.status, flags);
         // the partial state of row tid: o staged in swizzled shared memory
