@@ -89,6 +89,27 @@ def test_row_without_the_shared_pages_is_reported():
     assert pkv.pkv_read_device_status(ws) & pkv.DEV_BAD_PREFIX
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_bad_prefix_page_is_skipped_and_reported(variant):
+    """A page id outside the pool inside the shared prefix (the same in every
+    row, so the rows still share it): the prefix pass skips that chunk and
+    flags PKV_DEV_BAD_PAGE, like the plain decode, whose output it then
+    matches (both attend every token but those 16)."""
+    w = _shared(31, B=4, Hq=8, Hkv=2, D=128, P=16, dtype=torch.bfloat16, prefix=64,
+                suffix_max=40)
+    w.page_table[:, 1] = w.num_pages + 3
+    out, ws = _run(w, 64, variant)
+    assert pkv.pkv_read_device_status(ws) & pkv.DEV_BAD_PAGE
+    table, lens, _ = to_dev(w)
+    plain = torch.full_like(w.q, float("nan"))
+    wsp = pkv.alloc_workspace(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, variant=variant)
+    pkv.paged_decode_attention(w.q, w.k_pool, w.v_pool, table, lens, w.scale, plain, wsp,
+                               variant=variant)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_device_status(wsp) & pkv.DEV_BAD_PAGE
+    assert_close(out, plain.float().cpu().numpy().astype(np.float64), what="bad prefix page")
+
+
 def test_length_shorter_than_prefix_is_reported():
     w = _shared(9, B=3, Hq=8, Hkv=2, D=128, P=16, dtype=torch.bfloat16, prefix=64,
                 suffix_max=50)
