@@ -36,6 +36,7 @@ import hashlib
 import io
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -121,10 +122,15 @@ def measured_peak():
 
 
 def decode_source_hash() -> str:
+    """Hash of the decode kernel's sources with comments and blank space
+    removed: an edit of a comment keeps a profile taken on the same code."""
     h = hashlib.sha256()
     for rel in DECODE_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -561,6 +567,38 @@ def run_ours(args):
     if pkv.pkv_read_device_status(ws):
         raise RuntimeError("device status set during warm-up")
 
+    # An untimed read of twice the L2 size (a read, not a write: dirty lines
+    # would be written back inside the next timed region) before each run of
+    # flushed_ms.  Used for the decode kernel's roofline timing and for a
+    # second figure of the step: no run finds anything of its own in L2.
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flushed_ms(fn, n):
+        """Mean of n runs of fn, each timed by its own events after a flush."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.amax()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
+    def timed_loop(fn, n):
+        """Mean of n runs of fn back to back (after warm-up)."""
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(dist, e0.elapsed_time(e1) / n, dev)
+
     K = args.steps
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -579,6 +617,9 @@ def run_ours(args):
     total_ms = t_start.elapsed_time(t_end)
     ms_step = total_ms / K
     ms_step = max_over_ranks(dist, ms_step, dev)
+    # the same step with L2 flushed before each
+    KF = max(1, min(K, 2000))
+    ms_flushed = max_over_ranks(dist, flushed_ms(step, KF), dev)
     clocks = sampler.finish()
 
     # ---- the same step with the rotary embedding of q and k_new fused into
@@ -590,21 +631,7 @@ def run_ours(args):
         pkv.paged_decode_step_rope(w.k_new, w.v_new, pos, w.q, w.k_pool, w.v_pool, table, lens,
                                    w.scale, rope_theta, out, ws, nw, variant=var)
 
-    for _ in range(max(3, args.warmup)):
-        rope_step()
-    r0 = torch.cuda.Event(enable_timing=True)
-    r1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    r0.record(stream)
-    for _ in range(KR):
-        rope_step()
-    r1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    rope_ms = max_over_ranks(dist, r0.elapsed_time(r1) / KR, dev)
+    rope_ms = timed_loop(rope_step, KR)
     # the same with the per-head RMS norm of q and k before the rotation
     gn = torch.Generator(device=dev).manual_seed(args.seed + 2)
     wq = (1.0 + 0.3 * torch.randn(w.head_dim, generator=gn, device=dev)).to(w.dtype)
@@ -615,19 +642,7 @@ def run_ours(args):
                                    w.scale, rope_theta, out, ws, nw, variant=var,
                                    q_norm_weight=wq, k_norm_weight=wk, norm_eps=1e-6)
 
-    for _ in range(max(3, args.warmup)):
-        rope_norm_step()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    r0.record(stream)
-    for _ in range(KR):
-        rope_norm_step()
-    r1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    rope_norm_ms = max_over_ranks(dist, r0.elapsed_time(r1) / KR, dev)
+    rope_norm_ms = timed_loop(rope_norm_step, KR)
 
     # ---- shared-prefix decode on the prefix-sharing workload (64 sequences,
     # one 2048-token prefix): the cascade against the plain decode ----
@@ -640,25 +655,18 @@ def run_ours(args):
     wsp = pkv.alloc_prefix_workspace(wp.batch, wp.n_q_heads, wp.n_kv_heads, wp.head_dim, nw,
                                      device=dev, variant=var)
 
-    def timed_loop(fn, n):
-        for _ in range(max(3, args.warmup)):
-            fn()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return max_over_ranks(dist, e0.elapsed_time(e1) / n, dev)
-
     KP = max(1, min(K, 2000))
     prefix_ms = timed_loop(lambda: pkv.paged_decode_attention_prefix(
         wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, wp.prefix_len, op, wsp, nw,
         variant=var), KP)
     plain_ms = timed_loop(lambda: pkv.paged_decode_attention(
         wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, op, wsp_plain, nw, variant=var), KP)
+    # its unique K/V (84 MB) fits in L2: the same two calls with L2 flushed before each
+    prefix_ms_flushed = max_over_ranks(dist, flushed_ms(lambda: pkv.paged_decode_attention_prefix(
+        wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, wp.prefix_len, op, wsp, nw,
+        variant=var), KP), dev)
+    plain_ms_flushed = max_over_ranks(dist, flushed_ms(lambda: pkv.paged_decode_attention(
+        wp.q, wp.k_pool, wp.v_pool, tp, lp, wp.scale, op, wsp_plain, nw, variant=var), KP), dev)
     pby = step_bytes(wp)
     del wp, tp, lp, op, wsp, wsp_plain
 
@@ -722,6 +730,7 @@ def run_ours(args):
     dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
     torch.cuda.synchronize()
     for i in range(KD):
+        flush.amax()
         split_step(dec0[i], dec1[i])
     torch.cuda.synchronize()
     dec_ms = [a.elapsed_time(b) for a, b in zip(dec0, dec1)]
@@ -805,6 +814,10 @@ def run_ours(args):
                     "(3 launches chained by programmatic dependent launch)",
         },
         "seqs_per_s": world * B / (ms_step * 1e-3),
+        "l2_flushed": {"ms_per_step": ms_flushed, "steps": KF,
+                       "value": aggregate_gbs(world, by["step"], ms_flushed), "unit": UNIT,
+                       "what": "the same step, each run after an untimed read of twice the "
+                               "L2 size, timed by its own events"},
         "pct_of_peak": 100.0 * value / world / peak,
         "bytes_per_step": by,
         "decode_kernel_ms": dec_avg,
@@ -817,7 +830,8 @@ def run_ours(args):
                      if var == pkv.VARIANT_CUDA_CORES else "pkv::decode_mma_kernel (tensor cores)",
                      "algorithmic_bytes": by["decode"],
                      "timing": f"CUDA events around paged_decode_run on its stream, mean of "
-                               f"{KD} steps run right after the timed region"},
+                               f"{KD} steps run right after the timed region, L2 flushed "
+                               f"before each"},
         "e2e": {"value": aggregate_gbs(world, by["step"], e2e_ms), "unit": UNIT,
                 "mode": "CUDA graph replay per step: packed pinned inputs in, "
                         "paged_decode_step, output out, then a host sync",
@@ -833,6 +847,7 @@ def run_ours(args):
                     "for all queries, then the suffixes, then the merge) vs "
                     "paged_decode_attention on the prefix_sharing workload",
             "ms_prefix": prefix_ms, "ms_plain": plain_ms, "steps": KP,
+            "ms_prefix_l2_flushed": prefix_ms_flushed, "ms_plain_l2_flushed": plain_ms_flushed,
             "gbs_unique_prefix": (pby["kv_unique"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
             "gbs_logical_prefix": (pby["kv_logical"] + pby["qo"]) / (prefix_ms * 1e-3) / 1e9,
             "gbs_logical_plain": (pby["kv_logical"] + pby["qo"]) / (plain_ms * 1e-3) / 1e9},

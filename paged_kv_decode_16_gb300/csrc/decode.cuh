@@ -144,6 +144,9 @@ decode_kernel(const DecodeParams p) {
         return;
     }
     const int units_per_b = ws.units_per_b;
+    // K/V lines are read once per call: they go first, so that what is read
+    // again (page table, schedule, partial states) stays in L2
+    const uint64_t kv_policy = l2_evict_first_policy();
 
     // Issue the copies of stream position j into stage j % STAGES; false past
     // the end of the stream.
@@ -158,8 +161,10 @@ decode_kernel(const DecodeParams p) {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bar[st], 2 * kv_bytes + q_bytes);
             if (kv_bytes) {
-                bulk_g2s(sk + st * kChunk * D, kpool + d.off * D, kv_bytes, &bar[st]);
-                bulk_g2s(sv + st * kChunk * D, vpool + d.off * D, kv_bytes, &bar[st]);
+                bulk_g2s_hint(sk + st * kChunk * D, kpool + d.off * D, kv_bytes, &bar[st],
+                              kv_policy);
+                bulk_g2s_hint(sv + st * kChunk * D, vpool + d.off * D, kv_bytes, &bar[st],
+                              kv_policy);
             }
             if (q_bytes) {
                 const int b = d.u / units_per_b;

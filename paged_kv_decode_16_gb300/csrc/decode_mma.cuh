@@ -168,6 +168,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
     }
 
     const int units_per_b = ws.units_per_b;
+    // K/V lines are read once per call: they go first, so that what is read
+    // again (page table, schedule, partial states) stays in L2
+    const uint64_t kv_policy = l2_evict_first_policy();
     const int g_lo = lane >> 2;          // query row of c0/c1 (c2/c3: g_lo + 8)
     const int tq = (lane & 3) * 2;       // first token (or d) column of this lane in a tile
     const T* __restrict__ qg = static_cast<const T*>(p.q);
@@ -197,9 +200,10 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 const int y = (int)d.off;  // first pool row of the chunk
 #pragma unroll
                 for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                    tma_load_2d(stage + bx * Lay::kBoxBytes, &kmap, bx * 64, y, &bar[st]);
-                    tma_load_2d(stage + (Lay::kBoxes + bx) * Lay::kBoxBytes, &vmap, bx * 64, y,
-                                &bar[st]);
+                    tma_load_2d_hint(stage + bx * Lay::kBoxBytes, &kmap, bx * 64, y, &bar[st],
+                                     kv_policy);
+                    tma_load_2d_hint(stage + (Lay::kBoxes + bx) * Lay::kBoxBytes, &vmap, bx * 64,
+                                     y, &bar[st], kv_policy);
                 }
             }
             if (q_bytes) {
