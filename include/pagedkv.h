@@ -323,11 +323,18 @@ typedef enum pkv_decode_variant {
     PKV_VARIANT_AUTO = 0,          /* the tensor-core kernel */
     PKV_VARIANT_CUDA_CORES = 1,    /* fp32 FMA on CUDA cores; K/V chunks by 1-D bulk copies;
                                       query sub-groups of at most 8 heads */
-    PKV_VARIANT_TENSOR_CORES = 2   /* q.k and p.v by warp MMA (m16n8k16, fp32 accumulate);
+    PKV_VARIANT_TENSOR_CORES = 2,  /* q.k and p.v by warp MMA (m16n8k16, fp32 accumulate);
                                       K/V chunks by swizzled 2-D tensor copies; query
                                       sub-groups of at most 16 heads; P enters the p.v
                                       product in the input dtype (bf16: as a high part
                                       plus a bf16 residual, two MMAs) */
+    PKV_VARIANT_TCGEN05 = 3        /* several query tokens per sequence only
+                                      (paged_decode_attention_multi), head_dim 128: units
+                                      of up to 64 query rows (tokens x heads) on the
+                                      fifth-generation tensor cores, one CTA per SM, the
+                                      products taken transposed (128 tokens of a block as
+                                      the tile's rows), accumulators in tensor memory;
+                                      other calls: PKV_ERR_UNSUPPORTED */
 } pkv_decode_variant;
 
 /* Bytes of device workspace paged_decode_attention needs for these shapes on

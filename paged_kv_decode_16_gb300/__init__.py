@@ -29,7 +29,7 @@ __all__ = [
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
     "pkv_read_device_status", "pkv_read_no_alloc_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
-    "VARIANT_AUTO", "VARIANT_CUDA_CORES", "VARIANT_TENSOR_CORES",
+    "VARIANT_AUTO", "VARIANT_CUDA_CORES", "VARIANT_TENSOR_CORES", "VARIANT_TCGEN05",
 ]
 
 PKV_OK = 0
@@ -38,7 +38,7 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 6: "PKV_ERR_CUDA", 7: "PKV_ERR_DEVICE_CHECK", 8: "PKV_ERR_REFCOUNT"}
 DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT, DEV_BAD_PREFIX = 0x1, 0x2, 0x4, 0x8
 # decode kernels (pkv_decode_variant)
-VARIANT_AUTO, VARIANT_CUDA_CORES, VARIANT_TENSOR_CORES = 0, 1, 2
+VARIANT_AUTO, VARIANT_CUDA_CORES, VARIANT_TENSOR_CORES, VARIANT_TCGEN05 = 0, 1, 2, 3
 # size of the library's fixed device scratch (PKV_NO_ALLOC_SCRATCH_BYTES)
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
 _DT = {torch.float16: 0, torch.bfloat16: 1}

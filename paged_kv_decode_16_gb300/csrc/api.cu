@@ -26,6 +26,7 @@ namespace {
 
 using pkv::DecodeKernelInfo;
 using pkv::DecodeMmaInfo;
+using pkv::DecodeUmmaInfo;
 using pkv::WsHeader;
 
 constexpr int kMinChunksPerWorker = 4;  // automatic worker count: at least this many chunks each
@@ -65,28 +66,45 @@ pkv_status check_shapes(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
 }
 
 inline bool valid_variant(int v) {
-    return v == PKV_VARIANT_AUTO || v == PKV_VARIANT_CUDA_CORES || v == PKV_VARIANT_TENSOR_CORES;
+    return v == PKV_VARIANT_AUTO || v == PKV_VARIANT_CUDA_CORES ||
+           v == PKV_VARIANT_TENSOR_CORES || v == PKV_VARIANT_TCGEN05;
 }
 
-// The decode kernel chosen for a call: an entry of either instantiation table.
+// The decode kernel chosen for a call: an entry of one instantiation table.
+// A worker is a warp, except on the tcgen05 kernel, where it is a CTA.
 struct KernelPick {
-    int variant = 0;  // PKV_VARIANT_CUDA_CORES or PKV_VARIANT_TENSOR_CORES
+    int variant = 0;  // PKV_VARIANT_CUDA_CORES, _TENSOR_CORES or _TCGEN05
     DecodeKernelInfo cc{};
     DecodeMmaInfo mma{};
+    DecodeUmmaInfo um{};
     const void* fn() const {
-        return variant == PKV_VARIANT_TENSOR_CORES ? reinterpret_cast<const void*>(mma.fn)
-                                                   : reinterpret_cast<const void*>(cc.fn);
+        return variant == PKV_VARIANT_TCGEN05     ? reinterpret_cast<const void*>(um.fn)
+               : variant == PKV_VARIANT_TENSOR_CORES ? reinterpret_cast<const void*>(mma.fn)
+                                                     : reinterpret_cast<const void*>(cc.fn);
     }
-    int warps() const { return variant == PKV_VARIANT_TENSOR_CORES ? mma.warps : cc.warps; }
+    int threads() const {
+        return variant == PKV_VARIANT_TCGEN05       ? 128
+               : variant == PKV_VARIANT_TENSOR_CORES ? mma.warps * 32
+                                                     : cc.warps * 32;
+    }
+    int warps() const {  // workers per CTA
+        return variant == PKV_VARIANT_TCGEN05       ? 1
+               : variant == PKV_VARIANT_TENSOR_CORES ? mma.warps
+                                                     : cc.warps;
+    }
     int smem() const {
-        return variant == PKV_VARIANT_TENSOR_CORES ? mma.smem_bytes : cc.smem_bytes;
+        return variant == PKV_VARIANT_TCGEN05       ? um.smem_bytes
+               : variant == PKV_VARIANT_TENSOR_CORES ? mma.smem_bytes
+                                                     : cc.smem_bytes;
     }
 };
 
 KernelPick pick_kernel(pkv_dtype dtype, int head_dim, int variant, int gs) {
     KernelPick k;
     k.variant = variant;
-    if (variant == PKV_VARIANT_TENSOR_CORES) {
+    if (variant == PKV_VARIANT_TCGEN05) {
+        k.um = pkv::decode_umma_info(dtype == PKV_BF16, head_dim, gs);
+    } else if (variant == PKV_VARIANT_TENSOR_CORES) {
         if (dtype == PKV_BF16)
             k.mma = head_dim == 128 ? pkv::decode_mma_info_bf16_d128(gs)
                                     : pkv::decode_mma_info_bf16_d64(gs);
@@ -101,7 +119,7 @@ KernelPick pick_kernel(pkv_dtype dtype, int head_dim, int variant, int gs) {
 }
 
 // Per (device, kernel): dynamic shared memory opt-in done, and the automatic
-// worker count = SMs x resident CTAs per SM x warps per CTA.
+// worker count = SMs x resident CTAs per SM x workers per CTA.
 std::mutex g_mu;
 std::map<std::pair<int, const void*>, int> g_auto_workers;
 
@@ -123,7 +141,7 @@ pkv_status prepare_kernel(const KernelPick& k, int* auto_workers) {
     if (cudaFuncSetAttribute(k.fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem()) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn(), k.warps() * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn(), k.threads(),
                                                       k.smem()) != cudaSuccess)
         return PKV_ERR_CUDA;
     const int workers = sms * (per_sm > 0 ? per_sm : 1) * k.warps();
@@ -190,8 +208,11 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
         // into the fewest tiles of at most kUnitRows tokens, of equal size but
         // the last, times the most heads of the group that still fit kUnitRows
         // rows; units of more than 16 rows run on the two-tile kernel
-        if (v != PKV_VARIANT_TENSOR_CORES || n_queries > kMaxQueries) return PKV_ERR_UNSUPPORTED;
-        constexpr int kUnitRows = 32;
+        if ((v != PKV_VARIANT_TENSOR_CORES && v != PKV_VARIANT_TCGEN05) ||
+            n_queries > kMaxQueries)
+            return PKV_ERR_UNSUPPORTED;
+        // tcgen05: one tile of up to 64 rows (N of the transposed products)
+        const int kUnitRows = v == PKV_VARIANT_TCGEN05 ? 64 : 32;
         const int t0 = (n_queries + kUnitRows - 1) / kUnitRows;
         const int qpu = (n_queries + t0 - 1) / t0;
         const int tiles = (n_queries + qpu - 1) / qpu;
@@ -199,9 +220,14 @@ pkv_status setup_decode(int batch, int n_q_heads, int n_kv_heads, int head_dim, 
         for (int d = 1; d <= s->group; ++d)
             if (s->group % d == 0 && qpu * d <= kUnitRows) hpu = d;
         const int rows = qpu * hpu;
-        s->gs = rows > 16 ? 32 : rows;
+        if (v == PKV_VARIANT_TCGEN05)
+            s->gs = rows <= 16 ? 16 : (rows <= 32 ? 32 : 64);  // N of the tile
+        else
+            s->gs = rows > 16 ? 32 : rows;
         s->sub_groups = (s->group / hpu) * tiles;
         s->rs = pkv::RowShape{n_queries, qpu, hpu, s->group / hpu, s->group, n_q_heads};
+    } else if (v == PKV_VARIANT_TCGEN05) {
+        return PKV_ERR_UNSUPPORTED;  // one query per sequence: the warp kernels
     } else if (force_gs > 0) {  // a sub-group size chosen by the caller (divides the group)
         if (force_gs > max_gs || s->group % force_gs) return PKV_ERR_UNSUPPORTED;
         s->gs = force_gs;
@@ -433,6 +459,24 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
     p.sub_groups = s.sub_groups;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int blocks = (s.workers + s.kernel.warps() - 1) / s.kernel.warps();
+    if (s.kernel.variant == PKV_VARIANT_TCGEN05) {
+        const long long rows = (long long)num_pages * n_kv_heads * page_size;
+        if (rows > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // 32-bit tensor row coordinate
+        const pkv::RowShape& rs = s.rs;
+        if ((long long)batch * rs.n_queries > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+        // q [B * n_queries][Hq][D]: a box is one unit's rows (queries_per_unit
+        // tokens x heads_per_unit heads, token-major)
+        CUtensorMap qm, km, vm;
+        pkv_status st = q_tile_map(q, batch * rs.n_queries, n_q_heads, head_dim, dtype,
+                                   rs.heads_per_unit, rs.heads_per_unit * rs.queries_per_unit,
+                                   &qm);
+        if (st == PKV_OK) st = pool_map(k_pool, rows, head_dim, dtype, &km);
+        if (st == PKV_OK) st = pool_map(v_pool, rows, head_dim, dtype, &vm);
+        if (st != PKV_OK) return st;
+        if (merge || all_partials) return PKV_ERR_UNSUPPORTED;  // the combine kernel merges
+        return cuda_status(pkv::launch_pdl(s.kernel.um.fn, dim3(blocks), dim3(128),
+                                           s.kernel.um.smem_bytes, stream, p, qm, km, vm));
+    }
     if (s.kernel.variant == PKV_VARIANT_TENSOR_CORES) {
         const long long rows = (long long)num_pages * n_kv_heads * page_size;
         if (rows > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // 32-bit tensor row coordinate

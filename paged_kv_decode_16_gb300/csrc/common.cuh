@@ -335,6 +335,16 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Launch configuration of one tcgen05 decode instantiation (decode_umma.cu:
+// one CTA of 128 threads per worker; the kernel also takes the q, K and V
+// tensor maps).
+struct DecodeUmmaInfo {
+    void (*fn)(DecodeParams, CUtensorMap, CUtensorMap, CUtensorMap) = nullptr;
+    int stages = 0;
+    int smem_bytes = 0;
+    int n = 0;  // query rows of the tile (a unit's rows rounded up)
+};
+
 // Launch configuration of one tensor-core decode instantiation (the kernel
 // also takes the K and V tensor maps).
 struct DecodeMmaInfo {

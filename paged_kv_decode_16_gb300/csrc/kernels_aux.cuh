@@ -162,6 +162,7 @@ DecodeKernelInfo decode_info_f16(int head_dim, int gs);
 // Tensor-core variant (decode_mma.cuh).
 DecodeMmaInfo decode_mma_info_bf16_d64(int gs);
 DecodeMmaInfo decode_mma_info_bf16_d128(int gs);
+DecodeUmmaInfo decode_umma_info(bool bf16, int head_dim, int rows);
 DecodeMmaInfo decode_mma_info_f16_d64(int gs);
 DecodeMmaInfo decode_mma_info_f16_d128(int gs);
 

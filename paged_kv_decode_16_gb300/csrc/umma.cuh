@@ -28,11 +28,12 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uin
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16 or
-// both fp16, A K-major, B K-major or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t umma_idesc(int m, int n, bool bf16, bool b_mn_major) {
+// both fp16, each K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc(int m, int n, bool bf16, bool b_mn_major,
+                                                  bool a_mn_major = false) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(m >> 4) << 24);
+           ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

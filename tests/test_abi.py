@@ -69,7 +69,8 @@ def _decode(lib, **kw):
     (dict(stride=0), INVALID),
     (dict(dt=5), INVALID),
     (dict(workers=-2), INVALID),
-    (dict(variant=3), INVALID),
+    (dict(variant=3), UNSUPPORTED),       # tcgen05: several query tokens only
+    (dict(variant=4), INVALID),
     (dict(variant=-1), INVALID),
     (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID),

@@ -162,3 +162,69 @@ def test_multi_captured_in_cuda_graph_equals_eager():
     w.context_lens[:] = lens.cpu().numpy()
     assert pkv.pkv_read_device_status(ws) == 0
     assert_close(out, _oracle(w, q), what="replay with new lengths")
+
+
+# ---- the tcgen05 kernel (PKV_VARIANT_TCGEN05): units of up to 64 rows, the
+# products transposed (128 tokens of a block as the tile's rows) ----
+
+UMMA_CASES = [c for c in range(len(CASES)) if CASES[c][4] == 128]
+
+
+@pytest.mark.parametrize("case", UMMA_CASES)
+def test_tcgen05_multi_query_matches_oracle(case):
+    B, Qn, Hq, Hkv, D, P, dtype, lens = CASES[case]
+    w, q = _case(200 + case, B=B, Qn=Qn, Hq=Hq, Hkv=Hkv, D=D, P=P, dtype=dtype, lens=lens)
+    ref = _oracle(w, q)
+    for nw in (0, 3, 1000):
+        out, ws = _run(w, q, num_workers=nw, variant=pkv.VARIANT_TCGEN05)
+        assert pkv.pkv_read_device_status(ws) == 0
+        assert_close(out, ref, what=f"tcgen05 case {case} workers {nw}")
+
+
+@pytest.mark.parametrize("qn", [2, 4, 8, 16])
+def test_tcgen05_on_the_llama3_8b_cache(qn):
+    """Llama-3-8B heads (32 / 8, D 128, bf16), the named workload's cache
+    (contexts 512-4096, poisoned unused slots), qn draft tokens per sequence:
+    units of qn x 4 rows (8..64), every output element against the oracle."""
+    w = wl.make("llama3_8b", seed=0, device="cuda", poison=True)
+    gen = torch.Generator(device="cuda").manual_seed(240 + qn)
+    q = torch.randn(w.batch, qn, w.n_q_heads, w.head_dim, generator=gen, device="cuda",
+                    dtype=torch.float32).to(w.dtype)
+    out, ws = _run(w, q, variant=pkv.VARIANT_TCGEN05)
+    assert pkv.pkv_read_device_status(ws) == 0
+    assert_close(out, _oracle(w, q), strict=True, what=f"llama3_8b cache, {qn} queries")
+
+
+def test_tcgen05_equals_warp_kernel_within_tolerance_and_is_deterministic():
+    rng = np.random.default_rng(241)
+    lens = rng.integers(1, 2500, size=12)
+    w, q = _case(241, B=12, Qn=8, Hq=32, Hkv=8, D=128, P=16, dtype=torch.bfloat16, lens=lens)
+    a, _ = _run(w, q, variant=pkv.VARIANT_TCGEN05)
+    b, _ = _run(w, q, variant=pkv.VARIANT_TCGEN05)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    c, _ = _run(w, q, variant=pkv.VARIANT_TENSOR_CORES)
+    assert_close(a, c.float().cpu().numpy().astype(np.float64), what="tcgen05 vs warp MMA")
+
+
+def test_tcgen05_bad_page_is_skipped_and_reported():
+    """A page id outside the pool: its chunk is skipped (not copied, not
+    attended) and PKV_DEV_BAD_PAGE is set, as in the warp kernel, whose
+    output it then matches."""
+    w, q = _case(242, B=3, Qn=4, Hq=16, Hkv=4, D=128, P=16, dtype=torch.bfloat16,
+                 lens=[200, 500, 64])
+    w.page_table[1, 3] = w.num_pages + 5
+    out, ws = _run(w, q, variant=pkv.VARIANT_TCGEN05)
+    assert pkv.pkv_read_device_status(ws) & pkv.DEV_BAD_PAGE
+    ref, ws2 = _run(w, q, variant=pkv.VARIANT_TENSOR_CORES)
+    assert pkv.pkv_read_device_status(ws2) & pkv.DEV_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, ref.float().cpu().numpy().astype(np.float64), what="bad page")
+
+
+def test_tcgen05_unsupported_shapes():
+    with pytest.raises(pkv.PagedKVError) as e:   # head_dim 64
+        pkv.alloc_multi_workspace(2, 4, 8, 2, 64, variant=pkv.VARIANT_TCGEN05)
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"
+    with pytest.raises(pkv.PagedKVError) as e:   # one query per sequence
+        pkv.alloc_workspace(2, 8, 2, 128, variant=pkv.VARIANT_TCGEN05)
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"
