@@ -68,7 +68,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-workers", type=int, default=0)
-    ap.add_argument("--variant", choices=["auto", "cuda_cores", "tensor_cores"], default="auto",
+    ap.add_argument("--variant", choices=["auto", "cuda_cores", "tensor_cores", "tcgen05"],
+                    default="auto",
                     help="decode kernel (auto = tensor cores)")
     ap.add_argument("--report", action="store_true",
                     help="per-configuration results instead of the bench line: for each named "
@@ -478,8 +479,16 @@ def run_ours(args):
                               w.k_pool, w.v_pool)
     out = torch.empty_like(w.q)
     nw = args.num_workers
+    # tcgen05 runs several query tokens per sequence only: the profile of the
+    # multi-query call; the step itself keeps the automatic kernel
+    multi_var = None
+    if args.variant == "tcgen05":
+        if not (args.profile_only and args.profile_path == "multi"):
+            raise SystemExit("--variant tcgen05 needs --profile-only --profile-path multi")
+        multi_var = pkv.VARIANT_TCGEN05
     var = {"auto": pkv.VARIANT_AUTO, "cuda_cores": pkv.VARIANT_CUDA_CORES,
-           "tensor_cores": pkv.VARIANT_TENSOR_CORES}[args.variant]
+           "tensor_cores": pkv.VARIANT_TENSOR_CORES,
+           "tcgen05": pkv.VARIANT_AUTO}[args.variant]
     ws = pkv.alloc_workspace(B, w.n_q_heads, w.n_kv_heads, w.head_dim, nw, device=dev,
                              variant=var)
     stream = torch.cuda.current_stream(dev)
@@ -506,11 +515,12 @@ def run_ours(args):
         qm = torch.randn(B, 8, w.n_q_heads, w.head_dim, generator=gq, device=dev,
                          dtype=torch.float32).to(w.dtype)
         om = torch.empty_like(qm)
+        mv = multi_var if multi_var is not None else var
         wsm = pkv.alloc_multi_workspace(B, 8, w.n_q_heads, w.n_kv_heads, w.head_dim, nw,
-                                        device=dev, variant=var)
+                                        device=dev, variant=mv)
         for _ in range(args.warmup + args.steps):
             pkv.paged_decode_attention_multi(qm, w.k_pool, w.v_pool, table, lens, w.scale, om,
-                                             wsm, nw, variant=var)
+                                             wsm, nw, variant=mv)
         torch.cuda.synchronize()
         status = pkv.pkv_read_device_status(wsm)
         if rank == 0:
@@ -675,18 +685,21 @@ def run_ours(args):
     QN = 4
     multi = None
     if var != pkv.VARIANT_CUDA_CORES:
-        def multi_ms_for(qn):
+        def multi_ms_for(qn, mvar=var):
             gq = torch.Generator(device=dev).manual_seed(args.seed + qn)
             qm = torch.randn(B, qn, w.n_q_heads, w.head_dim, generator=gq, device=dev,
                              dtype=torch.float32).to(w.dtype)
             om = torch.empty_like(qm)
             wsm = pkv.alloc_multi_workspace(B, qn, w.n_q_heads, w.n_kv_heads, w.head_dim, nw,
-                                            device=dev, variant=var)
+                                            device=dev, variant=mvar)
             return timed_loop(lambda: pkv.paged_decode_attention_multi(
-                qm, w.k_pool, w.v_pool, table, lens, w.scale, om, wsm, nw, variant=var), KP)
+                qm, w.k_pool, w.v_pool, table, lens, w.scale, om, wsm, nw, variant=mvar), KP)
 
         multi_ms = multi_ms_for(QN)
         multi8_ms = multi_ms_for(8)
+        # the tcgen05 kernel (transposed products, units of up to 64 rows)
+        tc5 = {qn: multi_ms_for(qn, pkv.VARIANT_TCGEN05) for qn in (4, 8, 16)}
+        multi16_ms = multi_ms_for(16)
         one_ms = timed_loop(lambda: pkv.paged_decode_attention(
             w.q, w.k_pool, w.v_pool, table, lens, w.scale, out, ws, nw, variant=var), KP)
         mbytes = by["kv_unique"] + QN * by["qo"]
@@ -699,7 +712,11 @@ def run_ours(args):
                  "tokens_per_s_multi": B * QN / (multi_ms * 1e-3),
                  "tokens_per_s_one_query": B / (one_ms * 1e-3),
                  "ms_multi_8": multi8_ms,
-                 "tokens_per_s_multi_8": B * 8 / (multi8_ms * 1e-3)}
+                 "tokens_per_s_multi_8": B * 8 / (multi8_ms * 1e-3),
+                 "ms_multi_16": multi16_ms,
+                 "tcgen05": {"what": "the same calls with variant PKV_VARIANT_TCGEN05",
+                             "ms_multi_4": tc5[4], "ms_multi_8": tc5[8],
+                             "ms_multi_16": tc5[16]}}
 
     # ---- the same step on the other full-size workloads: one sequence-long
     # context per (sequence, KV head) split over many warps, and the mixed

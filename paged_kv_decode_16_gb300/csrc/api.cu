@@ -83,7 +83,7 @@ struct KernelPick {
                                                      : reinterpret_cast<const void*>(cc.fn);
     }
     int threads() const {
-        return variant == PKV_VARIANT_TCGEN05       ? 128
+        return variant == PKV_VARIANT_TCGEN05       ? um.threads
                : variant == PKV_VARIANT_TENSOR_CORES ? mma.warps * 32
                                                      : cc.warps * 32;
     }
@@ -474,7 +474,7 @@ pkv_status do_run(const void* q, const void* k_pool, const void* v_pool, const i
         if (st == PKV_OK) st = pool_map(v_pool, rows, head_dim, dtype, &vm);
         if (st != PKV_OK) return st;
         if (merge || all_partials) return PKV_ERR_UNSUPPORTED;  // the combine kernel merges
-        return cuda_status(pkv::launch_pdl(s.kernel.um.fn, dim3(blocks), dim3(128),
+        return cuda_status(pkv::launch_pdl(s.kernel.um.fn, dim3(blocks), dim3(s.kernel.um.threads),
                                            s.kernel.um.smem_bytes, stream, p, qm, km, vm));
     }
     if (s.kernel.variant == PKV_VARIANT_TENSOR_CORES) {

@@ -98,6 +98,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
@@ -109,6 +113,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -336,13 +353,13 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 // Launch configuration of one tcgen05 decode instantiation (decode_umma.cu:
-// one CTA of 128 threads per worker; the kernel also takes the q, K and V
-// tensor maps).
+// one CTA per worker; the kernel also takes the q, K and V tensor maps).
 struct DecodeUmmaInfo {
     void (*fn)(DecodeParams, CUtensorMap, CUtensorMap, CUtensorMap) = nullptr;
     int stages = 0;
     int smem_bytes = 0;
-    int n = 0;  // query rows of the tile (a unit's rows rounded up)
+    int n = 0;        // query rows of the tile (a unit's rows rounded up)
+    int threads = 0;  // threads of a CTA (consumer warps + the producer warp)
 };
 
 // Launch configuration of one tensor-core decode instantiation (the kernel
