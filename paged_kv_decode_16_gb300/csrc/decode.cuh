@@ -128,7 +128,6 @@ decode_kernel(const DecodeParams p) {
     __syncwarp();
     // the plan (previous kernel of the stream) must be complete from here on
     pdl_wait();
-    pdl_trigger();
 
     const int nw = p.hdr->num_workers;
     const int gw = blockIdx.x * WARPS + warp;
@@ -371,6 +370,10 @@ decode_kernel(const DecodeParams p) {
         // refill: positions up to i + STAGES (stage i % STAGES is free again)
         while (issued <= i + STAGES && issue(issued)) ++issued;
     }
+    // the next kernel (combine, or the prefix pass) may launch once every CTA
+    // has a warp past its chunk stream: earlier, its CTAs only wait beside
+    // these (measured slower, cold and warm)
+    pdl_trigger();
     if (npend > 0)
         finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, lane);
 }

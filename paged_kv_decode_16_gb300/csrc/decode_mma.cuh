@@ -151,7 +151,6 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
     }
     __syncwarp();
     pdl_wait();
-    pdl_trigger();
 
     const int nw = p.hdr->num_workers;
     const int gw = blockIdx.x * WARPS + warp;
@@ -525,6 +524,10 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
         // refill: positions up to i + STAGES (stage i % STAGES is free again)
         while (issued <= i + STAGES && issue(issued)) ++issued;
     }
+    // the next kernel (combine, or the prefix pass) may launch once every CTA
+    // has a warp past its chunk stream: earlier, its CTAs only wait beside
+    // these (measured slower, cold and warm)
+    pdl_trigger();
     if (npend > 0)
         finish_pending<T, D, GS>(p, npend, pend0, pend1, ws.sw, ws.r, lane);
 }
