@@ -67,7 +67,7 @@ constexpr int kColS = 64;              // tensor memory: S^T of block i in [64 (
 constexpr int kColO = 128;             // O^T in [128, 128 + N)
 constexpr int kTmemCols = 256;
 
-// A block as warp 0 described it (shared memory, one per stage).
+// A block as the producer warp described it (shared memory, one per stage).
 struct BlockDesc {
     int u;          // unit
     int k0;         // first chunk of the block within the unit
@@ -97,9 +97,11 @@ struct UmmaLayout {
     static constexpr int kQSlot = 2 * kRowBlock;
     static constexpr int kDesc = kQ + kQSlots * kQSlot;
     static constexpr int kRed = kDesc + STAGES * (int)sizeof(BlockDesc);   // [4][N] floats
-    static constexpr int kRowM = kRed + 4 * N * 4;        // running maximum per row
-    static constexpr int kRowRef = kRowM + N * 4;         // the block's reference maximum
-    static constexpr int kRowAlpha = kRowRef + N * 4;     // rescale factor of the block
+    // each row's reference maximum (the running maximum of the blocks that moved it)
+    static constexpr int kRowRef = kRed + 4 * N * 4;
+    // each row's rescale factor in a block that moved the reference; at a
+    // segment end, each row's sum of weights
+    static constexpr int kRowAlpha = kRowRef + N * 4;
     // barriers: full[STAGES], empty[STAGES], S done[2], S read[2], P ready, P V done, drain
     static constexpr int kBar = (kRowAlpha + N * 4 + 15) / 16 * 16;
     static constexpr int kTmemSlot = kBar + (2 * STAGES + 7) * 8;  // then the issued count
@@ -110,7 +112,7 @@ struct UmmaLayout {
 // regions for STAGES = 3), else two.
 template <int N>
 constexpr int umma_stages() {
-    return 3 * 4 * kBlkTok * 128 + 4 * 2 * N * 128 + 3 * (int)sizeof(BlockDesc) + 7 * N * 4 +
+    return 3 * 4 * kBlkTok * 128 + 4 * 2 * N * 128 + 3 * (int)sizeof(BlockDesc) + 6 * N * 4 +
                        16 + 13 * 8 + 16 + 1024 <=
                    227 * 1024
                ? 3
@@ -174,7 +176,6 @@ decode_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap qma
     const uint32_t sb = raw + pad;
     BlockDesc* desc = reinterpret_cast<BlockDesc*>(base + Lay::kDesc);
     float* red = reinterpret_cast<float*>(base + Lay::kRed);
-    float* row_m = reinterpret_cast<float*>(base + Lay::kRowM);
     float* row_ref = reinterpret_cast<float*>(base + Lay::kRowRef);
     float* row_alpha = reinterpret_cast<float*>(base + Lay::kRowAlpha);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + Lay::kBar);  // copies of a stage landed
@@ -221,7 +222,6 @@ decode_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap qma
     const uint32_t tmem = *tmem_slot;
 
     pdl_wait();
-    pdl_trigger();
 
     const int gw = blockIdx.x;
     const int units_per_b = p.n_kv_heads * p.sub_groups;
@@ -615,6 +615,7 @@ decode_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap qma
                 break;
             }
         }
+        pdl_trigger();  // the combine may launch once every CTA's consumers are done
         if (cons_sync_or(local_fail)) failed = 1;
         if (failed && tid == 0) set_status(p.status, PKV_DEV_TIMEOUT);
         if (tid == 0) issued_slot[1] = failed ? consumed : -1;
