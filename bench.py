@@ -579,8 +579,8 @@ def run_ours(args):
 
     # An untimed read of twice the L2 size (a read, not a write: dirty lines
     # would be written back inside the next timed region) before each run of
-    # flushed_ms.  Used for the decode kernel's roofline timing and for a
-    # second figure of the step: no run finds anything of its own in L2.
+    # flushed_ms and before each flushed decode launch: second figures of the
+    # step and of the decode kernel, where no run finds anything of its own in L2.
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def flushed_ms(fn, n):
@@ -741,17 +741,24 @@ def run_ours(args):
             "device_status": pkv.pkv_read_device_status(ws2)}
         del w2, t2, l2, p2, o2, ws2
 
-    # ---- the decode kernel alone: events around its launch on its stream ----
+    # ---- the decode kernel alone: events around its launch on its stream,
+    # in steps run back to back as in the timed region (the roofline), and
+    # each after an L2 flush (reported beside it) ----
     KD = max(1, min(K, 2000))
-    dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
-    dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
-    torch.cuda.synchronize()
-    for i in range(KD):
-        flush.amax()
-        split_step(dec0[i], dec1[i])
-    torch.cuda.synchronize()
-    dec_ms = [a.elapsed_time(b) for a, b in zip(dec0, dec1)]
-    dec_avg = statistics.mean(dec_ms)
+
+    def decode_ms(flushed):
+        dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
+        dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(KD)]
+        torch.cuda.synchronize()
+        for i in range(KD):
+            if flushed:
+                flush.amax()
+            split_step(dec0[i], dec1[i])
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in zip(dec0, dec1))
+
+    dec_avg = decode_ms(False)
+    dec_avg_flushed = decode_ms(True)
 
     # ---- end to end through host buffers (pinned), one sync per step ----
     # The step's inputs travel as one packed pinned buffer (one host->device
@@ -847,8 +854,9 @@ def run_ours(args):
                      if var == pkv.VARIANT_CUDA_CORES else "pkv::decode_mma_kernel (tensor cores)",
                      "algorithmic_bytes": by["decode"],
                      "timing": f"CUDA events around paged_decode_run on its stream, mean of "
-                               f"{KD} steps run right after the timed region, L2 flushed "
-                               f"before each"},
+                               f"{KD} steps run back to back right after the timed region",
+                     "decode_kernel_ms_l2_flushed": dec_avg_flushed,
+                     "frac_l2_flushed": by["decode"] / (dec_avg_flushed * 1e-3) / 1e9 / peak},
         "e2e": {"value": aggregate_gbs(world, by["step"], e2e_ms), "unit": UNIT,
                 "mode": "CUDA graph replay per step: packed pinned inputs in, "
                         "paged_decode_step, output out, then a host sync",
