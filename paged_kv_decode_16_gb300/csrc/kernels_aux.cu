@@ -458,7 +458,7 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     pdl_wait();
     pdl_trigger();
     const SlotSegs sg{partials, segs.base, partial_slot_floats(gs, D), gs, D};
-    merge_rows<T, D>(sg, ns, rs.rows(sgi), threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+    merge_rows_cta<T, D>(sg, ns, rs.rows(sgi), threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
                      [&](int g) { return out + rs.row(b, h, sgi, g) * D; });
 }
 
@@ -518,7 +518,7 @@ cascade_combine_kernel(CascadeArgs c) {
         const CascadeSegs<TileSegs> sg{
             TileSegs{c.v_partials, (long long)(h * c.v_tiles + t) * c.v_splits, D}, ro,
             c.v_splits, suf};
-        merge_rows<T, D>(sg, c.v_splits + ns, gs, threadIdx.x >> 5, kCombineWarps,
+        merge_rows_cta<T, D>(sg, c.v_splits + ns, gs, threadIdx.x >> 5, kCombineWarps,
                          threadIdx.x & 31, [&](int g) { return o + (long long)g * D; });
     } else {
         // the virtual unit holding this unit's rows
@@ -531,7 +531,7 @@ cascade_combine_kernel(CascadeArgs c) {
         const CascadeSegs<SlotSegs> sg{
             SlotSegs{c.v_partials, pv.base, partial_slot_floats(c.v_gs, D), c.v_gs, D}, ro, np,
             suf};
-        merge_rows<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+        merge_rows_cta<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
                          [&](int g) { return o + (long long)g * D; });
     }
 }

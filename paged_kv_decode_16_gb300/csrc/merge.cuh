@@ -103,9 +103,13 @@ __device__ __forceinline__ MergeRow merge_row(const Segs& sg, int ns, int g, int
         wl = merge_weight(m, M);
         den = fmaf(wl, l, 0.f);
     } else {
+        // (unrolled: the loads of several segments go out before the first
+        // use; each lane's operations stay in segment order)
+#pragma unroll 8
         for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(sg.m(s, g)));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+#pragma unroll 8
         for (int s = lane; s < ns; s += 32)
             den = fmaf(merge_weight(__ldcg(sg.m(s, g)), M), __ldcg(sg.l(s, g)), den);
     }
@@ -124,14 +128,73 @@ __device__ __forceinline__ void merge_store(const float4& acc, float den, int d4
     *reinterpret_cast<uint2*>(out_row + d4 * 4) = w2;
 }
 
+// Rows of more than 32 segments (one sequence split over many workers): pass
+// 2 sums the o vectors of groups of kMergeGroup segments -- each group in
+// segment order -- and adds the groups into kMergeSlots slots (slot j takes
+// groups j, j + kMergeSlots, ...), then the slots in order, starting from 0.
+// A combine CTA of kMergeSlots warps gives each slot its own warp (a group's
+// loads all in flight); a single warp walks the slots itself, in the same
+// order, so both give the same bits.
+constexpr int kMergeGroup = 16;
+constexpr int kMergeSlots = 8;
+
+// Slot j of row g: its groups' weighted sums, added in order.
+template <int D, class Segs>
+__device__ __forceinline__ float4 merge_slot(const Segs& sg, int ns, int g, float M, int slot,
+                                             int lane) {
+    const bool act = lane < D / 4;
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int grp = slot; grp * kMergeGroup < ns; grp += kMergeSlots) {
+        const int s0 = grp * kMergeGroup;
+        float4 v[kMergeGroup];
+        float w[kMergeGroup];
+#pragma unroll
+        for (int j = 0; j < kMergeGroup; ++j) {
+            const int s = s0 + j;
+            v[j] = act && s < ns ? __ldcg(sg.o4(s, g, lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            w[j] = s < ns ? merge_weight(__ldcg(sg.m(s, g)), M) : 0.f;
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kMergeGroup; ++j) {
+            if (s0 + j >= ns) break;
+            acc.x = fmaf(w[j], v[j].x, acc.x);
+            acc.y = fmaf(w[j], v[j].y, acc.y);
+            acc.z = fmaf(w[j], v[j].z, acc.z);
+            acc.w = fmaf(w[j], v[j].w, acc.w);
+        }
+        part.x += acc.x;
+        part.y += acc.y;
+        part.z += acc.z;
+        part.w += acc.w;
+    }
+    return part;
+}
+
 // Merge rows [0, nrows) of a unit with the warps of a CTA (warp w of nwarps
 // takes rows w, w + nwarps, ...); out_rows(g) gives row g's output.  Pass 2:
-// lane t sums output vector t of the row, sum_s w_s o_s in segment order.
+// lane t sums output vector t of the row, sum_s w_s o_s in segment order (up
+// to 32 segments), or in the grouped order above, a warp walking the slots.
 template <typename T, int D, class Segs, class RowOut>
 __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, int warp, int nwarps,
                                            int lane, const RowOut& out_rows) {
     constexpr int Q = D / 4;  // output vectors per row
     static_assert(Q <= 32, "one vector per lane");
+    if (ns > 32) {
+        for (int g = warp; g < nrows; g += nwarps) {
+            const MergeRow mr = merge_row(sg, ns, g, lane);
+            float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < kMergeSlots; ++j) {
+                const float4 q = merge_slot<D>(sg, ns, g, mr.M, j, lane);
+                total.x += q.x;
+                total.y += q.y;
+                total.z += q.z;
+                total.w += q.w;
+            }
+            if (lane < Q) merge_store<T, D>(total, mr.den, lane, out_rows(g));
+        }
+        return;
+    }
     for (int g = warp; g < nrows; g += nwarps) {
         const MergeRow mr = merge_row(sg, ns, g, lane);
         const bool act = lane < Q;
@@ -147,9 +210,7 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
                 v[j] = act && s < ns
                            ? __ldcg(sg.o4(s, g, lane))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                w[j] = s >= ns ? 0.f
-                       : ns <= 32 ? __shfl_sync(kFull, mr.w, s & 31)
-                                  : merge_weight(__ldcg(sg.m(s, g)), mr.M);
+                w[j] = s >= ns ? 0.f : __shfl_sync(kFull, mr.w, s & 31);
             }
 #pragma unroll
             for (int j = 0; j < kMergeBlock; ++j) {
@@ -161,6 +222,37 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
             }
         }
         if (act) merge_store<T, D>(x, mr.den, lane, out_rows(g));
+    }
+}
+
+// merge_rows for a combine CTA of kMergeSlots warps (every warp calls it):
+// rows of more than 32 segments are taken one after another, warp j summing
+// slot j, warp 0 adding the slots in order -- merge_rows' bits.
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows_cta(const Segs& sg, int ns, int nrows, int warp,
+                                               int nwarps, int lane, const RowOut& out_rows) {
+    if (ns <= 32 || nwarps != kMergeSlots) {
+        merge_rows<T, D>(sg, ns, nrows, warp, nwarps, lane, out_rows);
+        return;
+    }
+    __shared__ float4 s_part[kMergeSlots][32];
+    for (int g = 0; g < nrows; ++g) {
+        const MergeRow mr = merge_row(sg, ns, g, lane);
+        s_part[warp][lane] = merge_slot<D>(sg, ns, g, mr.M, warp, lane);
+        __syncthreads();
+        if (warp == 0) {
+            float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kMergeSlots; ++j) {
+                const float4 q = s_part[j][lane];
+                total.x += q.x;
+                total.y += q.y;
+                total.z += q.z;
+                total.w += q.w;
+            }
+            if (lane < D / 4) merge_store<T, D>(total, mr.den, lane, out_rows(g));
+        }
+        __syncthreads();
     }
 }
 
