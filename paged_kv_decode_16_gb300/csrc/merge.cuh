@@ -226,8 +226,10 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
 }
 
 // merge_rows for a combine CTA of kMergeSlots warps (every warp calls it):
-// rows of more than 32 segments are taken one after another, warp j summing
-// slot j, warp 0 adding the slots in order -- merge_rows' bits.
+// rows of more than 32 segments are taken kCtaRows at a time -- warps
+// 0 .. kCtaRows-1 find the rows' maxima and denominators, then every warp sums
+// (row, slot) items (item i: row i / kMergeSlots, slot i % kMergeSlots), then
+// warp r adds row r's slots in order -- merge_rows' bits.
 template <typename T, int D, class Segs, class RowOut>
 __device__ __forceinline__ void merge_rows_cta(const Segs& sg, int ns, int nrows, int warp,
                                                int nwarps, int lane, const RowOut& out_rows) {
@@ -235,22 +237,35 @@ __device__ __forceinline__ void merge_rows_cta(const Segs& sg, int ns, int nrows
         merge_rows<T, D>(sg, ns, nrows, warp, nwarps, lane, out_rows);
         return;
     }
-    __shared__ float4 s_part[kMergeSlots][32];
-    for (int g = 0; g < nrows; ++g) {
-        const MergeRow mr = merge_row(sg, ns, g, lane);
-        s_part[warp][lane] = merge_slot<D>(sg, ns, g, mr.M, warp, lane);
+    constexpr int kCtaRows = 4;
+    __shared__ float4 s_part[kCtaRows][kMergeSlots][32];
+    __shared__ float s_M[kCtaRows], s_den[kCtaRows];
+    for (int g0 = 0; g0 < nrows; g0 += kCtaRows) {
+        const int rb = min(kCtaRows, nrows - g0);
+        if (warp < rb) {
+            const MergeRow mr = merge_row(sg, ns, g0 + warp, lane);
+            if (lane == 0) {
+                s_M[warp] = mr.M;
+                s_den[warp] = mr.den;
+            }
+        }
         __syncthreads();
-        if (warp == 0) {
+        for (int it = warp; it < rb * kMergeSlots; it += kMergeSlots) {
+            const int r = it / kMergeSlots, j = it - r * kMergeSlots;
+            s_part[r][j][lane] = merge_slot<D>(sg, ns, g0 + r, s_M[r], j, lane);
+        }
+        __syncthreads();
+        if (warp < rb) {
             float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < kMergeSlots; ++j) {
-                const float4 q = s_part[j][lane];
+                const float4 q = s_part[warp][j][lane];
                 total.x += q.x;
                 total.y += q.y;
                 total.z += q.z;
                 total.w += q.w;
             }
-            if (lane < D / 4) merge_store<T, D>(total, mr.den, lane, out_rows(g));
+            if (lane < D / 4) merge_store<T, D>(total, s_den[warp], lane, out_rows(g0 + warp));
         }
         __syncthreads();
     }
