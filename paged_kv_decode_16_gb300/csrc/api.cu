@@ -500,7 +500,7 @@ pkv_status do_combine(int batch, int n_q_heads, int head_dim, pkv_dtype dtype, v
         dtype, head_dim, reinterpret_cast<const float*>(ws + s.ws.partials),
         reinterpret_cast<const int32_t*>(ws + s.ws.prefix),
         reinterpret_cast<const int32_t*>(ws + s.ws.lens_eff), reinterpret_cast<const WsHeader*>(ws),
-        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.rs, stream));
+        out, (int)s.units, s.units_per_b, s.sub_groups, s.gs, s.rs, s.workers, stream));
 }
 
 // --- fixed device scratch for paged_decode_attention_no_alloc -------------

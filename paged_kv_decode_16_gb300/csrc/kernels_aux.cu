@@ -427,10 +427,12 @@ cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
 }
 
 // ---------------------------------------------------------------------------
-// Combine: one CTA per unit (sequence, KV head, sub-group); units finished by
-// a single worker and empty sequences exit at once.  Each warp merges rows of
-// the unit with merge_rows (the decode kernels' own merge does the same
-// arithmetic, several rows per warp).
+// Combine: one CTA per unit (sequence, KV head, sub-group), or per (unit,
+// row) when units are few beside the workers (row_split > 1: a long sequence
+// in a small batch, whose units have many segments); units finished by a
+// single worker and empty sequences exit at once.  The warps merge the rows
+// with merge_rows_cta (the decode kernels' own merge does the same arithmetic
+// per row, whichever CTA takes the row).
 // ---------------------------------------------------------------------------
 constexpr int kCombineWarps = 8;
 
@@ -438,11 +440,13 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ prefix,
                const int32_t* __restrict__ lens_eff, const WsHeader* __restrict__ hdr,
-               T* __restrict__ out, int units_per_b, int sub_groups, int gs, RowShape rs) {
+               T* __restrict__ out, int units_per_b, int sub_groups, int gs, RowShape rs,
+               int row_split) {
     // Everything up to pdl_wait reads only what the plan wrote: the plan grid
     // completed before any decode CTA passed its own wait and let this
     // kernel launch.  The partial states are read after the wait.
-    const int u = blockIdx.x;
+    const int u = blockIdx.x / row_split;
+    const int part = blockIdx.x - u * row_split;  // row_split > 1: this CTA's row
     const int b = u / units_per_b;
     const int uidx = u - b * units_per_b;
     const int h = uidx / sub_groups;
@@ -455,11 +459,19 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
         unit_segments(hdr->chunks_per_worker, hdr->extra_chunks, u, prefix[b] + uidx * nch, nch);
     const int ns = segs.count();
     if (ns <= 1) return;  // finished in place by its worker
+    const int nrows = rs.rows(sgi);
+    if (row_split > 1 && part >= nrows) return;
     pdl_wait();
     pdl_trigger();
     const SlotSegs sg{partials, segs.base, partial_slot_floats(gs, D), gs, D};
-    merge_rows_cta<T, D>(sg, ns, rs.rows(sgi), threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
-                     [&](int g) { return out + rs.row(b, h, sgi, g) * D; });
+    if (row_split > 1) {
+        const RowShift<SlotSegs> one{sg, part};
+        merge_rows_cta<T, D>(one, ns, 1, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+                             [&](int) { return out + rs.row(b, h, sgi, part) * D; });
+    } else {
+        merge_rows_cta<T, D>(sg, ns, nrows, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+                             [&](int g) { return out + rs.row(b, h, sgi, g) * D; });
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -664,12 +676,15 @@ cudaError_t launch_cascade_plan(const PlanArgs& ps, const PlanArgs& pv, const Ca
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           const RowShape& rs, cudaStream_t stream) {
+                           const RowShape& rs, int workers, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
-#define PKV_COMBINE(T, D)                                                                     \
-    return launch_pdl(combine_kernel<T, D>, dim3(units), dim3(kCombineWarps * 32), 0, stream, \
-                      partials, prefix, lens_eff, hdr, static_cast<T*>(out), units_per_b,     \
-                      sub_groups, gs, rs)
+    // few units beside the workers: their rows have many segments each, so a
+    // CTA per (unit, row)
+    const int row_split = (long long)units * 32 < workers ? gs : 1;
+#define PKV_COMBINE(T, D)                                                                   \
+    return launch_pdl(combine_kernel<T, D>, dim3(units * row_split), dim3(kCombineWarps * 32), \
+                      0, stream, partials, prefix, lens_eff, hdr, static_cast<T*>(out),     \
+                      units_per_b, sub_groups, gs, rs, row_split)
     if (dtype == PKV_BF16) {
         if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128);
         PKV_COMBINE(__nv_bfloat16, 64);

@@ -66,7 +66,7 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,
                            void* out, int units, int units_per_b, int sub_groups, int gs,
-                           const RowShape& rs, cudaStream_t stream);
+                           const RowShape& rs, int workers, cudaStream_t stream);
 
 // batches up to this size keep their chunk prefix sums in the plan's shared memory
 constexpr int kPlanSmemSeqs = 4096;

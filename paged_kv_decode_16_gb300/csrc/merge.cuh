@@ -75,6 +75,18 @@ struct TileSegs {
     __device__ __forceinline__ const float* l(int s, int g) const { return m(s, g) + kRows; }
 };
 
+// Row r + off of Segs as row r (one row of a unit merged on its own).
+template <class Segs>
+struct RowShift {
+    const Segs& sg;
+    int off;
+    __device__ __forceinline__ const float4* o4(int s, int g, int v) const {
+        return sg.o4(s, g + off, v);
+    }
+    __device__ __forceinline__ const float* m(int s, int g) const { return sg.m(s, g + off); }
+    __device__ __forceinline__ const float* l(int s, int g) const { return sg.l(s, g + off); }
+};
+
 constexpr int kMergeBlock = 8;  // segments whose loads are in flight together
 
 struct MergeRow {
