@@ -435,6 +435,7 @@ cascade_plan_kernel(PlanArgs ps, PlanArgs pv, CascadeGather g, int k) {
 // per row, whichever CTA takes the row).
 // ---------------------------------------------------------------------------
 constexpr int kCombineWarps = 8;
+static_assert(kCombineWarps == kMergeSlots, "a combine warp per merge slot");
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
@@ -466,10 +467,10 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
     const SlotSegs sg{partials, segs.base, partial_slot_floats(gs, D), gs, D};
     if (row_split > 1) {
         const RowShift<SlotSegs> one{sg, part};
-        merge_rows_cta<T, D>(one, ns, 1, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+        merge_rows_cta<T, D>(one, ns, 1, threadIdx.x >> 5, threadIdx.x & 31,
                              [&](int) { return out + rs.row(b, h, sgi, part) * D; });
     } else {
-        merge_rows_cta<T, D>(sg, ns, nrows, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+        merge_rows_cta<T, D>(sg, ns, nrows, threadIdx.x >> 5, threadIdx.x & 31,
                              [&](int g) { return out + rs.row(b, h, sgi, g) * D; });
     }
 }
@@ -482,7 +483,7 @@ combine_kernel(const float* __restrict__ partials, const int32_t* __restrict__ p
 // ran each sequence's own tokens.  Both left only partial states.  One CTA per
 // real unit (sequence, KV head, sub-group of gs rows): its rows sit at rows
 // ro .. ro+gs-1 of one tile or virtual unit (gs divides both).  The prefix
-// segments, then the suffix segments, are merged as one list with merge_rows.
+// segments, then the suffix segments, are merged as one list with merge_rows_seq.
 // ---------------------------------------------------------------------------
 template <class Pre>
 struct CascadeSegs {
@@ -530,8 +531,8 @@ cascade_combine_kernel(CascadeArgs c) {
         const CascadeSegs<TileSegs> sg{
             TileSegs{c.v_partials, (long long)(h * c.v_tiles + t) * c.v_splits, D}, ro,
             c.v_splits, suf};
-        merge_rows_cta<T, D>(sg, c.v_splits + ns, gs, threadIdx.x >> 5, kCombineWarps,
-                         threadIdx.x & 31, [&](int g) { return o + (long long)g * D; });
+        merge_rows_seq<T, D>(sg, c.v_splits + ns, gs, threadIdx.x >> 5, kCombineWarps,
+                             threadIdx.x & 31, [&](int g) { return o + (long long)g * D; });
     } else {
         // the virtual unit holding this unit's rows
         const int vu = h * c.v_sub + r0 / c.v_gs, ro = r0 % c.v_gs;
@@ -543,8 +544,8 @@ cascade_combine_kernel(CascadeArgs c) {
         const CascadeSegs<SlotSegs> sg{
             SlotSegs{c.v_partials, pv.base, partial_slot_floats(c.v_gs, D), c.v_gs, D}, ro, np,
             suf};
-        merge_rows_cta<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
-                         [&](int g) { return o + (long long)g * D; });
+        merge_rows_seq<T, D>(sg, np + ns, gs, threadIdx.x >> 5, kCombineWarps, threadIdx.x & 31,
+                             [&](int g) { return o + (long long)g * D; });
     }
 }
 

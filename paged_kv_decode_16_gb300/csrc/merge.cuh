@@ -103,7 +103,7 @@ __device__ __forceinline__ float merge_weight(float m, float M) {
 // to 32 segments lane t holds segment t's m and l (one round of loads) and
 // keeps its weight for pass 2; beyond, lane t walks segments t, t+32, ...
 // twice.  Both give the same sums: lane t adds its segments' w_s l_s in order.
-template <class Segs>
+template <bool kUnroll = true, class Segs>
 __device__ __forceinline__ MergeRow merge_row(const Segs& sg, int ns, int g, int lane) {
     float M = -INFINITY, den = 0.f, wl = 0.f;
     if (ns <= 32) {
@@ -115,15 +115,26 @@ __device__ __forceinline__ MergeRow merge_row(const Segs& sg, int ns, int g, int
         wl = merge_weight(m, M);
         den = fmaf(wl, l, 0.f);
     } else {
-        // (unrolled: the loads of several segments go out before the first
-        // use; each lane's operations stay in segment order)
+        // kUnroll: unrolled 8 times, so that the loads of several segments go
+        // out before the first use; else the compiler's choice (measured 1 us
+        // faster in the shared-prefix merge, whose rows rarely have more than
+        // 32 segments).  Each lane's operations stay in segment order.
+        if constexpr (kUnroll) {
 #pragma unroll 8
-        for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(sg.m(s, g)));
+            for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(sg.m(s, g)));
+        } else {
+            for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(sg.m(s, g)));
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        if constexpr (kUnroll) {
 #pragma unroll 8
-        for (int s = lane; s < ns; s += 32)
-            den = fmaf(merge_weight(__ldcg(sg.m(s, g)), M), __ldcg(sg.l(s, g)), den);
+            for (int s = lane; s < ns; s += 32)
+                den = fmaf(merge_weight(__ldcg(sg.m(s, g)), M), __ldcg(sg.l(s, g)), den);
+        } else {
+            for (int s = lane; s < ns; s += 32)
+                den = fmaf(merge_weight(__ldcg(sg.m(s, g)), M), __ldcg(sg.l(s, g)), den);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
@@ -183,30 +194,50 @@ __device__ __forceinline__ float4 merge_slot(const Segs& sg, int ns, int g, floa
     return part;
 }
 
-// Merge rows [0, nrows) of a unit with the warps of a CTA (warp w of nwarps
-// takes rows w, w + nwarps, ...); out_rows(g) gives row g's output.  Pass 2:
-// lane t sums output vector t of the row, sum_s w_s o_s in segment order (up
-// to 32 segments), or in the grouped order above, a warp walking the slots.
-template <typename T, int D, class Segs, class RowOut>
-__device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, int warp, int nwarps,
-                                           int lane, const RowOut& out_rows) {
-    constexpr int Q = D / 4;  // output vectors per row
-    static_assert(Q <= 32, "one vector per lane");
-    if (ns > 32) {
-        for (int g = warp; g < nrows; g += nwarps) {
-            const MergeRow mr = merge_row(sg, ns, g, lane);
-            float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < kMergeSlots; ++j) {
-                const float4 q = merge_slot<D>(sg, ns, g, mr.M, j, lane);
-                total.x += q.x;
-                total.y += q.y;
-                total.z += q.z;
-                total.w += q.w;
+// merge_slot with a group's loads in two halves (8 in flight): the same
+// multiply-adds in the same order, so the same bits, with fewer registers
+// (the combine kernels' occupancy).
+template <int D, class Segs>
+__device__ __forceinline__ float4 merge_slot_lean(const Segs& sg, int ns, int g, float M,
+                                                  int slot, int lane) {
+    constexpr int H = kMergeGroup / 2;
+    const bool act = lane < D / 4;
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int grp = slot; grp * kMergeGroup < ns; grp += kMergeSlots) {
+        const int s0 = grp * kMergeGroup;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float4 v[H];
+            float w[H];
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const int s = s0 + hh * H + j;
+                v[j] = act && s < ns ? __ldcg(sg.o4(s, g, lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                w[j] = s < ns ? merge_weight(__ldcg(sg.m(s, g)), M) : 0.f;
             }
-            if (lane < Q) merge_store<T, D>(total, mr.den, lane, out_rows(g));
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                if (s0 + hh * H + j >= ns) break;
+                acc.x = fmaf(w[j], v[j].x, acc.x);
+                acc.y = fmaf(w[j], v[j].y, acc.y);
+                acc.z = fmaf(w[j], v[j].z, acc.z);
+                acc.w = fmaf(w[j], v[j].w, acc.w);
+            }
         }
-        return;
+        part.x += acc.x;
+        part.y += acc.y;
+        part.z += acc.z;
+        part.w += acc.w;
     }
+    return part;
+}
+
+// merge_rows' pass 2 for up to 32 segments: segment order, loads in blocks.
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows_upto32(const Segs& sg, int ns, int nrows, int warp,
+                                                  int nwarps, int lane, const RowOut& out_rows) {
+    constexpr int Q = D / 4;
     for (int g = warp; g < nrows; g += nwarps) {
         const MergeRow mr = merge_row(sg, ns, g, lane);
         const bool act = lane < Q;
@@ -237,6 +268,69 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
     }
 }
 
+// Merge rows [0, nrows) of a unit with the warps of a CTA (warp w of nwarps
+// takes rows w, w + nwarps, ...); out_rows(g) gives row g's output.  Pass 2:
+// lane t sums output vector t of the row, sum_s w_s o_s in segment order (up
+// to 32 segments), or in the grouped order above, a warp walking the slots.
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, int warp, int nwarps,
+                                           int lane, const RowOut& out_rows) {
+    constexpr int Q = D / 4;  // output vectors per row
+    static_assert(Q <= 32, "one vector per lane");
+    if (ns > 32) {
+        for (int g = warp; g < nrows; g += nwarps) {
+            const MergeRow mr = merge_row(sg, ns, g, lane);
+            float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < kMergeSlots; ++j) {
+                const float4 q = merge_slot<D>(sg, ns, g, mr.M, j, lane);
+                total.x += q.x;
+                total.y += q.y;
+                total.z += q.z;
+                total.w += q.w;
+            }
+            if (lane < Q) merge_store<T, D>(total, mr.den, lane, out_rows(g));
+        }
+        return;
+    }
+    merge_rows_upto32<T, D>(sg, ns, nrows, warp, nwarps, lane, out_rows);
+}
+
+// Merge rows [0, nrows) in segment order for any segment count (warp w of
+// nwarps takes rows w, w + nwarps, ...; beyond 32 segments each weight comes
+// from its own load).  For a merge whose bits no other path has to match (the
+// shared-prefix call's): it keeps that kernel's register count.
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows_seq(const Segs& sg, int ns, int nrows, int warp,
+                                               int nwarps, int lane, const RowOut& out_rows) {
+    constexpr int Q = D / 4;
+    for (int g = warp; g < nrows; g += nwarps) {
+        const MergeRow mr = merge_row<false>(sg, ns, g, lane);
+        const bool act = lane < Q;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < ns; s0 += kMergeBlock) {
+            float4 v[kMergeBlock];
+            float w[kMergeBlock];
+#pragma unroll
+            for (int j = 0; j < kMergeBlock; ++j) {
+                const int s = s0 + j;
+                v[j] = act && s < ns ? __ldcg(sg.o4(s, g, lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                w[j] = s >= ns ? 0.f
+                       : ns <= 32 ? __shfl_sync(kFull, mr.w, s & 31)
+                                  : merge_weight(__ldcg(sg.m(s, g)), mr.M);
+            }
+#pragma unroll
+            for (int j = 0; j < kMergeBlock; ++j) {
+                if (s0 + j >= ns) break;
+                x.x = fmaf(w[j], v[j].x, x.x);
+                x.y = fmaf(w[j], v[j].y, x.y);
+                x.z = fmaf(w[j], v[j].z, x.z);
+                x.w = fmaf(w[j], v[j].w, x.w);
+            }
+        }
+        if (act) merge_store<T, D>(x, mr.den, lane, out_rows(g));
+    }
+}
+
 // merge_rows for a combine CTA of kMergeSlots warps (every warp calls it):
 // rows of more than 32 segments are taken kCtaRows at a time -- warps
 // 0 .. kCtaRows-1 find the rows' maxima and denominators, then every warp sums
@@ -244,12 +338,12 @@ __device__ __forceinline__ void merge_rows(const Segs& sg, int ns, int nrows, in
 // warp r adds row r's slots in order -- merge_rows' bits.
 template <typename T, int D, class Segs, class RowOut>
 __device__ __forceinline__ void merge_rows_cta(const Segs& sg, int ns, int nrows, int warp,
-                                               int nwarps, int lane, const RowOut& out_rows) {
-    if (ns <= 32 || nwarps != kMergeSlots) {
-        merge_rows<T, D>(sg, ns, nrows, warp, nwarps, lane, out_rows);
+                                               int lane, const RowOut& out_rows) {
+    if (ns <= 32) {
+        merge_rows_upto32<T, D>(sg, ns, nrows, warp, kMergeSlots, lane, out_rows);
         return;
     }
-    constexpr int kCtaRows = 4;
+    constexpr int kCtaRows = 2;
     __shared__ float4 s_part[kCtaRows][kMergeSlots][32];
     __shared__ float s_M[kCtaRows], s_den[kCtaRows];
     for (int g0 = 0; g0 < nrows; g0 += kCtaRows) {
@@ -264,7 +358,7 @@ __device__ __forceinline__ void merge_rows_cta(const Segs& sg, int ns, int nrows
         __syncthreads();
         for (int it = warp; it < rb * kMergeSlots; it += kMergeSlots) {
             const int r = it / kMergeSlots, j = it - r * kMergeSlots;
-            s_part[r][j][lane] = merge_slot<D>(sg, ns, g0 + r, s_M[r], j, lane);
+            s_part[r][j][lane] = merge_slot_lean<D>(sg, ns, g0 + r, s_M[r], j, lane);
         }
         __syncthreads();
         if (warp < rb) {
