@@ -12,10 +12,13 @@ through the C ABI (three kernel launches on one CUDA stream).
 value      = algorithmic bytes of the step / device time of the step, GB/s:
              unique K+V bytes read + q read + out written + append bytes
              (k_new/v_new read and written into the pool).
-e2e        = the same metric through paged_decode_step with
-             the step's inputs (q, k_new, v_new, page table, lengths,
-             positions) copied from pinned host memory each step and the
-             output copied back, all inside the timed region.
+e2e        = the same metric through paged_decode_step_host: the step's
+             inputs (q, k_new, v_new, page table, lengths, positions) in
+             pinned host memory, read by the kernels across the host-device
+             link each step, and the output stored into pinned host memory,
+             all inside the timed region (with a host sync per step);
+             e2e.copy_engine: the same with copy-engine copies in and out
+             around paged_decode_step.
 roofline   = the decode kernel alone: its algorithmic bytes (K+V+q+out) over
              its duration (CUDA events around paged_decode_run on its stream,
              in a second region of the same steps issued as separate calls),
@@ -761,10 +764,57 @@ def run_ours(args):
     dec_avg_flushed = decode_ms(True)
 
     # ---- end to end through host buffers (pinned), one sync per step ----
-    # The step's inputs travel as one packed pinned buffer (one host->device
-    # copy per step, as a serving loop would batch them); the result comes back
-    # with one device->host copy.
+    # paged_decode_step_host: the step's inputs sit in pinned host memory and
+    # its kernels read them (and store the result into pinned host memory)
+    # across the host-device link themselves.  Beside it, the same step with
+    # copy-engine copies: the inputs as one packed pinned buffer copied in,
+    # paged_decode_step, the output copied out.  Each is recorded once into a
+    # CUDA graph; a step replays it and waits for the result.
+    def graph_of(body):
+        body()
+        torch.cuda.synchronize()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                body()
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        return g
+
+    KE = max(1, min(args.e2e_steps, K))
+
+    def e2e_time(g):
+        def e2e_step():
+            g.replay()
+            torch.cuda.current_stream(dev).synchronize()
+        for _ in range(10):
+            e2e_step()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(KE):
+            e2e_step()
+        return max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / KE, dev)
+
     srcs = [w.q, w.k_new, w.v_new, table, lens, pos]
+    pinned = [t.detach().cpu().contiguous().pin_memory() for t in srcs]
+    q_h, kn_h, vn_h, tb_h, ln_h, ps_h = pinned
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    ws_host = pkv.alloc_step_host_workspace(B, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                            table.shape[1], nw, device=dev, variant=var)
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = out.numel() * out.element_size()
+
+    def e2e_host_body():
+        pkv.paged_decode_step_host(kn_h, vn_h, ps_h, q_h, w.k_pool, w.v_pool, tb_h, ln_h, w.scale,
+                                   out_h, ws_host, nw, variant=var)
+
+    e2e_ms = e2e_time(graph_of(e2e_host_body))
+    host_status = pkv.pkv_read_device_status(ws_host)
+
     offs, total = [], 0
     for t in srcs:
         offs.append(total)
@@ -777,44 +827,15 @@ def run_ours(args):
         in_h[o:o + nb].copy_(t.detach().cpu().reshape(-1).view(torch.uint8))
         views_d.append(in_d[o:o + nb].view(t.dtype).view(t.shape))
     q_d, kn_d, vn_d, tb_d, ln_d, ps_d = views_d
-    out_h = torch.empty_like(out, device="cpu").pin_memory()
-    h2d = total
-    d2h = out.numel() * out.element_size()
+    out_h2 = torch.empty_like(out, device="cpu").pin_memory()
 
-    def e2e_body():
+    def e2e_copy_body():
         in_d.copy_(in_h, non_blocking=True)
         pkv.paged_decode_step(kn_d, vn_d, ps_d, q_d, w.k_pool, w.v_pool, tb_d, ln_d, w.scale,
                               out, ws, nw, variant=var)
-        out_h.copy_(out, non_blocking=True)
+        out_h2.copy_(out, non_blocking=True)
 
-    # The copy in, the step's three launches and the copy out are recorded
-    # once into a CUDA graph; each step replays it and waits for the result.
-    e2e_body()
-    torch.cuda.synchronize()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(graph, stream=cap):
-            e2e_body()
-    stream.wait_stream(cap)
-    torch.cuda.synchronize()
-
-    def e2e_step():
-        graph.replay()
-        torch.cuda.current_stream(dev).synchronize()
-
-    for _ in range(10):
-        e2e_step()
-    KE = max(1, min(args.e2e_steps, K))
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(KE):
-        e2e_step()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / KE
-    e2e_ms = max_over_ranks(dist, e2e_ms, dev)
+    e2e_copy_ms = e2e_time(graph_of(e2e_copy_body))
     status = pkv.pkv_read_device_status(ws)
 
     value = aggregate_gbs(world, by["step"], ms_step)
@@ -858,10 +879,17 @@ def run_ours(args):
                      "decode_kernel_ms_l2_flushed": dec_avg_flushed,
                      "frac_l2_flushed": by["decode"] / (dec_avg_flushed * 1e-3) / 1e9 / peak},
         "e2e": {"value": aggregate_gbs(world, by["step"], e2e_ms), "unit": UNIT,
-                "mode": "CUDA graph replay per step: packed pinned inputs in, "
-                        "paged_decode_step, output out, then a host sync",
+                "mode": "CUDA graph replay per step of paged_decode_step_host (the step's "
+                        "inputs in pinned host memory, read by the plan launch across the "
+                        "host-device link; the output stored by the kernels into pinned host "
+                        "memory), then a host sync",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": KE},
+                "steps": KE, "device_status": host_status,
+                "copy_engine": {"value": aggregate_gbs(world, by["step"], e2e_copy_ms),
+                                "unit": UNIT, "ms_per_step": e2e_copy_ms,
+                                "mode": "CUDA graph replay per step: the packed pinned inputs "
+                                        "copied in, paged_decode_step, the output copied out, "
+                                        "then a host sync"}},
         "rope_step": {"value": aggregate_gbs(world, by["step"], rope_ms), "unit": UNIT,
                       "ms_per_step": rope_ms, "steps": KR, "rope_theta": rope_theta,
                       "ms_per_step_with_qk_norm": rope_norm_ms,

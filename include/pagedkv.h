@@ -433,6 +433,44 @@ pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const in
                                   int num_workers, pkv_decode_variant variant,
                                   pkv_stream stream);
 
+/* paged_decode_step with the step's inputs and its output in page-locked host
+ * memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister, or a pinned torch
+ * tensor): k_new, v_new, positions, q, page_table, context_lens and out are
+ * HOST pointers; k_pool, v_pool and workspace are device memory as before.
+ * No copy engine is used: the plan launch reads the lengths, the new rows,
+ * the positions and the table straight from host memory (the append writes
+ * the pools as in paged_decode_step) while extra CTAs of the same launch copy
+ * q and the page table into the workspace; the decode and combine kernels
+ * read those copies and store the result straight into `out`.  On a
+ * Grace-Blackwell system these accesses cross NVLink-C2C.  The result is in
+ * `out` once the stream's work is done (e.g. after cudaStreamSynchronize);
+ * the inputs must stay unchanged until then.  Outputs are bitwise those of
+ * paged_decode_step on device copies of the same inputs (same kernels, same
+ * schedule).  Each host range is checked at its first and last byte
+ * (page-locked, mapped for the current device, contiguous): else INVALID_ARG
+ * and nothing is launched.  ws_bytes >= paged_decode_step_host_workspace_size
+ * (...) (else WORKSPACE).  Other arguments and errors as for
+ * paged_decode_step.  (CacheIR, "Compiler Example": the new K/V are written
+ * into the cache, then paged_attention_decode runs; the host-buffer form is
+ * this library's.)  Three launches. */
+pkv_status paged_decode_step_host(const void* k_new, const void* v_new, const int32_t* positions,
+                                  const void* q, void* k_pool, void* v_pool,
+                                  const int32_t* page_table, int table_stride,
+                                  const int32_t* context_lens, int batch, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                  pkv_dtype dtype, float scale, void* out, void* workspace,
+                                  size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                                  pkv_stream stream);
+
+/* Bytes of the workspace of paged_decode_step_host: the decode's own
+ * (paged_decode_workspace_size) followed by room for q [batch][n_q_heads]
+ * [head_dim] and the page table [batch][table_stride], each from a 256-byte
+ * boundary.  Same shape errors as paged_decode_workspace_size;
+ * table_stride <= 0 is INVALID_ARG. */
+pkv_status paged_decode_step_host_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                                 int head_dim, int table_stride, int num_workers,
+                                                 pkv_decode_variant variant, size_t* bytes);
+
 /* ------------------------------------------------------------------------
  * Shared-prefix decode (CacheIR, "Current Capabilities": batched decode over
  * shared page tables; Experimental LibTorch prefix cache, "Short shared prefix

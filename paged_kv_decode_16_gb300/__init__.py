@@ -28,6 +28,7 @@ __all__ = [
     "check_bounded_wait",
     "paged_decode_plan", "paged_decode_run", "paged_decode_combine", "paged_decode_attention",
     "paged_decode_step", "paged_decode_attention_no_alloc", "NO_ALLOC_SCRATCH_BYTES",
+    "paged_decode_step_host", "paged_decode_step_host_workspace_size", "alloc_step_host_workspace",
     "pkv_read_device_status", "pkv_read_no_alloc_status", "alloc_workspace", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
     "VARIANT_AUTO", "VARIANT_CUDA_CORES", "VARIANT_TENSOR_CORES", "VARIANT_TCGEN05",
 ]
@@ -115,6 +116,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
                                V], I),
         "paged_decode_attention_no_alloc": ([V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, I, I,
                                              V], I),
+        "paged_decode_step_host": ([V, V, V, V, V, V, V, I, V, I, I, I, I, I, I, I, F, V, V, Z, I,
+                                    I, V], I),
+        "paged_decode_step_host_workspace_size": ([I, I, I, I, I, I, I, ctypes.POINTER(Z)], I),
         "pkv_read_device_status": ([V, ctypes.POINTER(ctypes.c_uint32)], I),
         "pkv_read_no_alloc_status": ([ctypes.POINTER(ctypes.c_uint32)], I),
     }
@@ -609,6 +613,81 @@ def paged_decode_step(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch
         _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
         float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(num_workers),
         int(variant), _stream(stream)), "paged_decode_step")
+    return out
+
+
+def _host(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    """A contiguous pinned (page-locked) CPU tensor (of dtype / ndim when
+    given), else raise.  The library checks the pages themselves again."""
+    try:
+        ok = (not t.is_cuda and t.is_contiguous() and t.is_pinned()
+              and (dtype is None or t.dtype == dtype) and (ndim is None or t.dim() == ndim))
+    except AttributeError:
+        raise TypeError(f"{name} must be a torch tensor") from None
+    if ok:
+        return t
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor (tensor.pin_memory())")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def paged_decode_step_host_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int,
+                                          head_dim: int, table_stride: int, num_workers: int = 0,
+                                          variant: int = VARIANT_AUTO) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().paged_decode_step_host_workspace_size(
+        batch, n_q_heads, n_kv_heads, head_dim, table_stride, num_workers, variant,
+        ctypes.byref(n)), "paged_decode_step_host_workspace_size")
+    return n.value
+
+
+def alloc_step_host_workspace(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                              table_stride: int, num_workers: int = 0, device=None,
+                              variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """A torch uint8 device buffer of the size paged_decode_step_host needs."""
+    n = paged_decode_step_host_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                              table_stride, num_workers, variant)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_step_host(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
+                           q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           page_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: torch.Tensor, workspace: torch.Tensor, num_workers: int = 0,
+                           stream=None, variant: int = VARIANT_AUTO) -> torch.Tensor:
+    """paged_decode_step with k_new, v_new, positions, q, page_table,
+    context_lens and out in pinned host memory (the pools and the workspace on
+    the device): the kernels read the inputs and write out across the
+    host-device link themselves.  out holds the result once the stream has
+    finished the step."""
+    _host(q, "q", None, 3)
+    dt = _dtype_code(q)
+    _dev(k_pool, "k_pool", q.dtype, 4)
+    _dev(v_pool, "v_pool", q.dtype, 4)
+    _dev(workspace, "workspace", torch.uint8)
+    _host(out, "out", q.dtype, 3)
+    _host(page_table, "page_table", torch.int32, 2)
+    _host(context_lens, "context_lens", torch.int32, 1)
+    _host(k_new, "k_new", q.dtype, 3)
+    _host(v_new, "v_new", q.dtype, 3)
+    _host(positions, "positions", torch.int32, 1)
+    B, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or out.shape != q.shape:
+        raise ValueError("q/out [B, Hq, D] and pools [NP, Hkv, P, D] disagree")
+    if page_table.shape[0] != B:
+        raise ValueError("page_table rows != batch")
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    _check(load_library().paged_decode_step_host(
+        _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        _ptr(page_table), page_table.shape[1], _ptr(context_lens), B, Hq, Hkv, D, P, NP, dt,
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(num_workers),
+        int(variant), _stream(stream)), "paged_decode_step_host")
     return out
 
 

@@ -397,7 +397,7 @@ pkv::PlanArgs plan_args(const int32_t* context_lens, const int32_t* table, int b
                         int page_size, int table_stride, int num_workers, void* workspace,
                         const DecodeSetup& s, int skip_cols = 0, int uniform_len = -1) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    pkv::PlanArgs pa;
+    pkv::PlanArgs pa = {};  // lens_host = 0: device lengths
     pa.lens = context_lens;
     pa.len_offset = skip_cols * page_size;
     pa.uniform_len = uniform_len;
@@ -531,7 +531,7 @@ pkv_status no_alloc_scratch(void** out) {
 pkv::AppendArgs make_append(const void* k_new, const void* v_new, const int32_t* positions,
                             const int32_t* table, int table_stride, void* k_pool, void* v_pool,
                             int n_kv_heads, int head_dim, int page_size, int num_pages) {
-    pkv::AppendArgs a;
+    pkv::AppendArgs a = {};  // host = 0: device inputs
     a.k_new = static_cast<const uint4*>(k_new);
     a.v_new = static_cast<const uint4*>(v_new);
     a.positions = positions;
@@ -923,6 +923,139 @@ pkv_status paged_decode_step_rope(const void* k_new, const void* v_new, const in
                      context_lens, batch, n_q_heads, n_kv_heads, head_dim, page_size, num_pages,
                      dtype, scale, true, rope_theta, q_norm_weight, k_norm_weight, norm_eps, out,
                      workspace, ws_bytes, num_workers, variant, stream);
+}
+
+}  // extern "C" (reopened below)
+
+namespace {
+// The device address of [p, p + bytes) in page-locked host memory (under
+// unified addressing the same number).  Its first and its last byte must both
+// be page-locked host memory mapped for the current device, the last at
+// distance bytes - 1 from the first; else INVALID_ARG and nothing launches.
+pkv_status host_range(const void* p, size_t bytes, const void** dev) {
+    if (!p) return PKV_ERR_INVALID_ARG;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return PKV_ERR_INVALID_ARG;
+    if (bytes > 1) {
+        cudaPointerAttributes e;
+        const char* last = static_cast<const char*>(p) + (bytes - 1);
+        if (cudaPointerGetAttributes(&e, last) != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_INVALID_ARG;
+        }
+        if (e.type != cudaMemoryTypeHost ||
+            static_cast<const char*>(e.devicePointer) !=
+                static_cast<const char*>(a.devicePointer) + (bytes - 1))
+            return PKV_ERR_INVALID_ARG;
+    }
+    *dev = a.devicePointer;
+    return PKV_OK;
+}
+
+// Workspace of a host-buffer step: the decode's own, then the device copies
+// of q and of the page table (each from a 256-byte boundary).
+struct HostStepLayout {
+    size_t q, table, total;
+};
+
+HostStepLayout host_step_layout(const DecodeSetup& s, int batch, int n_q_heads, int head_dim,
+                                int table_stride) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    HostStepLayout l;
+    l.q = up(s.ws.total);
+    l.table = l.q + up((size_t)batch * n_q_heads * head_dim * 2);
+    l.total = l.table + up((size_t)batch * table_stride * 4);
+    return l;
+}
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_decode_step_host_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                                 int head_dim, int table_stride, int num_workers,
+                                                 pkv_decode_variant variant, size_t* bytes) {
+    if (!bytes) return PKV_ERR_INVALID_ARG;
+    *bytes = 0;
+    pkv_status st = check_shapes(batch, n_q_heads, n_kv_heads, head_dim, 16);
+    if (st != PKV_OK) return st;
+    if (table_stride <= 0 || num_workers < 0 || !valid_variant(variant))
+        return PKV_ERR_INVALID_ARG;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, 16, PKV_BF16, num_workers,
+                           variant, &s)) != PKV_OK)
+        return st;
+    *bytes = host_step_layout(s, batch, n_q_heads, head_dim, table_stride).total;
+    return PKV_OK;
+}
+
+pkv_status paged_decode_step_host(const void* k_new, const void* v_new, const int32_t* positions,
+                                  const void* q, void* k_pool, void* v_pool,
+                                  const int32_t* page_table, int table_stride,
+                                  const int32_t* context_lens, int batch, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                  pkv_dtype dtype, float scale, void* out, void* workspace,
+                                  size_t ws_bytes, int num_workers, pkv_decode_variant variant,
+                                  pkv_stream stream) {
+    pkv_status st = validate_decode_args(q, k_pool, v_pool, page_table, table_stride,
+                                         context_lens, true, batch, n_q_heads, n_kv_heads,
+                                         head_dim, page_size, num_pages, dtype, scale, out,
+                                         workspace, ws_bytes, num_workers, variant);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!k_new || !v_new || !positions) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    const size_t row_bytes = (size_t)batch * n_kv_heads * head_dim * 2;
+    const size_t qo_bytes = (size_t)batch * n_q_heads * head_dim * 2;
+    const size_t table_bytes = (size_t)batch * table_stride * 4;
+    const size_t seq_bytes = (size_t)batch * 4;
+    if (overlaps(out, qo_bytes, k_new, row_bytes) || overlaps(out, qo_bytes, v_new, row_bytes) ||
+        overlaps(out, qo_bytes, positions, seq_bytes))
+        return PKV_ERR_ALIAS;
+    const void *q_h, *kn_h, *vn_h, *pos_h, *tab_h, *len_h, *out_h;
+    if ((st = host_range(q, qo_bytes, &q_h)) != PKV_OK ||
+        (st = host_range(k_new, row_bytes, &kn_h)) != PKV_OK ||
+        (st = host_range(v_new, row_bytes, &vn_h)) != PKV_OK ||
+        (st = host_range(positions, seq_bytes, &pos_h)) != PKV_OK ||
+        (st = host_range(page_table, table_bytes, &tab_h)) != PKV_OK ||
+        (st = host_range(context_lens, seq_bytes, &len_h)) != PKV_OK ||
+        (st = host_range(out, qo_bytes, &out_h)) != PKV_OK)
+        return st;
+    DecodeSetup s;
+    if ((st = setup_decode(batch, n_q_heads, n_kv_heads, head_dim, page_size, dtype, num_workers,
+                           variant, &s)) != PKV_OK)
+        return st;
+    const HostStepLayout hl = host_step_layout(s, batch, n_q_heads, head_dim, table_stride);
+    if (ws_bytes < hl.total) return PKV_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* q_dev = ws + hl.q;
+    int32_t* table_dev = reinterpret_cast<int32_t*>(ws + hl.table);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // the append reads its inputs from host memory; the staging CTAs copy q
+    // and the table next to the decode's workspace; the plan reads the lengths
+    pkv::AppendArgs a = make_append(kn_h, vn_h, static_cast<const int32_t*>(pos_h),
+                                    static_cast<const int32_t*>(tab_h), table_stride, k_pool,
+                                    v_pool, n_kv_heads, head_dim, page_size, num_pages);
+    a.host = 1;
+    pkv::PlanArgs pa = plan_args(static_cast<const int32_t*>(len_h), nullptr, batch, page_size,
+                                 table_stride, num_workers, workspace, s);
+    pa.lens_host = 1;
+    pkv::StageArgs sa = {};
+    sa.q_src = static_cast<const uint4*>(q_h);
+    sa.q_dst = static_cast<uint4*>(q_dev);
+    sa.q_vecs = (long long)(qo_bytes / 16);
+    sa.t_src = static_cast<const int32_t*>(tab_h);
+    sa.t_dst = table_dev;
+    sa.t_words = (long long)batch * table_stride;
+    if ((st = cuda_status(pkv::launch_plan(pa, &a, cs, &sa))) != PKV_OK) return st;
+    void* out_dev = const_cast<void*>(out_h);
+    if ((st = do_run(q_dev, k_pool, v_pool, table_dev, table_stride, batch, n_q_heads, n_kv_heads,
+                     head_dim, page_size, num_pages, dtype, scale, out_dev, workspace, s, false,
+                     cs)) != PKV_OK)
+        return st;
+    return do_combine(batch, n_q_heads, head_dim, dtype, out_dev, workspace, s, cs);
 }
 
 pkv_status paged_decode_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool,

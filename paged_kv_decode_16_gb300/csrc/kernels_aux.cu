@@ -16,21 +16,30 @@ namespace pkv {
 // Serving" knob list: KV-append kernel).  Returns PKV_DEV_* bits for a
 // skipped row (reported once per row, by its vector 0 of head 0).
 // ---------------------------------------------------------------------------
+// A caller input: from page-locked host memory with ld.global.cv (a line the
+// GPU may hold is fetched again), else a plain load.
+template <bool kHost, typename V>
+__device__ __forceinline__ V ld_input(const V* p) {
+    if constexpr (kHost) return __ldcv(p);
+    else return *p;
+}
+
+template <bool kHost>
 __device__ __forceinline__ uint32_t append_vec(const AppendArgs& a, long long idx) {
     const int vec = (int)(idx % a.vecs);
     const long long row = idx / a.vecs;  // b * Hkv + h
     const int b = (int)(row / a.n_kv_heads);
     const int h = (int)(row - (long long)b * a.n_kv_heads);
-    const int p = a.positions[b];
+    const int p = ld_input<kHost>(a.positions + b);
     if (p < 0) return 0;  // padded batch slot: never writes
     const int pi = p / a.page_size;
     if (pi >= a.table_stride) return (vec == 0 && h == 0) ? PKV_DEV_BAD_LEN : 0u;
-    const int page = a.table[(long long)b * a.table_stride + pi];
+    const int page = ld_input<kHost>(a.table + (long long)b * a.table_stride + pi);
     if (page < 0 || page >= a.num_pages) return (vec == 0 && h == 0) ? PKV_DEV_BAD_PAGE : 0u;
     const long long dst =
         (((long long)page * a.n_kv_heads + h) * a.page_size + p % a.page_size) * a.vecs + vec;
-    a.k_pool[dst] = a.k_new[row * a.vecs + vec];
-    a.v_pool[dst] = a.v_new[row * a.vecs + vec];
+    a.k_pool[dst] = ld_input<kHost>(a.k_new + row * a.vecs + vec);
+    a.v_pool[dst] = ld_input<kHost>(a.v_new + row * a.vecs + vec);
     return 0;
 }
 
@@ -264,8 +273,10 @@ __device__ void plan_cta(const PlanArgs& pa, int status_slots) {
         const int b = base + tid;
         int cnt = 0;
         if (b < pa.batch) {
-            long long L = (long long)(pa.uniform_len >= 0 ? pa.uniform_len : pa.lens[b]) -
-                          pa.len_offset;
+            const int len = pa.uniform_len >= 0 ? pa.uniform_len
+                             : pa.lens_host         ? __ldcv(pa.lens + b)
+                                                    : pa.lens[b];
+            long long L = (long long)len - pa.len_offset;
             if (L < 0) { L = 0; atomicOr(&flags, PKV_DEV_BAD_LEN); }
             if (L > pa.cap) { L = pa.cap; atomicOr(&flags, PKV_DEV_BAD_LEN); }
             pa.lens_eff[b] = (int32_t)L;
@@ -355,8 +366,35 @@ __device__ void plan_cta(const PlanArgs& pa, int status_slots) {
         pa.wstart[w] = seq_of(w < nw ? range_begin(w, sw, r) : T - 1);
 }
 
+// Staging copies of a host-buffer step (StageArgs), CTA c of sa.ctas: each
+// thread has kStageLoads loads from host memory in flight before it stores.
+constexpr int kStageLoads = 4;
+
+__device__ void stage_cta(const StageArgs& sa, int c) {
+    const long long stride = (long long)sa.ctas * blockDim.x;
+    const long long t0 = (long long)c * blockDim.x + threadIdx.x;
+    for (long long i = t0; i < sa.q_vecs; i += kStageLoads * stride) {
+        uint4 v[kStageLoads];
+#pragma unroll
+        for (int j = 0; j < kStageLoads; ++j)
+            if (i + j * stride < sa.q_vecs) v[j] = __ldcv(sa.q_src + i + j * stride);
+#pragma unroll
+        for (int j = 0; j < kStageLoads; ++j)
+            if (i + j * stride < sa.q_vecs) sa.q_dst[i + j * stride] = v[j];
+    }
+    for (long long i = t0; i < sa.t_words; i += kStageLoads * stride) {
+        int32_t v[kStageLoads];
+#pragma unroll
+        for (int j = 0; j < kStageLoads; ++j)
+            if (i + j * stride < sa.t_words) v[j] = __ldcv(sa.t_src + i + j * stride);
+#pragma unroll
+        for (int j = 0; j < kStageLoads; ++j)
+            if (i + j * stride < sa.t_words) sa.t_dst[i + j * stride] = v[j];
+    }
+}
+
 __global__ void __launch_bounds__(1024)
-plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
+plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas, StageArgs sa) {
     // No early trigger: the decode grid launches as this grid completes.  Let
     // in early, its CTAs all leave their dependency wait in the same instant,
     // which measured 0.5 us slower back to back and 8 us slower after a large
@@ -364,6 +402,10 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
     pdl_wait();
     if (blockIdx.x == 0) {
         plan_cta(pa, append_ctas);
+        return;
+    }
+    if ((int)blockIdx.x > append_ctas) {  // staging CTAs (host-buffer step)
+        stage_cta(sa, blockIdx.x - 1 - append_ctas);
         return;
     }
     __shared__ uint32_t flags;
@@ -375,9 +417,13 @@ plan_kernel(PlanArgs pa, AppendArgs aa, int append_ctas) {
         f = rope_append_cta(aa, pa.batch, aa.vecs * 8, blockIdx.x - 1, append_ctas, s_rope);
     } else {
         const long long total = (long long)pa.batch * aa.n_kv_heads * aa.vecs;
-        for (long long idx = (long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; idx < total;
-             idx += (long long)append_ctas * blockDim.x)
-            f |= append_vec(aa, idx);
+        const long long i0 = (long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+        const long long stride = (long long)append_ctas * blockDim.x;
+        if (aa.host) {
+            for (long long idx = i0; idx < total; idx += stride) f |= append_vec<true>(aa, idx);
+        } else {
+            for (long long idx = i0; idx < total; idx += stride) f |= append_vec<false>(aa, idx);
+        }
     }
     if (f) atomicOr(&flags, f);
     __syncthreads();
@@ -605,7 +651,7 @@ append_kernel(AppendArgs a, int batch, uint32_t* status) {
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long total = (long long)batch * a.n_kv_heads * a.vecs;
     if (idx >= total) return;
-    const uint32_t f = append_vec(a, idx);
+    const uint32_t f = append_vec<false>(a, idx);
     if (f) set_status(status, f);
 }
 
@@ -644,7 +690,8 @@ gather_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool
 // ---------------------------------------------------------------------------
 // host-side launchers (stream-ordered, no synchronisation)
 // ---------------------------------------------------------------------------
-cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream_t stream) {
+cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream_t stream,
+                        const StageArgs* stage) {
     AppendArgs aa = {};
     int append_ctas = 0;
     if (append) {
@@ -659,8 +706,17 @@ cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream
         }
         append_ctas = (int)(ctas < kMaxAppendCtas ? ctas : kMaxAppendCtas);
     }
-    return launch_pdl(plan_kernel, dim3(1 + append_ctas), dim3(1024), 0, stream, pa, aa,
-                      append_ctas);
+    StageArgs sa = {};
+    if (stage) {
+        sa = *stage;
+        // 16-byte units of the copies over kStageLoads loads per thread
+        const long long units = sa.q_vecs + (sa.t_words + 3) / 4;
+        const long long per_cta = 1024LL * kStageLoads;
+        const long long ctas = (units + per_cta - 1) / per_cta;
+        sa.ctas = (int)(ctas < 1 ? 1 : (ctas > kMaxStageCtas ? kMaxStageCtas : ctas));
+    }
+    return launch_pdl(plan_kernel, dim3(1 + append_ctas + sa.ctas), dim3(1024), 0, stream, pa, aa,
+                      append_ctas, sa);
 }
 
 cudaError_t launch_cascade_plan(const PlanArgs& ps, const PlanArgs& pv, const CascadeGather& g,

@@ -28,6 +28,7 @@ struct PlanArgs {
     const int32_t* table;  // page table (nullable), prefetched into L2 for the decode kernel
     int table_stride;
     int page_size;
+    int lens_host;         // lens in page-locked host memory (read with ld.global.cv)
 };
 
 struct AppendArgs {
@@ -50,7 +51,24 @@ struct AppendArgs {
     const void* k_norm_w;
     float norm_eps;
     double inv_freq[64];   // theta^(-2i/D), i < D/2 (computed on the host)
+    int host;              // k_new, v_new, positions, table in page-locked host memory
 };
+
+// Copies of host-resident step inputs into device memory, run by extra CTAs
+// of the plan launch (a host-buffer step: the decode reads q and the page
+// table from these copies, issued after the launch's dependency wait).
+// Sources are page-locked host memory read with ld.global.cv; zero counts
+// copy nothing.
+struct StageArgs {
+    const uint4* q_src;    // q as 16-byte vectors
+    uint4* q_dst;
+    long long q_vecs;
+    const int32_t* t_src;  // page table as 4-byte words
+    int32_t* t_dst;
+    long long t_words;
+    int ctas;              // CTAs of the launch doing the copies (set by launch_plan)
+};
+constexpr int kMaxStageCtas = 64;
 
 // Shared memory of a rotary + append pass: the cos / sin table (one angle per
 // thread) and the two norm weight rows.
@@ -60,8 +78,10 @@ constexpr int kRopeSmemFloats = 2 * 1024 + 2 * 128;
 // (one angle per thread: 1024 / (D / 2)), and their cos / sin table.
 constexpr int kRopeThreads = 1024;
 
-// Plan, optionally with the append fused into the same launch.
-cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream_t stream);
+// Plan, optionally with the append and the staging copies fused into the
+// same launch.
+cudaError_t launch_plan(const PlanArgs& pa, const AppendArgs* append, cudaStream_t stream,
+                        const StageArgs* stage = nullptr);
 
 cudaError_t launch_combine(pkv_dtype dtype, int head_dim, const float* partials,
                            const int32_t* prefix, const int32_t* lens_eff, const WsHeader* hdr,

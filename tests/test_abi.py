@@ -266,6 +266,33 @@ def test_rope_entry_points_check_theta_on_host(lib):
         lib.kv_pool_destroy(h)
 
 
+def test_host_step_checks_on_host(lib):
+    """paged_decode_step_host: the decode checks, then k_new / v_new /
+    positions, aliasing of out, and page-locked host memory for every host
+    argument (the fake addresses here are not), all before any launch."""
+    V = ctypes.c_void_p
+
+    def step(batch=2, k_new=A * 30, out=A * 26, ws_bytes=1 << 20, stride=4):
+        return lib.paged_decode_step_host(V(k_new), V(A * 31), V(A * 32), V(A), V(A * 8),
+                                          V(A * 16), V(A * 24), stride, V(A * 25), batch, 8, 2,
+                                          128, 16, 8, BF16, ctypes.c_float(0.088), V(out),
+                                          V(A * 27), ws_bytes, 0, 0, None)
+    assert step(batch=0) == OK
+    assert step(batch=-1) == INVALID
+    assert step(stride=0) == INVALID
+    assert step(k_new=0) == INVALID
+    assert step(k_new=A * 30 + 8) == INVALID      # not 16-byte aligned
+    assert step(out=A * 30) == ALIAS              # out over k_new
+    assert step(out=A * 27) == ALIAS              # out over the workspace
+    assert step() == INVALID                      # not page-locked host memory
+    n = ctypes.c_size_t(7)
+    assert lib.paged_decode_step_host_workspace_size(2, 8, 2, 128, 0, 0, 0, ctypes.byref(n)) \
+        == INVALID and n.value == 0
+    assert lib.paged_decode_step_host_workspace_size(2, 8, 2, 96, 4, 0, 0, ctypes.byref(n)) \
+        == UNSUPPORTED
+    assert lib.paged_decode_step_host_workspace_size(2, 8, 2, 128, 4, 0, 0, None) == INVALID
+
+
 def test_no_alloc_status_reader_rejects_null(lib):
     assert lib.pkv_read_no_alloc_status(None) == INVALID
 
