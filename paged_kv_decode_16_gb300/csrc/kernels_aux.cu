@@ -30,6 +30,9 @@ __device__ __forceinline__ uint32_t append_vec(const AppendArgs& a, long long id
     const long long row = idx / a.vecs;  // b * Hkv + h
     const int b = (int)(row / a.n_kv_heads);
     const int h = (int)(row - (long long)b * a.n_kv_heads);
+    // the new rows' loads go out with the position's (independent of it)
+    const uint4 kv = ld_input<kHost>(a.k_new + row * a.vecs + vec);
+    const uint4 vv = ld_input<kHost>(a.v_new + row * a.vecs + vec);
     const int p = ld_input<kHost>(a.positions + b);
     if (p < 0) return 0;  // padded batch slot: never writes
     const int pi = p / a.page_size;
@@ -38,8 +41,8 @@ __device__ __forceinline__ uint32_t append_vec(const AppendArgs& a, long long id
     if (page < 0 || page >= a.num_pages) return (vec == 0 && h == 0) ? PKV_DEV_BAD_PAGE : 0u;
     const long long dst =
         (((long long)page * a.n_kv_heads + h) * a.page_size + p % a.page_size) * a.vecs + vec;
-    a.k_pool[dst] = ld_input<kHost>(a.k_new + row * a.vecs + vec);
-    a.v_pool[dst] = ld_input<kHost>(a.v_new + row * a.vecs + vec);
+    a.k_pool[dst] = kv;
+    a.v_pool[dst] = vv;
     return 0;
 }
 
@@ -368,7 +371,7 @@ __device__ void plan_cta(const PlanArgs& pa, int status_slots) {
 
 // Staging copies of a host-buffer step (StageArgs), CTA c of sa.ctas: each
 // thread has kStageLoads loads from host memory in flight before it stores.
-constexpr int kStageLoads = 4;
+constexpr int kStageLoads = 1;
 
 __device__ void stage_cta(const StageArgs& sa, int c) {
     const long long stride = (long long)sa.ctas * blockDim.x;
