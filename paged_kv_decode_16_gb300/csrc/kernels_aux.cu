@@ -550,6 +550,67 @@ struct CascadeSegs {
     }
 };
 
+// The shared-prefix merge of units of at most kCombineWarps / 2 rows and at
+// most 2 * kPairBlock segments: two warps per row, warp w taking row
+// w % nrows and half w / nrows of the segments (the first ceil(ns / 2), or
+// the rest).  Each warp issues its half's o loads together with the row's m
+// and l loads (lane s: segment s), forms the row's maximum and denominator
+// (both warps of a row the same bits), and sums its half in segment order;
+// the second half's sum is then added to the first's, through shared memory.
+// One round of loads per row instead of one plus one per 8 segments.
+constexpr int kPairBlock = 16;
+
+template <typename T, int D, class Segs, class RowOut>
+__device__ __forceinline__ void merge_rows_pair(const Segs& sg, int ns, int nrows, int warp,
+                                                int lane, float4* s_half,
+                                                const RowOut& out_rows) {
+    constexpr int Q = D / 4;
+    static_assert(Q <= 32, "one vector per lane");
+    const bool active = warp < 2 * nrows;
+    const int g = active ? warp % nrows : 0;
+    const int half = active ? warp / nrows : 0;
+    const int h0 = (ns + 1) >> 1;
+    const int s0 = half ? h0 : 0, s1 = half ? ns : h0;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (active) {
+        const float m = lane < ns ? __ldcg(sg.m(lane, g)) : -INFINITY;
+        const float l = lane < ns ? __ldcg(sg.l(lane, g)) : 0.f;
+        float4 v[kPairBlock];
+#pragma unroll
+        for (int j = 0; j < kPairBlock; ++j)
+            v[j] = lane < Q && s0 + j < s1 ? __ldcg(sg.o4(s0 + j, g, lane))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const float wl = merge_weight(m, M);
+        den = fmaf(wl, l, 0.f);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+#pragma unroll
+        for (int j = 0; j < kPairBlock; ++j) {
+            const float w = __shfl_sync(kFull, wl, (s0 + j) & 31);
+            if (s0 + j < s1) {
+                x.x = fmaf(w, v[j].x, x.x);
+                x.y = fmaf(w, v[j].y, x.y);
+                x.z = fmaf(w, v[j].z, x.z);
+                x.w = fmaf(w, v[j].w, x.w);
+            }
+        }
+        if (half == 1 && lane < Q) s_half[g * 32 + lane] = x;
+    }
+    __syncthreads();
+    if (active && half == 0 && lane < Q) {
+        const float4 y = s_half[g * 32 + lane];
+        x.x += y.x;
+        x.y += y.y;
+        x.z += y.z;
+        x.w += y.w;
+        merge_store<T, D>(x, den, lane, out_rows(g));
+    }
+}
+
 // kUmma: the prefix pass ran on the tensor-core row tiles (prefix_umma.cu);
 // else as a virtual decode of gs_v-row units.
 template <typename T, int D, bool kUmma>
@@ -580,8 +641,15 @@ cascade_combine_kernel(CascadeArgs c) {
         const CascadeSegs<TileSegs> sg{
             TileSegs{c.v_partials, (long long)(h * c.v_tiles + t) * c.v_splits, D}, ro,
             c.v_splits, suf};
-        merge_rows_seq<T, D>(sg, c.v_splits + ns, gs, threadIdx.x >> 5, kCombineWarps,
-                             threadIdx.x & 31, [&](int g) { return o + (long long)g * D; });
+        const int nseg = c.v_splits + ns;
+        if (2 * gs <= kCombineWarps && nseg <= 2 * kPairBlock) {
+            __shared__ float4 s_half[(kCombineWarps / 2) * 32];
+            merge_rows_pair<T, D>(sg, nseg, gs, threadIdx.x >> 5, threadIdx.x & 31, s_half,
+                                  [&](int g) { return o + (long long)g * D; });
+        } else {
+            merge_rows_seq<T, D>(sg, nseg, gs, threadIdx.x >> 5, kCombineWarps,
+                                 threadIdx.x & 31, [&](int g) { return o + (long long)g * D; });
+        }
     } else {
         // the virtual unit holding this unit's rows
         const int vu = h * c.v_sub + r0 / c.v_gs, ro = r0 % c.v_gs;
