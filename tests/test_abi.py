@@ -321,3 +321,14 @@ def test_binding_rejects_operands_on_another_device(monkeypatch):
         pkv._dev(t, "q", torch.bfloat16, 3)
     monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
     assert pkv._dev(t, "q", torch.bfloat16, 3) is t
+
+
+def test_host_step_binding_wants_pinned_host_tensors():
+    """paged_decode_step_host's binding refuses CPU tensors that are not
+    page-locked (and CUDA tensors where host memory is expected) before any
+    call into the library."""
+    import torch
+    t = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    assert not t.is_pinned()
+    with pytest.raises(ValueError, match="pinned host tensor"):
+        pkv.paged_decode_step_host(t, t, t, t, t, t, t, t, 0.125, t, t)
