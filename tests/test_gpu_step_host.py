@@ -133,6 +133,31 @@ def test_host_step_sees_new_host_inputs_each_call():
     assert pkv.pkv_read_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("dtype,D,P", [(torch.float16, 64, 32), (torch.bfloat16, 128, 16)])
+def test_host_step_empty_sequences_and_odd_shapes(dtype, D, P):
+    """Empty sequences (their rows zeroed straight into host memory), lengths
+    around page and chunk edges, group 6: host step == device step, bit for
+    bit, and the oracle."""
+    lens = [0, 1, 15, 16, 17, 0, 33, 64, 65, 200]
+    w1 = wl.make_random(31, batch=len(lens), n_q_heads=12, n_kv_heads=2, head_dim=D,
+                        page_size=P, dtype=dtype, lens=lens, device="cuda")
+    w2 = wl.make_random(31, batch=len(lens), n_q_heads=12, n_kv_heads=2, head_dim=D,
+                        page_size=P, dtype=dtype, lens=lens, device="cuda")
+    before = (wl.to_bits(w2.k_pool), wl.to_bits(w2.v_pool))
+    ws1 = pkv.alloc_workspace(w1.batch, w1.n_q_heads, w1.n_kv_heads, w1.head_dim)
+    ref = _device_step(w1, ws1)
+    h = _host_args(w2)
+    ws2 = pkv.alloc_step_host_workspace(w2.batch, w2.n_q_heads, w2.n_kv_heads, w2.head_dim,
+                                        w2.page_table.shape[1])
+    out = _host_step(w2, h, ws2)
+    assert pkv.pkv_read_device_status(ws2) == 0
+    assert torch.equal(_bits(out), _bits(ref))
+    assert not (out[0] != 0).any() and not (out[5] != 0).any()  # empty: zeros, not the NaN fill
+    # per-element bound: a 1-token sequence returns its V row, where bf16 rounding
+    # alone exceeds the absolute 2e-3 of the named workloads
+    assert_close(out.cuda(), oracle_full(w2, before, append=True), what="odd")
+
+
 def test_host_step_reports_bad_page_and_bad_position():
     """A page id outside the pool in a host table row and a position beyond
     the row: flagged in the device status like the device step, nothing
