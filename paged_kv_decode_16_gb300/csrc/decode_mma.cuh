@@ -335,14 +335,16 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                 }
                 __syncwarp();
             }
-            // ---- S = Q K^T : two n-tiles (tokens 0-7, 8-15), even/odd k chains ----
-            float s[TILES][2][2][4];
+            // ---- S = Q K^T : two n-tiles (tokens 0-7, 8-15); one tile: even/odd k
+            // chains, two tiles: the tiles' chains interleave (one chain each) ----
+            constexpr int KCH = TILES == 1 ? 2 : 1;
+            float s[TILES][2][KCH][4];
 #pragma unroll
             for (int t = 0; t < TILES; ++t)
 #pragma unroll
                 for (int a = 0; a < 2; ++a)
 #pragma unroll
-                    for (int b = 0; b < 2; ++b)
+                    for (int b = 0; b < KCH; ++b)
                         s[t][a][b][0] = s[t][a][b][1] = s[t][a][b][2] = s[t][a][b][3] = 0.f;
             // ldmatrix x4 rows: lane -> matrix mi = lane/8, row r = lane%8;
             // matrices: (tok 0-7, d+0..7), (tok 0-7, d+8..15), (tok 8-15, d+0..7), (tok 8-15, d+8..15)
@@ -367,8 +369,8 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
                         uint32_t qf[4];
                         ldsm_x4(smem_u32(sq) + qrow * kQRowBytes + (kk * 16 + (mi >> 1) * 8) * 2,
                                 qf);
-                        Mma<T>::run(s[t][0][kk & 1], qf, kb[0], kb[1]);
-                        Mma<T>::run(s[t][1][kk & 1], qf, kb[2], kb[3]);
+                        Mma<T>::run(s[t][0][kk % KCH], qf, kb[0], kb[1]);
+                        Mma<T>::run(s[t][1][kk % KCH], qf, kb[2], kb[3]);
                     }
                 }
             }
@@ -392,7 +394,9 @@ decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int tt = a * 8 + tq + (e & 1);
-                        const float v = (s[t][a][0][e] + s[t][a][1][e]) * p.scale_log2;
+                        const float v =
+                            (KCH == 2 ? s[t][a][0][e] + s[t][a][KCH - 1][e] : s[t][a][0][e]) *
+                            p.scale_log2;
                         sc[a][e] = (tt < nvalid && tt <= (e < 2 ? lim_lo : lim_hi)) ? v : -INFINITY;
                     }
                 {
