@@ -332,3 +332,24 @@ def test_host_step_binding_wants_pinned_host_tensors():
     assert not t.is_pinned()
     with pytest.raises(ValueError, match="pinned host tensor"):
         pkv.paged_decode_step_host(t, t, t, t, t, t, t, t, 0.125, t, t)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    """include/pagedkv.h is a C header: a C99 translation unit that includes it
+    and names every declared function compiles with -pedantic, no warnings."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    names = declared_functions()
+    src = tmp_path / "uses_header.c"
+    src.write_text('#include "pagedkv.h"\n'
+                   "typedef void (*any_fn)(void);\n"
+                   "any_fn pkv_symbols[] = {\n" +
+                   "".join(f"    (any_fn)&{n},\n" for n in names) +
+                   "};\n")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-fsyntax-only", "-I", os.path.dirname(HEADER), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
